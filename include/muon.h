@@ -1,0 +1,185 @@
+/*
+ * libmuon — the Muon optimizer step on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * One call, muon_step(), updates every registered 2-D weight matrix:
+ *
+ *   1. momentum      M <- beta*M + G ; U = G + beta*M (Nesterov) or U = M
+ *   2. normalise     X0 = U / (||U||_F + 1e-7), oriented short side first
+ *                    (a matrix with rows > cols is processed as U^T)
+ *   3. orthogonalise ns_steps quintic Newton-Schulz iterations, three
+ *                    products each: A = X X^T, B = b A + c A A, X <- a X + B X
+ *   4. update        W <- W - lr * max(1, rows/cols)^0.5 * O, O = X (or X^T)
+ *
+ * Sources: "Advancing Emerging Optimizers for Accelerated LLM Training"
+ * (NVIDIA developer blog, 22 Apr 2026, and its summaries).  Section
+ * "Distributed Newton-Schulz": the optimizer needs each layer's whole
+ * momentum-buffer matrix; section "Duplicated mode": the iteration runs
+ * "usually five" times per update and the weights are then updated with the
+ * orthogonalised momentum; section "Distributed mode": three matrix products
+ * per iteration; section "SYRK and fused all-reduce": the first two products
+ * are symmetric rank-k updates that compute only the upper-triangle tiles
+ * (diagonal tiles in full) and write the full, mirrored matrix; section
+ * "Blockwise mode": each locally held block is orthogonalised and updated on
+ * its own, with no communication; section "Load balancing": matrices differ
+ * in cost, so work is balanced by estimated cost rather than round-robin.
+ * The momentum form, the normalisation, the orientation rule and the shape
+ * scale are not written out on the pages; the library takes the plain
+ * readings listed above.
+ *
+ * Conventions for every entry point
+ *   - Return value: MUON_OK (0) or a negative MUON_ERR_* code.  The text of
+ *     the last error of a handle is available from muon_last_error().
+ *   - All argument checks run before any GPU work is queued, so a call that
+ *     returns an error has changed no memory.
+ *   - Pointers named "device" are CUDA device addresses on the handle's
+ *     device; nothing is copied from or to the host unless stated.
+ *   - GPU work is queued on the handle's stream and runs asynchronously;
+ *     errors raised on the GPU surface at muon_sync().
+ *   - Results are deterministic: the same inputs give bit-identical outputs
+ *     from run to run, and a matrix gives the same bits whether it is stepped
+ *     alone or together with others.
+ *   - A handle is not thread-safe; use one handle per host thread.
+ */
+#ifndef LIBMUON_MUON_H
+#define LIBMUON_MUON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MUON_API __attribute__((visibility("default")))
+#else
+#define MUON_API
+#endif
+
+/* error codes */
+#define MUON_OK                    0
+#define MUON_ERR_INVALID_ARG      -1  /* null pointer, bad size, bad enum   */
+#define MUON_ERR_UNSUPPORTED      -2  /* shape or dtype the library rejects */
+#define MUON_ERR_NO_WORKSPACE     -3  /* no workspace, or too small         */
+#define MUON_ERR_CUDA             -4  /* a CUDA runtime/driver call failed  */
+#define MUON_ERR_TIMEOUT          -5  /* a bounded wait on the GPU ran out  */
+#define MUON_ERR_STATE            -6  /* call out of order (e.g. no params) */
+
+/* element types */
+#define MUON_F32   0
+#define MUON_BF16  1
+
+/* orthogonalisation modes */
+#define MUON_FULL       0   /* each registered matrix as a whole            */
+#define MUON_BLOCKWISE  1   /* nb equal column blocks, each on its own      */
+
+typedef struct muon_ctx* muon_handle;
+
+/* One 2-D parameter.  w, g and m are device pointers to row-major matrices
+ * of rows x cols elements with leading dimensions ld_w, ld_g, ld_m (in
+ * elements, >= cols).  w is updated in place (w_dtype: MUON_BF16 or
+ * MUON_F32), g is read only (g_dtype: MUON_BF16 or MUON_F32), m is the fp32
+ * momentum buffer, updated in place.  The caller owns all three and keeps
+ * them valid while they are registered.  1 <= rows, cols <= 1048576 and
+ * min(rows, cols) <= 32768 (the m x m intermediates stay addressable). */
+typedef struct {
+    void*       w;
+    const void* g;
+    float*      m;
+    int64_t     rows, cols;
+    int64_t     ld_w, ld_g, ld_m;
+    int32_t     w_dtype, g_dtype;
+} muon_param;
+
+/* Creates a handle bound to CUDA device `device` and stream `cuda_stream`
+ * (a cudaStream_t; NULL = the legacy default stream).  Allocates no device
+ * memory.  *out receives the handle.  device = MUON_HOST_ONLY gives a handle
+ * that makes no CUDA call at all: it registers parameters (pointers are not
+ * dereferenced) and answers muon_workspace_size / muon_get_plan_info, while
+ * muon_step and muon_sync return MUON_ERR_STATE. */
+#define MUON_HOST_ONLY (-1)
+MUON_API int muon_create(muon_handle* out, int device, void* cuda_stream);
+
+/* Replaces the stream that later calls queue their work on. */
+MUON_API int muon_set_stream(muon_handle h, void* cuda_stream);
+
+/* Registers n >= 1 parameters (copied; the array may be freed afterwards),
+ * replacing any previous set.  Invalidates the current plan. */
+MUON_API int muon_register_params(muon_handle h, int n, const muon_param* params);
+
+/* Workspace the step needs for `mode` / `nb` with the registered set.
+ * *min_bytes: enough to run the step one group of matrices at a time
+ * (the largest single matrix or block plus the plan's tables);
+ * *full_bytes: enough to run every matrix in a single group.  Any size in
+ * between works; larger sizes give fewer, larger groups.  In blockwise mode
+ * nb must divide every registered cols (MUON_ERR_UNSUPPORTED otherwise). */
+MUON_API int muon_workspace_size(muon_handle h, int mode, int nb, size_t* min_bytes,
+                        size_t* full_bytes);
+
+/* Hands the library a caller-owned device buffer of `bytes` bytes (start
+ * aligned to 1024 bytes) to hold the plan's tables and all intermediate
+ * matrices.  The library never allocates device memory itself.  The buffer
+ * must stay valid until replaced or the handle is destroyed. */
+MUON_API int muon_set_workspace(muon_handle h, void* dptr, size_t bytes);
+
+/* One Muon step over all registered parameters.
+ *   lr, beta, nesterov   learning rate, momentum factor, Nesterov on/off
+ *   ns_steps             Newton-Schulz iterations (1..64; 5 is usual)
+ *   a, b, c              coefficients of a X + (b A + c A A) X
+ *   mode, nb             MUON_FULL (nb ignored) or MUON_BLOCKWISE with nb
+ *                        column blocks (nb >= 1 dividing every cols)
+ * The first step after registering params, changing the workspace, the mode
+ * or nb builds the plan and uploads its tables (host work plus one copy);
+ * later steps only queue kernels.  Returns once the work is queued. */
+MUON_API int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
+              float a, float b, float c, int mode, int nb);
+
+/* Waits for the handle's stream and reports any error raised on the GPU
+ * (MUON_ERR_TIMEOUT when a bounded wait ran out, MUON_ERR_CUDA otherwise). */
+MUON_API int muon_sync(muon_handle h);
+
+/* Releases the handle (no device memory is owned, none is freed). */
+MUON_API int muon_destroy(muon_handle h);
+
+/* Text of the handle's last error ("" if none).  Valid until the next call
+ * on the handle.  h may be NULL (returns the last create error). */
+MUON_API const char* muon_last_error(muon_handle h);
+
+/* ---- measurement and validation helpers ------------------------------- */
+
+/* Stage timing.  When on, muon_step records CUDA events around each kind of
+ * launch on the handle's stream; muon_stage_times() (after muon_sync) fills
+ * up to `n` totals in milliseconds for the last step, in the order
+ * momentum, norm, normalise, syrk1, syrk2, gemm, update, and the number of
+ * launches of each kind into `launches` (may be NULL).  Returns the number
+ * of stages written. */
+#define MUON_N_STAGES 7
+MUON_API int muon_set_profiling(muon_handle h, int on);
+MUON_API int muon_stage_times(muon_handle h, float* ms, int* launches, int n);
+
+/* Number of kernel launches the last muon_step queued. */
+MUON_API int muon_last_launch_count(muon_handle h);
+
+/* Optional exports written by the update stage of every later step, for
+ * parameter i (0 <= i < n): w_f32[i] receives the updated weight in fp32
+ * before it is stored in the weight's dtype, o_bf16[i] the orthogonalised
+ * update O in bf16; both rows x cols row-major with leading dimension cols,
+ * in the weight's orientation.  Entries (or whole arrays) may be NULL.
+ * n = 0 turns exports off.  Changing exports rebuilds the plan. */
+MUON_API int muon_debug_set_exports(muon_handle h, int n, float* const* w_f32,
+                           void* const* o_bf16);
+
+/* Plan statistics for `mode`/`nb`: number of units (matrices or blocks),
+ * groups, and tiles of the symmetric-product and GEMM stages. */
+typedef struct {
+    int64_t units, groups, syrk_tiles, gemm_tiles, ew_tiles;
+    /* per Newton-Schulz iteration, all units: useful = upper-triangle
+     * symmetric products + the GEMM; executed = what the tiles compute */
+    int64_t useful_flops, executed_flops;
+} muon_plan_info;
+MUON_API int muon_get_plan_info(muon_handle h, int mode, int nb, muon_plan_info* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LIBMUON_MUON_H */

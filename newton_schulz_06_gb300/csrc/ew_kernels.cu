@@ -1,0 +1,306 @@
+// Element-wise stages of the Muon step: momentum + sum of squares, the
+// per-unit Frobenius norm, normalisation into the short-side-first iterate
+// X0, and the weight update.  All four are bound by HBM bandwidth.
+//
+// Each CTA walks 64 x 64 tiles of a unit.  A tile is read in the weight's
+// orientation (coalesced, 16-byte vectors when aligned), staged in shared
+// memory, and processed in the X orientation (short side first), so that a
+// matrix and its transpose are reduced in exactly the same order and give
+// bit-identical norms and iterates.
+//
+// Readings (the pages, "Advancing Emerging Optimizers for Accelerated LLM
+// Training", name the momentum buffer and the orthogonalisation but not the
+// formulas): M <- beta*M + G; U = G + beta*M (Nesterov) else U = M;
+// X0 = U / (||U||_F + eps); W <- W - lr*scale*O.
+#include "muon_internal.h"
+#include "../../include/muon.h"
+
+namespace muon {
+namespace {
+
+__device__ __forceinline__ int find_unit(const EwUnit* __restrict__ units,
+                                         int n, int64_t t) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (units[mid].tile_base <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Loads `nval` (0..4) consecutive elements of type `dtype`; zero elsewhere.
+__device__ __forceinline__ void ld4(const void* base, int dtype, int64_t off,
+                                    int nval, bool vec, float (&v)[4]) {
+    if (dtype == MUON_F32) {
+        const float* p = static_cast<const float*>(base) + off;
+        if (vec && nval == 4) {
+            float4 q = *reinterpret_cast<const float4*>(p);
+            v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = e < nval ? p[e] : 0.f;
+        }
+    } else {
+        const __nv_bfloat16* p = static_cast<const __nv_bfloat16*>(base) + off;
+        if (vec && nval == 4) {
+            uint2 q = *reinterpret_cast<const uint2*>(p);
+            __nv_bfloat162 lo = *reinterpret_cast<__nv_bfloat162*>(&q.x);
+            __nv_bfloat162 hi = *reinterpret_cast<__nv_bfloat162*>(&q.y);
+            float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+            v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                v[e] = e < nval ? __bfloat162float(p[e]) : 0.f;
+        }
+    }
+}
+
+__device__ __forceinline__ void st4(void* base, int dtype, int64_t off,
+                                    int nval, bool vec, const float (&v)[4]) {
+    if (dtype == MUON_F32) {
+        float* p = static_cast<float*>(base) + off;
+        if (vec && nval == 4) {
+            *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) if (e < nval) p[e] = v[e];
+        }
+    } else {
+        __nv_bfloat16* p = static_cast<__nv_bfloat16*>(base) + off;
+        if (vec && nval == 4) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+            uint2 q;
+            q.x = *reinterpret_cast<uint32_t*>(&lo);
+            q.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(p) = q;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (e < nval) p[e] = __float2bfloat16_rn(v[e]);
+        }
+    }
+}
+
+struct TileGeom {
+    int u;
+    int xr0, xc0;     // tile origin in X orientation
+    int wr0, wc0;     // tile origin in W orientation
+};
+
+__device__ __forceinline__ TileGeom tile_geom(const EwUnit& U, int u,
+                                              int64_t t) {
+    TileGeom g;
+    g.u = u;
+    int64_t local = t - U.tile_base;
+    int tr = static_cast<int>(local / U.tiles_n);
+    int tc = static_cast<int>(local - static_cast<int64_t>(tr) * U.tiles_n);
+    g.xr0 = tr * EW_TILE;
+    g.xc0 = tc * EW_TILE;
+    g.wr0 = U.transposed ? g.xc0 : g.xr0;
+    g.wc0 = U.transposed ? g.xr0 : g.xc0;
+    return g;
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, off);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float s = 0.f;
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int w = 0; w < EW_THREADS / 32; ++w) s += red[w];
+    }
+    return s;   // valid in thread 0
+}
+
+// Pass 1: M <- beta*M + G, U as above; one fp32 sum of U^2 per tile.
+__global__ void __launch_bounds__(EW_THREADS)
+ew_momentum_kernel(const EwLaunch p) {
+    __shared__ float sU[EW_TILE][EW_TILE + 1];
+    __shared__ float red[EW_THREADS / 32];
+    const int i = threadIdx.x >> 4;          // 0..15
+    const int j4 = (threadIdx.x & 15) * 4;   // 0..60
+    for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        const int u = find_unit(p.units, p.num_units, t);
+        const EwUnit& U = p.units[u];
+        const TileGeom g = tile_geom(U, u, t);
+        const bool vec = U.vec_ok != 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = i + 16 * k;
+            const int wr = g.wr0 + r, wc = g.wc0 + j4;
+            int nval = (wr < U.rows) ? min(4, U.cols - wc) : 0;
+            nval = max(nval, 0);
+            float mv[4], gv[4], uv[4];
+            ld4(U.mom, MUON_F32, wr * U.ld_m + wc, nval, vec, mv);
+            ld4(U.g, U.g_dtype, wr * U.ld_g + wc, nval, vec, gv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                mv[e] = fmaf(p.beta, mv[e], gv[e]);
+                uv[e] = p.nesterov ? fmaf(p.beta, mv[e], gv[e]) : mv[e];
+                sU[r][j4 + e] = e < nval ? uv[e] : 0.f;
+            }
+            st4(U.mom, MUON_F32, wr * U.ld_m + wc, nval, vec, mv);
+        }
+        __syncthreads();
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int xr = i + 16 * k;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int xc = j4 + e;
+                const float v = U.transposed ? sU[xc][xr] : sU[xr][xc];
+                acc = fmaf(v, v, acc);
+            }
+        }
+        const float s = block_sum(acc, red);
+        if (threadIdx.x == 0) p.partial[t] = s;
+        __syncthreads();
+    }
+}
+
+// Per unit: ||U||_F from its tile sums in a fixed order (fp64), then
+// inv_norm = 1 / (||U|| + eps).  One warp per unit.
+__global__ void __launch_bounds__(256) ew_norm_kernel(const EwLaunch p) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= p.num_units) return;
+    const EwUnit& U = p.units[warp];
+    double s = 0.0;
+    for (int64_t k = lane; k < U.tile_count; k += 32)
+        s += static_cast<double>(p.partial[U.tile_base + k]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0)
+        p.inv_norm[warp] = static_cast<float>(1.0 / (sqrt(s) + (double)p.eps));
+}
+
+// Pass 2: X0 = bf16(U * inv_norm) in the X orientation.
+__global__ void __launch_bounds__(EW_THREADS)
+ew_normalise_kernel(const EwLaunch p) {
+    __shared__ float sU[EW_TILE][EW_TILE + 1];
+    const int i = threadIdx.x >> 4;
+    const int j4 = (threadIdx.x & 15) * 4;
+    for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        const int u = find_unit(p.units, p.num_units, t);
+        const EwUnit& U = p.units[u];
+        const TileGeom g = tile_geom(U, u, t);
+        const bool vec = U.vec_ok != 0;
+        const float inv = p.inv_norm[u];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = i + 16 * k;
+            const int wr = g.wr0 + r, wc = g.wc0 + j4;
+            int nval = (wr < U.rows) ? min(4, U.cols - wc) : 0;
+            nval = max(nval, 0);
+            float mv[4], gv[4];
+            ld4(U.mom, MUON_F32, wr * U.ld_m + wc, nval, vec, mv);
+            ld4(U.g, U.g_dtype, wr * U.ld_g + wc, nval, vec, gv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float uv = p.nesterov ? fmaf(p.beta, mv[e], gv[e]) : mv[e];
+                sU[r][j4 + e] = uv;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int xr = i + 16 * k;
+            const int gr = g.xr0 + xr, gc = g.xc0 + j4;
+            int nval = (gr < U.m) ? min(4, U.n - gc) : 0;
+            nval = max(nval, 0);
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int xc = j4 + e;
+                v[e] = (U.transposed ? sU[xc][xr] : sU[xr][xc]) * inv;
+            }
+            st4(U.x[0], MUON_BF16, static_cast<int64_t>(gr) * U.ld_x + gc,
+                nval, true, v);
+        }
+        __syncthreads();
+    }
+}
+
+// Update: W <- W - lr*scale*O with O read from the final iterate.
+__global__ void __launch_bounds__(EW_THREADS)
+ew_update_kernel(const EwLaunch p) {
+    __shared__ float sX[EW_TILE][EW_TILE + 1];
+    const int i = threadIdx.x >> 4;
+    const int j4 = (threadIdx.x & 15) * 4;
+    for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        const int u = find_unit(p.units, p.num_units, t);
+        const EwUnit& U = p.units[u];
+        const TileGeom g = tile_geom(U, u, t);
+        const bool vec = U.vec_ok != 0;
+        const __nv_bfloat16* X = U.x[p.src];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int xr = i + 16 * k;
+            const int gr = g.xr0 + xr, gc = g.xc0 + j4;
+            int nval = (gr < U.m) ? min(4, U.n - gc) : 0;
+            nval = max(nval, 0);
+            float v[4];
+            ld4(X, MUON_BF16, static_cast<int64_t>(gr) * U.ld_x + gc, nval,
+                true, v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sX[xr][j4 + e] = v[e];
+        }
+        __syncthreads();
+        const float step = p.lr * U.shape_scale;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = i + 16 * k;
+            const int wr = g.wr0 + r, wc = g.wc0 + j4;
+            int nval = (wr < U.rows) ? min(4, U.cols - wc) : 0;
+            nval = max(nval, 0);
+            float w[4], o[4];
+            ld4(U.w, U.w_dtype, wr * U.ld_w + wc, nval, vec, w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = j4 + e;
+                o[e] = U.transposed ? sX[c][r] : sX[r][c];
+                w[e] = fmaf(-step, o[e], w[e]);
+            }
+            st4(U.w, U.w_dtype, wr * U.ld_w + wc, nval, vec, w);
+            if (U.w_dbg)
+                st4(U.w_dbg, MUON_F32, wr * U.ld_dbg + wc, nval, false, w);
+            if (U.o_dbg)
+                st4(U.o_dbg, MUON_BF16, wr * U.ld_dbg + wc, nval, false, o);
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_ew_momentum(const EwLaunch& p, int grid, cudaStream_t s) {
+    ew_momentum_kernel<<<grid, EW_THREADS, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ew_norm(const EwLaunch& p, cudaStream_t s) {
+    const int warps_per_block = 8;
+    const int grid = (p.num_units + warps_per_block - 1) / warps_per_block;
+    ew_norm_kernel<<<grid, 32 * warps_per_block, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ew_normalise(const EwLaunch& p, int grid, cudaStream_t s) {
+    ew_normalise_kernel<<<grid, EW_THREADS, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ew_update(const EwLaunch& p, int grid, cudaStream_t s) {
+    ew_update_kernel<<<grid, EW_THREADS, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace muon

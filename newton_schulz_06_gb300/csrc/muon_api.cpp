@@ -1,0 +1,778 @@
+// Host runtime of libmuon: parameter registry, planner (units, groups,
+// cost-sorted tile lists, tensor maps, workspace layout), launch sequence,
+// stage timing and error reporting behind the C ABI of include/muon.h.
+//
+// Work decomposition.  Every registered matrix (full mode) or each of its nb
+// equal column blocks (blockwise mode, "Advancing Emerging Optimizers for
+// Accelerated LLM Training", section "Blockwise mode") is one unit with its
+// own norm, iteration and shape scale.  All units of a group go through each
+// stage in ONE launch: the single-GPU counterpart of the pages' layer-wise
+// distribution (section "Layer-wise distributed optimizer"), with tiles
+// ordered by estimated cost rather than round-robin (section "Load
+// balancing").  Groups exist only when the caller's workspace cannot hold
+// every unit's intermediates at once; they run one after another.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/muon.h"
+#include "muon_internal.h"
+
+using namespace muon;
+
+namespace {
+
+constexpr size_t HEADER_BYTES = 256;
+constexpr float NORM_EPS = 1e-7f;
+constexpr int64_t MAX_DIM = int64_t(1) << 20;
+constexpr int64_t MAX_SHORT = 32768;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+enum Stage { ST_MOMENTUM, ST_NORM, ST_NORMALISE, ST_SYRK1, ST_SYRK2,
+             ST_GEMM, ST_UPDATE };
+
+struct UnitDesc {
+    int param = 0, block = 0;
+    int64_t rows = 0, cols = 0, col_off = 0;
+    int m = 0, n = 0, ld_x = 0, ld_mm = 0;
+    bool transposed = false;
+    float scale = 1.f;
+    size_t x_bytes = 0, mm_bytes = 0, buf_bytes = 0;
+    int64_t ew_tiles = 0;
+    size_t need = 0;   // scratch bytes of this unit inside a group
+};
+
+struct GroupDesc {
+    int u0 = 0, u1 = 0;                      // unit range [u0, u1)
+    size_t ew_off = 0, ns_off = 0;           // metadata offsets in ws
+    size_t t_sx_off = 0, t_sa_off = 0, t_g_off = 0;
+    int n_sx = 0, n_sa = 0, n_g = 0;
+    int64_t ew_tiles = 0;
+};
+
+struct Plan {
+    bool valid = false;
+    int mode = -1, nb = 0;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    std::vector<UnitDesc> units;
+    std::vector<GroupDesc> groups;
+    size_t scratch_off = 0;                  // start of the group scratch
+    int64_t syrk_tiles = 0, gemm_tiles = 0, ew_tiles = 0;
+    int64_t useful_flops_iter = 0, executed_flops_iter = 0;
+};
+
+struct LaunchRec {
+    int stage;
+    cudaEvent_t start, stop;
+};
+
+}  // namespace
+
+struct muon_ctx {
+    int device = 0;
+    cudaStream_t stream = nullptr;
+    int num_sms = 0;
+    std::vector<muon_param> params;
+    std::vector<float*> exp_w;
+    std::vector<void*> exp_o;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    std::string err;
+    Plan plan;
+    bool profiling = false;
+    std::vector<cudaEvent_t> event_pool;
+    std::vector<LaunchRec> launches;
+    int last_launch_count = 0;
+    unsigned long long wait_limit_ns = 2000000000ull;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+};
+
+namespace {
+
+std::string g_create_err;
+
+int fail(muon_ctx* h, int code, const std::string& msg) {
+    if (h) h->err = msg; else g_create_err = msg;
+    return code;
+}
+
+int cuda_fail(muon_ctx* h, cudaError_t e, const char* what) {
+    return fail(h, MUON_ERR_CUDA,
+                std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev)
+            cudaSetDevice(prev);
+    }
+};
+
+size_t elem_size(int dtype) { return dtype == MUON_F32 ? 4 : 2; }
+
+// Per-unit work counts shared by planning and plan statistics.
+void unit_tiles(const UnitDesc& u, int64_t* syrk, int64_t* gemm,
+                int64_t* useful, int64_t* executed) {
+    const int64_t m = u.m, n = u.n;
+    const int64_t T = ceil_div(m, BM);
+    int64_t s = 0, ex = 0;
+    for (int64_t ti = 0; ti < T; ++ti)
+        for (int64_t tj = 0; tj < ceil_div(T, 2); ++tj) {
+            const int64_t bl = 2 * tj, br = 2 * tj + 1;
+            const int nl = (bl < T && bl >= ti) + (br < T && br >= ti);
+            if (!nl) continue;
+            ++s;
+            ex += 2 * BM * 128 * nl * (ceil_div(n, BK) * BK + ceil_div(m, BK) * BK);
+        }
+    const int64_t g = T * ceil_div(n, BN);
+    for (int64_t tj = 0; tj < ceil_div(n, BN); ++tj) {
+        const int64_t nl = std::min<int64_t>(BN, align_up(n - tj * BN, 16));
+        ex += T * 2 * BM * nl * ceil_div(m, BK) * BK;
+    }
+    *syrk = s;
+    *gemm = g;
+    *useful = m * (m + 1) * n + m * (m + 1) * m + 2 * m * m * n;
+    *executed = ex;
+}
+
+int build_units(muon_ctx* h, int mode, int nb, std::vector<UnitDesc>* out) {
+    out->clear();
+    if (mode != MUON_FULL && mode != MUON_BLOCKWISE)
+        return fail(h, MUON_ERR_INVALID_ARG, "mode must be MUON_FULL or MUON_BLOCKWISE");
+    const int nblk = (mode == MUON_BLOCKWISE) ? nb : 1;
+    if (nblk < 1) return fail(h, MUON_ERR_INVALID_ARG, "nb must be >= 1");
+    for (size_t i = 0; i < h->params.size(); ++i) {
+        const muon_param& p = h->params[i];
+        if (p.cols % nblk != 0)
+            return fail(h, MUON_ERR_UNSUPPORTED,
+                        "nb=" + std::to_string(nblk) + " does not divide cols=" +
+                            std::to_string(p.cols) + " of parameter " +
+                            std::to_string(i));
+        const int64_t bc = p.cols / nblk;
+        for (int j = 0; j < nblk; ++j) {
+            UnitDesc u;
+            u.param = static_cast<int>(i);
+            u.block = j;
+            u.rows = p.rows;
+            u.cols = bc;
+            u.col_off = j * bc;
+            u.transposed = p.rows > bc;
+            u.m = static_cast<int>(std::min(p.rows, bc));
+            u.n = static_cast<int>(std::max(p.rows, bc));
+            if (u.m > MAX_SHORT)
+                return fail(h, MUON_ERR_UNSUPPORTED,
+                            "short side above 32768 in parameter " + std::to_string(i));
+            u.ld_x = static_cast<int>(align_up(u.n, 64));
+            u.ld_mm = static_cast<int>(align_up(u.m, 64));
+            u.scale = static_cast<float>(
+                std::sqrt(std::max(1.0, double(p.rows) / double(bc))));
+            u.x_bytes = align_up(size_t(u.m) * u.ld_x * 2, 1024);
+            u.mm_bytes = align_up(size_t(u.m) * u.ld_mm * 2, 1024);
+            u.buf_bytes = 2 * u.x_bytes + 2 * u.mm_bytes;
+            u.ew_tiles = ceil_div(u.m, EW_TILE) * ceil_div(u.n, EW_TILE);
+            u.need = u.buf_bytes + size_t(u.ew_tiles) * 4 + 4;
+            out->push_back(u);
+        }
+    }
+    return MUON_OK;
+}
+
+size_t meta_bound(const std::vector<UnitDesc>& units) {
+    size_t b = 0;
+    for (const UnitDesc& u : units) {
+        int64_t s, g, x, y;
+        unit_tiles(u, &s, &g, &x, &y);
+        b += sizeof(EwUnit) + sizeof(NsUnit) + 5 * 256 +
+             size_t(2 * s + g) * sizeof(TileItem);
+    }
+    return align_up(b, 1024);
+}
+
+constexpr size_t GROUP_SLACK = 4096;
+
+void sizes_for(const std::vector<UnitDesc>& units, size_t* min_b, size_t* full_b) {
+    const size_t fixed = align_up(HEADER_BYTES + meta_bound(units), 1024) + GROUP_SLACK;
+    size_t mx = 0, sum = 0;
+    for (const UnitDesc& u : units) {
+        mx = std::max(mx, u.need);
+        sum += u.need;
+    }
+    *min_b = align_up(fixed + mx, 1024);
+    *full_b = align_up(fixed + sum, 1024);
+}
+
+// Greedy grouping in registration order within the scratch budget.
+bool make_groups(const std::vector<UnitDesc>& units, size_t scratch,
+                 std::vector<GroupDesc>* groups) {
+    groups->clear();
+    size_t acc = 0;
+    GroupDesc g;
+    g.u0 = 0;
+    for (size_t i = 0; i < units.size(); ++i) {
+        const size_t need = units[i].need;
+        if (need + GROUP_SLACK > scratch) return false;
+        if (acc + need + GROUP_SLACK > scratch && i > static_cast<size_t>(g.u0)) {
+            g.u1 = static_cast<int>(i);
+            groups->push_back(g);
+            g = GroupDesc();
+            g.u0 = static_cast<int>(i);
+            acc = 0;
+        }
+        acc += need;
+    }
+    g.u1 = static_cast<int>(units.size());
+    if (g.u1 > g.u0) groups->push_back(g);
+    return true;
+}
+
+int encode_map(muon_ctx* h, CUtensorMap* tm, void* base, int64_t inner,
+               int64_t outer, int64_t ld) {
+    cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+    cuuint64_t strides[1] = {cuuint64_t(ld) * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = h->encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
+                           strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(h, MUON_ERR_CUDA,
+                    "cuTensorMapEncodeTiled failed with code " + std::to_string(int(r)));
+    return MUON_OK;
+}
+
+void sort_tiles(std::vector<TileItem>* v) {
+    std::stable_sort(v->begin(), v->end(), [](const TileItem& a, const TileItem& b) {
+        const int64_t ca = int64_t(a.k_blocks) * a.n_len;
+        const int64_t cb = int64_t(b.k_blocks) * b.n_len;
+        return ca > cb;
+    });
+}
+
+int build_plan(muon_ctx* h, int mode, int nb) {
+    Plan& P = h->plan;
+    P = Plan();
+    int rc = build_units(h, mode, nb, &P.units);
+    if (rc) return rc;
+    if (!h->ws) return fail(h, MUON_ERR_NO_WORKSPACE, "no workspace set (muon_set_workspace)");
+    size_t min_b, full_b;
+    sizes_for(P.units, &min_b, &full_b);
+    if (h->ws_bytes < min_b)
+        return fail(h, MUON_ERR_NO_WORKSPACE,
+                    "workspace of " + std::to_string(h->ws_bytes) + " bytes is below the minimum " +
+                        std::to_string(min_b));
+    const size_t meta_b = meta_bound(P.units);
+    P.scratch_off = align_up(HEADER_BYTES + meta_b, 1024);
+    const size_t scratch = h->ws_bytes - P.scratch_off;
+    if (!make_groups(P.units, scratch, &P.groups))
+        return fail(h, MUON_ERR_NO_WORKSPACE, "a unit does not fit the workspace");
+
+    // host image of header + metadata
+    std::vector<uint8_t> meta(P.scratch_off, 0);
+    size_t off = HEADER_BYTES;
+    char* ws = static_cast<char*>(h->ws);
+    for (GroupDesc& g : P.groups) {
+        const int nu = g.u1 - g.u0;
+        // scratch layout of this group: inv | partials | buffers
+        const size_t inv_off = P.scratch_off;
+        int64_t tiles = 0;
+        for (int i = g.u0; i < g.u1; ++i) tiles += P.units[i].ew_tiles;
+        g.ew_tiles = tiles;
+        const size_t part_off = align_up(inv_off + size_t(nu) * 4, 256);
+        size_t buf_off = align_up(part_off + size_t(tiles) * 4, 1024);
+
+        off = align_up(off, 256);
+        g.ew_off = off;
+        off += sizeof(EwUnit) * nu;
+        off = align_up(off, 256);
+        g.ns_off = off;
+        off += sizeof(NsUnit) * nu;
+        std::vector<TileItem> tsx, tsa, tg;
+        int64_t tile_base = 0;
+        for (int i = g.u0; i < g.u1; ++i) {
+            const UnitDesc& u = P.units[i];
+            const muon_param& pr = h->params[u.param];
+            char* xb0 = ws + buf_off;
+            char* xb1 = xb0 + u.x_bytes;
+            char* ab = xb1 + u.x_bytes;
+            char* bb = ab + u.mm_bytes;
+            buf_off += u.buf_bytes;
+
+            EwUnit e;
+            std::memset(&e, 0, sizeof(e));
+            e.w = static_cast<char*>(pr.w) + u.col_off * elem_size(pr.w_dtype);
+            e.g = static_cast<const char*>(pr.g) + u.col_off * elem_size(pr.g_dtype);
+            e.mom = pr.m + u.col_off;
+            const bool have_w = u.param < int(h->exp_w.size()) && h->exp_w[u.param];
+            const bool have_o = u.param < int(h->exp_o.size()) && h->exp_o[u.param];
+            e.w_dbg = have_w ? h->exp_w[u.param] + u.col_off : nullptr;
+            e.o_dbg = have_o ? static_cast<__nv_bfloat16*>(h->exp_o[u.param]) + u.col_off
+                             : nullptr;
+            e.x[0] = reinterpret_cast<__nv_bfloat16*>(xb0);
+            e.x[1] = reinterpret_cast<__nv_bfloat16*>(xb1);
+            e.ld_w = pr.ld_w;
+            e.ld_g = pr.ld_g;
+            e.ld_m = pr.ld_m;
+            e.ld_dbg = pr.cols;
+            e.rows = static_cast<int32_t>(u.rows);
+            e.cols = static_cast<int32_t>(u.cols);
+            e.m = u.m;
+            e.n = u.n;
+            e.ld_x = u.ld_x;
+            e.w_dtype = pr.w_dtype;
+            e.g_dtype = pr.g_dtype;
+            e.transposed = u.transposed ? 1 : 0;
+            auto al = [](const void* p, size_t a) {
+                return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+            };
+            const size_t wa = pr.w_dtype == MUON_F32 ? 16 : 8;
+            const size_t ga = pr.g_dtype == MUON_F32 ? 16 : 8;
+            e.vec_ok = (u.cols % 4 == 0) && (pr.ld_w % 4 == 0) && (pr.ld_g % 4 == 0) &&
+                       (pr.ld_m % 4 == 0) && al(e.w, wa) && al(e.g, ga) && al(e.mom, 16);
+            e.tiles_n = static_cast<int32_t>(ceil_div(u.n, EW_TILE));
+            e.tile_base = tile_base;
+            e.tile_count = u.ew_tiles;
+            e.shape_scale = u.scale;
+            tile_base += u.ew_tiles;
+            std::memcpy(meta.data() + g.ew_off + sizeof(EwUnit) * (i - g.u0), &e, sizeof(e));
+
+            NsUnit ns;
+            std::memset(&ns, 0, sizeof(ns));
+            if ((rc = encode_map(h, &ns.tm_x[0], xb0, u.n, u.m, u.ld_x))) return rc;
+            if ((rc = encode_map(h, &ns.tm_x[1], xb1, u.n, u.m, u.ld_x))) return rc;
+            if ((rc = encode_map(h, &ns.tm_a, ab, u.m, u.m, u.ld_mm))) return rc;
+            if ((rc = encode_map(h, &ns.tm_b, bb, u.m, u.m, u.ld_mm))) return rc;
+            ns.x[0] = e.x[0];
+            ns.x[1] = e.x[1];
+            ns.a = reinterpret_cast<__nv_bfloat16*>(ab);
+            ns.b = reinterpret_cast<__nv_bfloat16*>(bb);
+            ns.m = u.m;
+            ns.n = u.n;
+            ns.ld_x = u.ld_x;
+            ns.ld_mm = u.ld_mm;
+            std::memcpy(meta.data() + g.ns_off + sizeof(NsUnit) * (i - g.u0), &ns, sizeof(ns));
+
+            // tile lists
+            const int li = i - g.u0;
+            const int64_t T = ceil_div(u.m, BM);
+            const int kx = static_cast<int>(ceil_div(u.n, BK));
+            const int km = static_cast<int>(ceil_div(u.m, BK));
+            for (int64_t ti = 0; ti < T; ++ti)
+                for (int64_t tj = 0; tj < ceil_div(T, 2); ++tj) {
+                    const int64_t bl = 2 * tj, br = 2 * tj + 1;
+                    const bool lneed = bl < T && bl >= ti;
+                    const bool rneed = br < T && br >= ti;
+                    if (!lneed && !rneed) continue;
+                    TileItem t;
+                    t.unit = li;
+                    t.ti = static_cast<int16_t>(ti);
+                    t.tj = static_cast<int16_t>(tj);
+                    t.n_off = lneed ? 0 : 128;
+                    t.n_len = static_cast<int16_t>(128 * (int(lneed) + int(rneed)));
+                    t.k_blocks = kx;
+                    tsx.push_back(t);
+                    t.k_blocks = km;
+                    tsa.push_back(t);
+                }
+            for (int64_t ti = 0; ti < T; ++ti)
+                for (int64_t tj = 0; tj < ceil_div(u.n, BN); ++tj) {
+                    TileItem t;
+                    t.unit = li;
+                    t.ti = static_cast<int16_t>(ti);
+                    t.tj = static_cast<int16_t>(tj);
+                    t.n_off = 0;
+                    t.n_len = static_cast<int16_t>(
+                        std::min<int64_t>(BN, align_up(u.n - tj * BN, 16)));
+                    t.k_blocks = km;
+                    tg.push_back(t);
+                }
+            int64_t s, gg, us, ex;
+            unit_tiles(u, &s, &gg, &us, &ex);
+            P.useful_flops_iter += us;
+            P.executed_flops_iter += ex;
+        }
+        sort_tiles(&tsx);
+        sort_tiles(&tsa);
+        sort_tiles(&tg);
+        auto put = [&](const std::vector<TileItem>& v, size_t* o, int* n) {
+            off = align_up(off, 256);
+            *o = off;
+            *n = static_cast<int>(v.size());
+            if (!v.empty()) std::memcpy(meta.data() + off, v.data(), v.size() * sizeof(TileItem));
+            off += v.size() * sizeof(TileItem);
+        };
+        put(tsx, &g.t_sx_off, &g.n_sx);
+        put(tsa, &g.t_sa_off, &g.n_sa);
+        put(tg, &g.t_g_off, &g.n_g);
+        P.syrk_tiles += g.n_sx;
+        P.gemm_tiles += g.n_g;
+        P.ew_tiles += g.ew_tiles;
+        if (off > P.scratch_off)
+            return fail(h, MUON_ERR_STATE, "internal: metadata exceeds its bound");
+        // stash scratch offsets in the group (reuse fields via locals below)
+        (void)part_off;
+    }
+    cudaError_t e = cudaMemcpyAsync(h->ws, meta.data(), meta.size(),
+                                    cudaMemcpyHostToDevice, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "metadata upload");
+    e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "metadata upload sync");
+    P.mode = mode;
+    P.nb = (mode == MUON_BLOCKWISE) ? nb : 1;
+    P.ws = h->ws;
+    P.ws_bytes = h->ws_bytes;
+    P.valid = true;
+    return MUON_OK;
+}
+
+cudaEvent_t pool_event(muon_ctx* h, size_t idx) {
+    while (h->event_pool.size() <= idx) {
+        cudaEvent_t ev;
+        if (cudaEventCreate(&ev) != cudaSuccess) return nullptr;
+        h->event_pool.push_back(ev);
+    }
+    return h->event_pool[idx];
+}
+
+}  // namespace
+
+extern "C" {
+
+int muon_create(muon_handle* out, int device, void* cuda_stream) {
+    if (!out) return fail(nullptr, MUON_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (device == MUON_HOST_ONLY) {
+        muon_ctx* h = new muon_ctx();
+        h->device = MUON_HOST_ONLY;
+        h->num_sms = 148;
+        *out = h;
+        return MUON_OK;
+    }
+    int ndev = 0;
+    cudaError_t e = cudaGetDeviceCount(&ndev);
+    if (e != cudaSuccess) return fail(nullptr, MUON_ERR_CUDA, cudaGetErrorString(e));
+    if (device < 0 || device >= ndev)
+        return fail(nullptr, MUON_ERR_INVALID_ARG, "device index out of range");
+    DeviceGuard guard(device);
+    muon_ctx* h = new muon_ctx();
+    h->device = device;
+    h->stream = static_cast<cudaStream_t>(cuda_stream);
+    cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device);
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+    if (major != 10 || minor != 3) {
+        delete h;
+        return fail(nullptr, MUON_ERR_UNSUPPORTED,
+                    "libmuon is built for sm_103a (GB300); device has compute capability " +
+                        std::to_string(major) + "." + std::to_string(minor));
+    }
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+        delete h;
+        return fail(nullptr, MUON_ERR_CUDA, "cuTensorMapEncodeTiled not available");
+    }
+    h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    if (const char* s = std::getenv("MUON_WAIT_LIMIT_MS")) {
+        const long long ms = std::atoll(s);
+        if (ms > 0) h->wait_limit_ns = static_cast<unsigned long long>(ms) * 1000000ull;
+    }
+    *out = h;
+    return MUON_OK;
+}
+
+int muon_set_stream(muon_handle h, void* cuda_stream) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    h->stream = static_cast<cudaStream_t>(cuda_stream);
+    return MUON_OK;
+}
+
+int muon_register_params(muon_handle h, int n, const muon_param* params) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (n < 1 || !params) return fail(h, MUON_ERR_INVALID_ARG, "need n >= 1 parameters");
+    for (int i = 0; i < n; ++i) {
+        const muon_param& p = params[i];
+        const std::string who = "parameter " + std::to_string(i) + ": ";
+        if (!p.w || !p.g || !p.m) return fail(h, MUON_ERR_INVALID_ARG, who + "NULL pointer");
+        if (p.rows < 1 || p.cols < 1 || p.rows > MAX_DIM || p.cols > MAX_DIM)
+            return fail(h, MUON_ERR_INVALID_ARG, who + "rows/cols out of range");
+        if (p.ld_w < p.cols || p.ld_g < p.cols || p.ld_m < p.cols)
+            return fail(h, MUON_ERR_INVALID_ARG, who + "leading dimension below cols");
+        if ((p.w_dtype != MUON_F32 && p.w_dtype != MUON_BF16) ||
+            (p.g_dtype != MUON_F32 && p.g_dtype != MUON_BF16))
+            return fail(h, MUON_ERR_UNSUPPORTED, who + "dtype must be MUON_F32 or MUON_BF16");
+        if (std::min(p.rows, p.cols) > MAX_SHORT)
+            return fail(h, MUON_ERR_UNSUPPORTED, who + "short side above 32768");
+    }
+    h->params.assign(params, params + n);
+    h->exp_w.clear();
+    h->exp_o.clear();
+    h->plan.valid = false;
+    h->err.clear();
+    return MUON_OK;
+}
+
+int muon_workspace_size(muon_handle h, int mode, int nb, size_t* min_bytes,
+                        size_t* full_bytes) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (!min_bytes || !full_bytes) return fail(h, MUON_ERR_INVALID_ARG, "NULL output");
+    if (h->params.empty()) return fail(h, MUON_ERR_STATE, "no parameters registered");
+    std::vector<UnitDesc> units;
+    int rc = build_units(h, mode, nb, &units);
+    if (rc) return rc;
+    sizes_for(units, min_bytes, full_bytes);
+    return MUON_OK;
+}
+
+int muon_set_workspace(muon_handle h, void* dptr, size_t bytes) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (!dptr || bytes == 0) return fail(h, MUON_ERR_INVALID_ARG, "NULL or empty workspace");
+    if (reinterpret_cast<uintptr_t>(dptr) % 1024 != 0)
+        return fail(h, MUON_ERR_INVALID_ARG, "workspace must be 1024-byte aligned");
+    h->ws = dptr;
+    h->ws_bytes = bytes;
+    h->plan.valid = false;
+    return MUON_OK;
+}
+
+int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
+              float a, float b, float c, int mode, int nb) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (h->device == MUON_HOST_ONLY) return fail(h, MUON_ERR_STATE, "host-only handle");
+    if (h->params.empty()) return fail(h, MUON_ERR_STATE, "no parameters registered");
+    if (ns_steps < 1 || ns_steps > 64)
+        return fail(h, MUON_ERR_INVALID_ARG, "ns_steps must be in 1..64");
+    if (!std::isfinite(lr) || !std::isfinite(beta) || !std::isfinite(a) ||
+        !std::isfinite(b) || !std::isfinite(c))
+        return fail(h, MUON_ERR_INVALID_ARG, "non-finite hyper-parameter");
+    if (mode != MUON_FULL && mode != MUON_BLOCKWISE)
+        return fail(h, MUON_ERR_INVALID_ARG, "mode must be MUON_FULL or MUON_BLOCKWISE");
+    if (mode == MUON_BLOCKWISE && nb < 1) return fail(h, MUON_ERR_INVALID_ARG, "nb must be >= 1");
+    DeviceGuard guard(h->device);
+    const int want_nb = (mode == MUON_BLOCKWISE) ? nb : 1;
+    Plan& P = h->plan;
+    if (!P.valid || P.mode != mode || P.nb != want_nb || P.ws != h->ws ||
+        P.ws_bytes != h->ws_bytes) {
+        const int rc = build_plan(h, mode, nb);
+        if (rc) {
+            P.valid = false;
+            return rc;
+        }
+    }
+    char* ws = static_cast<char*>(h->ws);
+    int* err_word = reinterpret_cast<int*>(ws);
+    h->launches.clear();
+    size_t ev_idx = 0;
+    int count = 0;
+    auto begin = [&](int stage) -> bool {
+        ++count;
+        if (!h->profiling) return true;
+        LaunchRec r;
+        r.stage = stage;
+        r.start = pool_event(h, ev_idx++);
+        r.stop = pool_event(h, ev_idx++);
+        if (!r.start || !r.stop) return false;
+        cudaEventRecord(r.start, h->stream);
+        h->launches.push_back(r);
+        return true;
+    };
+    auto end = [&]() {
+        if (h->profiling) cudaEventRecord(h->launches.back().stop, h->stream);
+    };
+    const int ew_grid_cap = h->num_sms * 8;
+    for (const GroupDesc& g : P.groups) {
+        const int nu = g.u1 - g.u0;
+        const size_t inv_off = P.scratch_off;
+        const size_t part_off = align_up(inv_off + size_t(nu) * 4, 256);
+        EwLaunch ew;
+        ew.units = reinterpret_cast<const EwUnit*>(ws + g.ew_off);
+        ew.num_units = nu;
+        ew.num_tiles = g.ew_tiles;
+        ew.partial = reinterpret_cast<float*>(ws + part_off);
+        ew.inv_norm = reinterpret_cast<float*>(ws + inv_off);
+        ew.beta = beta;
+        ew.nesterov = nesterov ? 1 : 0;
+        ew.lr = lr;
+        ew.src = 0;
+        ew.eps = NORM_EPS;
+        const int ew_grid = static_cast<int>(std::min<int64_t>(g.ew_tiles, ew_grid_cap));
+        cudaError_t e;
+        if (!begin(ST_MOMENTUM)) return fail(h, MUON_ERR_CUDA, "event create");
+        e = launch_ew_momentum(ew, ew_grid, h->stream);
+        end();
+        if (e != cudaSuccess) return cuda_fail(h, e, "momentum launch");
+        if (!begin(ST_NORM)) return fail(h, MUON_ERR_CUDA, "event create");
+        e = launch_ew_norm(ew, h->stream);
+        end();
+        if (e != cudaSuccess) return cuda_fail(h, e, "norm launch");
+        if (!begin(ST_NORMALISE)) return fail(h, MUON_ERR_CUDA, "event create");
+        e = launch_ew_normalise(ew, ew_grid, h->stream);
+        end();
+        if (e != cudaSuccess) return cuda_fail(h, e, "normalise launch");
+        NsLaunch L;
+        L.units = reinterpret_cast<const NsUnit*>(ws + g.ns_off);
+        L.a = a;
+        L.b = b;
+        L.c = c;
+        L.wait_limit_ns = h->wait_limit_ns;
+        L.err = err_word;
+        int cur = 0;
+        for (int s = 0; s < ns_steps; ++s) {
+            L.src = cur;
+            const struct { NsOp op; size_t off; int n; int st; } seq[3] = {
+                {OP_SYRK_X, g.t_sx_off, g.n_sx, ST_SYRK1},
+                {OP_SYRK_A, g.t_sa_off, g.n_sa, ST_SYRK2},
+                {OP_GEMM_BX, g.t_g_off, g.n_g, ST_GEMM}};
+            for (const auto& q : seq) {
+                L.tiles = reinterpret_cast<const TileItem*>(ws + q.off);
+                L.num_tiles = q.n;
+                const int grid = std::min(q.n, h->num_sms);
+                if (!begin(q.st)) return fail(h, MUON_ERR_CUDA, "event create");
+                e = launch_ns(q.op, L, grid, h->stream);
+                end();
+                if (e != cudaSuccess) return cuda_fail(h, e, "tensor-core stage launch");
+            }
+            cur ^= 1;
+        }
+        ew.src = cur;
+        if (!begin(ST_UPDATE)) return fail(h, MUON_ERR_CUDA, "event create");
+        e = launch_ew_update(ew, ew_grid, h->stream);
+        end();
+        if (e != cudaSuccess) return cuda_fail(h, e, "update launch");
+    }
+    h->last_launch_count = count;
+    return MUON_OK;
+}
+
+int muon_sync(muon_handle h) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (h->device == MUON_HOST_ONLY) return fail(h, MUON_ERR_STATE, "host-only handle");
+    DeviceGuard guard(h->device);
+    cudaError_t e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "stream synchronize");
+    if (h->ws) {
+        int word = 0;
+        e = cudaMemcpy(&word, h->ws, sizeof(int), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(h, e, "error word read");
+        if (word != 0) {
+            const int zero = 0;
+            cudaMemcpy(h->ws, &zero, sizeof(int), cudaMemcpyHostToDevice);
+            if (word == DEV_ERR_TIMEOUT)
+                return fail(h, MUON_ERR_TIMEOUT, "a bounded wait on the GPU ran out");
+            return fail(h, MUON_ERR_CUDA, "device error word " + std::to_string(word));
+        }
+    }
+    return MUON_OK;
+}
+
+int muon_destroy(muon_handle h) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (h->device != MUON_HOST_ONLY) {
+        DeviceGuard guard(h->device);
+        for (cudaEvent_t ev : h->event_pool) cudaEventDestroy(ev);
+    }
+    delete h;
+    return MUON_OK;
+}
+
+const char* muon_last_error(muon_handle h) {
+    return h ? h->err.c_str() : g_create_err.c_str();
+}
+
+int muon_set_profiling(muon_handle h, int on) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    h->profiling = on != 0;
+    return MUON_OK;
+}
+
+int muon_stage_times(muon_handle h, float* ms, int* launches, int n) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (h->device == MUON_HOST_ONLY) return fail(h, MUON_ERR_STATE, "host-only handle");
+    if (!ms || n < 0) return fail(h, MUON_ERR_INVALID_ARG, "NULL output");
+    DeviceGuard guard(h->device);
+    const int k = std::min(n, MUON_N_STAGES);
+    for (int i = 0; i < k; ++i) {
+        ms[i] = 0.f;
+        if (launches) launches[i] = 0;
+    }
+    for (const LaunchRec& r : h->launches) {
+        float t = 0.f;
+        cudaError_t e = cudaEventSynchronize(r.stop);
+        if (e != cudaSuccess) return cuda_fail(h, e, "event synchronize");
+        e = cudaEventElapsedTime(&t, r.start, r.stop);
+        if (e != cudaSuccess) return cuda_fail(h, e, "event elapsed time");
+        if (r.stage < k) {
+            ms[r.stage] += t;
+            if (launches) launches[r.stage] += 1;
+        }
+    }
+    return k;
+}
+
+int muon_last_launch_count(muon_handle h) { return h ? h->last_launch_count : 0; }
+
+int muon_debug_set_exports(muon_handle h, int n, float* const* w_f32, void* const* o_bf16) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (n < 0 || n > static_cast<int>(h->params.size()))
+        return fail(h, MUON_ERR_INVALID_ARG, "n out of range");
+    h->exp_w.assign(h->params.size(), nullptr);
+    h->exp_o.assign(h->params.size(), nullptr);
+    for (int i = 0; i < n; ++i) {
+        if (w_f32) h->exp_w[i] = w_f32[i];
+        if (o_bf16) h->exp_o[i] = o_bf16[i];
+    }
+    h->plan.valid = false;
+    return MUON_OK;
+}
+
+int muon_get_plan_info(muon_handle h, int mode, int nb, muon_plan_info* out) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (!out) return fail(h, MUON_ERR_INVALID_ARG, "NULL output");
+    if (h->params.empty()) return fail(h, MUON_ERR_STATE, "no parameters registered");
+    std::vector<UnitDesc> units;
+    int rc = build_units(h, mode, nb, &units);
+    if (rc) return rc;
+    std::memset(out, 0, sizeof(*out));
+    out->units = static_cast<int64_t>(units.size());
+    for (const UnitDesc& u : units) {
+        int64_t s, g, us, ex;
+        unit_tiles(u, &s, &g, &us, &ex);
+        out->syrk_tiles += s;
+        out->gemm_tiles += g;
+        out->ew_tiles += u.ew_tiles;
+        out->useful_flops += us;
+        out->executed_flops += ex;
+    }
+    std::vector<GroupDesc> groups;
+    size_t min_b, full_b;
+    sizes_for(units, &min_b, &full_b);
+    if (h->ws && h->ws_bytes >= min_b) {
+        const size_t scratch = h->ws_bytes - align_up(HEADER_BYTES + meta_bound(units), 1024);
+        make_groups(units, scratch, &groups);
+        out->groups = static_cast<int64_t>(groups.size());
+    } else {
+        out->groups = 1;
+    }
+    return MUON_OK;
+}
+
+}  // extern "C"

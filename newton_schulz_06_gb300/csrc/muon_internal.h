@@ -1,0 +1,105 @@
+// Internal data structures shared by the host planner and the kernels.
+// Nothing here is part of the public C ABI (include/muon.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace muon {
+
+// Tile edge of the element-wise stages (momentum, normalise, update).
+constexpr int EW_TILE = 64;
+constexpr int EW_THREADS = 256;
+
+// Tensor-core stages: one CTA computes a BM x BN output tile, K in BK steps.
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;            // 64 bf16 = 128 bytes = one swizzle row
+constexpr int STAGES = 4;
+
+// Device error word codes (first error wins).
+constexpr int DEV_ERR_TIMEOUT = 1;
+constexpr int DEV_ERR_BAD_TILE = 2;
+
+// One unit of work: a whole matrix (full mode) or one column block of a
+// matrix (blockwise mode), seen by the element-wise stages.  All pointers are
+// already offset to the unit's first element.  X is the unit oriented short
+// side first: m x n with m = min(rows, cols); if `transposed`, X = W-block^T.
+struct EwUnit {
+    void* w;
+    const void* g;
+    float* mom;
+    float* w_dbg;            // optional fp32 export of the updated weight
+    __nv_bfloat16* o_dbg;    // optional bf16 export of O (W orientation)
+    __nv_bfloat16* x[2];     // iteration ping-pong buffers (m x ld_x)
+    int64_t ld_w, ld_g, ld_m, ld_dbg;
+    int32_t rows, cols;      // unit shape in the weight's orientation
+    int32_t m, n, ld_x;
+    int32_t w_dtype, g_dtype;
+    int32_t transposed;
+    int32_t vec_ok;          // 16-byte vector path allowed
+    int32_t tiles_n;         // 64-tiles along n (X orientation)
+    int64_t tile_base;       // first global element-wise tile of the unit
+    int64_t tile_count;
+    float lr_scale_unused;   // kept for alignment
+    float shape_scale;
+};
+
+// One unit as seen by the tensor-core stages.  Tensor maps come first and
+// are 64-byte aligned (TMA reads them from global memory).
+struct alignas(128) NsUnit {
+    CUtensorMap tm_x[2];     // X ping/pong: dims {n, m}, box {64, 64}
+    CUtensorMap tm_a;        // A = X X^T : dims {m, m}, box {64, 64}
+    CUtensorMap tm_b;        // B = bA+cAA: dims {m, m}, box {64, 64}
+    __nv_bfloat16* x[2];
+    __nv_bfloat16* a;
+    __nv_bfloat16* b;
+    int32_t m, n, ld_x, ld_mm;
+};
+
+// One output tile of a tensor-core stage.
+//   symmetric stages: rows [128*ti, +128) x cols [256*tj + n_off, +n_len)
+//   GEMM stage:       rows [128*ti, +128) x cols [256*tj, +n_len)
+struct TileItem {
+    int32_t unit;
+    int16_t ti, tj;
+    int16_t n_off, n_len;
+    int32_t k_blocks;        // number of BK steps (cost, also used by LPT)
+};
+
+enum NsOp { OP_SYRK_X = 0, OP_SYRK_A = 1, OP_GEMM_BX = 2 };
+
+struct NsLaunch {
+    const NsUnit* units;
+    const TileItem* tiles;
+    int32_t num_tiles;
+    int32_t src;             // which X buffer is the current iterate
+    float a, b, c;
+    unsigned long long wait_limit_ns;
+    int* err;                // device error word
+};
+
+struct EwLaunch {
+    const EwUnit* units;
+    int32_t num_units;
+    int64_t num_tiles;       // total element-wise tiles of the group
+    float* partial;          // one fp32 sum of squares per tile
+    float* inv_norm;         // one fp32 1/(||U||+eps) per unit
+    float beta;
+    int32_t nesterov;
+    float lr;
+    int32_t src;             // X buffer holding the final iterate (update)
+    float eps;
+};
+
+// Launch wrappers (defined in the .cu files).  Return cudaGetLastError().
+cudaError_t launch_ew_momentum(const EwLaunch& p, int grid, cudaStream_t s);
+cudaError_t launch_ew_norm(const EwLaunch& p, cudaStream_t s);
+cudaError_t launch_ew_normalise(const EwLaunch& p, int grid, cudaStream_t s);
+cudaError_t launch_ew_update(const EwLaunch& p, int grid, cudaStream_t s);
+cudaError_t launch_ns(NsOp op, const NsLaunch& p, int grid, cudaStream_t s);
+size_t ns_smem_bytes();
+
+}  // namespace muon

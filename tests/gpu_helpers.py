@@ -1,0 +1,102 @@
+"""Shared helpers of the GPU parity tests: run libmuon through its C ABI on
+seeded inputs, run the float64 oracle on host copies of the same inputs, and
+compare with the tolerances of the step:
+
+  * orthogonalised update O: relative Frobenius error <= 3e-2 per unit
+    (bf16 operands, fp32 accumulation);
+  * updated weight: relative Frobenius error <= 1e-3 on the fp32 value the
+    update computes before it is stored (bf16 rounding of a N(0, 0.02)
+    weight alone is ~1.7e-3), plus a bit-exact check that the stored bf16
+    weight is the round-to-nearest-even of that fp32 value; fp32 weights are
+    compared directly;
+  * momentum: fp32 M = fma(beta, M, G) against the float64 value, within
+    one fp32 rounding.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from newton_schulz_06_gb300 import MUON_BLOCKWISE, MUON_FULL, Muon
+
+COEFFS = tuple(float(np.float32(x)) for x in (3.4445, -4.7750, 2.0315))
+O_TOL = 3e-2
+W_TOL = 1e-3
+
+
+def f32(x):
+    return float(np.float32(x))
+
+
+def relF(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    nb = np.linalg.norm(b)
+    return np.linalg.norm(a - b) / (nb if nb > 0 else 1.0)
+
+
+def to_np(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def gpu_step(triples, *, lr=0.02, beta=0.95, nesterov=True, ns_steps=5,
+             coeffs=COEFFS, mode="full", nb=1, exports=True,
+             max_workspace=None, steps=1):
+    """Runs `steps` Muon steps on device tensors in place; returns
+    (host copies of the inputs, fp32 W exports, bf16 O exports, opt)."""
+    inputs = [(to_np(W), to_np(G), to_np(M)) for W, G, M in triples]
+    opt = Muon(triples)
+    md = MUON_BLOCKWISE if mode == "blockwise" else MUON_FULL
+    opt.ensure_workspace(md, nb, max_workspace)
+    wexp = oexp = None
+    if exports:
+        wexp = [torch.empty(W.shape, dtype=torch.float32, device=W.device)
+                for W, _, _ in triples]
+        oexp = [torch.empty(W.shape, dtype=torch.bfloat16, device=W.device)
+                for W, _, _ in triples]
+        opt.set_exports(wexp, oexp)
+    for _ in range(steps):
+        opt.step(lr=f32(lr), beta=f32(beta), nesterov=nesterov,
+                 ns_steps=ns_steps, coeffs=coeffs, mode=md, nb=nb)
+    opt.sync()
+    torch.cuda.synchronize()
+    return inputs, wexp, oexp, opt
+
+
+def oracle_step(inp, *, lr=0.02, beta=0.95, nesterov=True, ns_steps=5,
+                coeffs=COEFFS, mode="full", nb=1):
+    W, G, M = inp
+    a, b, c = coeffs
+    return oracle.muon_step(W, G, M, lr=f32(lr), beta=f32(beta),
+                            nesterov=nesterov, ns_steps=ns_steps, a=a, b=b,
+                            c=c, mode=mode, nb=nb)
+
+
+def check_against_oracle(triple, inp, wexp, oexp, ref, *, mode="full", nb=1):
+    """Asserts the three tolerances for one parameter; returns the errors."""
+    W, G, M = triple
+    rows, cols = W.shape
+    errs = {}
+    O_gpu = to_np(oexp)
+    if mode == "blockwise":
+        w = cols // nb
+        blocks = [(j * w, (j + 1) * w) for j in range(nb)]
+    else:
+        blocks = [(0, cols)]
+    errs["O"] = max(relF(O_gpu[:, lo:hi], ref["O"][:, lo:hi])
+                    for lo, hi in blocks)
+    assert errs["O"] <= O_TOL, errs
+    w32 = to_np(wexp)
+    errs["W"] = relF(w32, ref["W"])
+    assert errs["W"] <= W_TOL, errs
+    if W.dtype == torch.bfloat16:
+        assert torch.equal(W, wexp.to(torch.bfloat16)), "stored W != RNE(fp32)"
+    else:
+        assert torch.equal(W, wexp)
+    M_gpu = to_np(M)
+    diff = np.abs(M_gpu - ref["M"])
+    bound = 1.2e-7 * (np.abs(ref["M"]) + np.abs(inp[1])) + 1e-30
+    errs["M"] = float(np.max(diff / bound)) if diff.size else 0.0
+    assert np.all(diff <= bound), errs
+    return errs

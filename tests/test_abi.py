@@ -1,0 +1,145 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, validates arguments, and its host planner counts tiles and FLOPs the
+way an independent enumeration does."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from newton_schulz_06_gb300 import build as b
+    b.build()
+    from newton_schulz_06_gb300 import _lib
+    return _lib
+
+
+def declared_entry_points():
+    text = open(os.path.join(ROOT, "include", "muon.h")).read()
+    return sorted(set(re.findall(r"MUON_API\s+[\w\s\*]*?\b(muon_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_list(L):
+    assert declared_entry_points() == sorted(L.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    lib = L.lib()
+    for name in declared_entry_points():
+        assert hasattr(lib, name), name
+
+
+def test_elf_dynamic_symbols(L):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH],
+                         capture_output=True, text=True).stdout
+    syms = set(re.findall(r"\bT (muon_\w+)", out))
+    assert set(declared_entry_points()) <= syms
+    # nothing but the C ABI is exported from the library's own code
+    assert all(s.startswith("muon_") for s in syms)
+
+
+def _planner(shapes, **kw):
+    from newton_schulz_06_gb300 import HostPlanner
+    return HostPlanner(shapes, **kw)
+
+
+def _syrk_tiles(m):
+    T = -(-m // 128)
+    return sum(1 for ti in range(T) for tj in range(-(-T // 2))
+               if any(2 * tj + h < T and 2 * tj + h >= ti for h in (0, 1)))
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096), (768, 2048), (2048, 768),
+                                   (576, 7168), (100, 37), (8, 16)])
+def test_plan_tile_counts(L, shape):
+    p = _planner([shape])
+    info = p.plan_info()
+    m, n = min(shape), max(shape)
+    assert info["units"] == 1 and info["groups"] == 1
+    assert info["syrk_tiles"] == _syrk_tiles(m)
+    assert info["gemm_tiles"] == (-(-m // 128)) * (-(-n // 256))
+    assert info["ew_tiles"] == (-(-m // 64)) * (-(-n // 64))
+
+
+def test_useful_flops_match_formula(L):
+    from newton_schulz_06_gb300 import flops
+    from newton_schulz_06_gb300.inputs import qwen3_30b_a3b_block_shapes
+    shapes = qwen3_30b_a3b_block_shapes()
+    info = _planner(shapes).plan_info()
+    assert info["units"] == 388
+    assert 5 * info["useful_flops"] == flops.useful_flops(shapes)
+    # executed FLOPs cover the useful ones and stay within the tile waste
+    assert info["executed_flops"] >= info["useful_flops"]
+    assert info["executed_flops"] < 1.2 * flops.gemm_equiv_flops(shapes) / 5
+
+
+def test_flop_counts_closed_form():
+    from newton_schulz_06_gb300 import flops
+    # 4096^2: GEMM-equivalent 6 m^3 per iteration; 2.06 TFLOP for 5 steps
+    assert flops.gemm_equiv_flops([(4096, 4096)]) == 5 * 6 * 4096 ** 3
+    u = flops.useful_flops([(4096, 4096)])
+    assert u == 5 * (2 * 4096 * 4097 * 4096 + 2 * 4096 ** 3)
+    assert abs(u / 1e12 - 1.375) < 0.001
+    # blockwise: nb blocks of rows x cols/nb
+    assert flops.useful_flops([(16384, 512)], mode="blockwise", nb=4) == \
+        4 * flops.useful_flops([(16384, 128)])
+
+
+def test_blockwise_units_and_validation(L):
+    from newton_schulz_06_gb300.inputs import kimi_k2_layer_shapes
+    shapes = kimi_k2_layer_shapes()
+    p = _planner(shapes)
+    assert p.plan_info(L.MUON_BLOCKWISE, 4)["units"] == 4 * len(shapes)
+    assert p.plan_info(L.MUON_FULL, 4)["units"] == len(shapes)
+    with pytest.raises(L.MuonError) as e:
+        p.plan_info(L.MUON_BLOCKWISE, 3)
+    assert e.value.code == L.MUON_ERR_UNSUPPORTED
+
+
+def test_workspace_sizes_monotone(L):
+    from newton_schulz_06_gb300.inputs import qwen3_30b_a3b_block_shapes
+    p = _planner(qwen3_30b_a3b_block_shapes())
+    mn, full = p.workspace_size()
+    # full holds every unit's X ping-pong: at least 2 * 2 bytes * elements
+    elems = sum(r * c for r, c in qwen3_30b_a3b_block_shapes())
+    assert full >= 4 * elems and mn < full
+    # the largest unit (2048 x 4096) needs its X pair and A, B
+    assert mn >= 2 * 2 * 2048 * 4096 + 2 * 2 * 2048 * 2048
+
+
+def test_register_rejects_bad_params(L):
+    import ctypes
+    lib = L.lib()
+    h = ctypes.c_void_p()
+    assert lib.muon_create(ctypes.byref(h), L.MUON_HOST_ONLY, None) == 0
+    P = L.MuonParam
+
+    def reg(**kw):
+        p = P()
+        p.w = p.g = p.m = 0x1000
+        p.rows, p.cols = 4, 8
+        p.ld_w = p.ld_g = p.ld_m = 8
+        p.w_dtype = p.g_dtype = L.MUON_BF16
+        for k, v in kw.items():
+            setattr(p, k, v)
+        arr = (P * 1)(p)
+        return lib.muon_register_params(h, 1, arr)
+
+    assert reg() == 0
+    assert reg(w=None) == L.MUON_ERR_INVALID_ARG
+    assert reg(rows=0) == L.MUON_ERR_INVALID_ARG
+    assert reg(ld_g=4) == L.MUON_ERR_INVALID_ARG
+    assert reg(w_dtype=7) == L.MUON_ERR_UNSUPPORTED
+    assert reg(rows=40000, cols=40000, ld_w=40000, ld_g=40000,
+               ld_m=40000) == L.MUON_ERR_UNSUPPORTED
+    assert lib.muon_register_params(h, 0, None) == L.MUON_ERR_INVALID_ARG
+    assert b"parameters" in lib.muon_last_error(h)
+    # a host-only handle plans but never launches
+    assert reg() == 0
+    assert lib.muon_step(h, 0.02, 0.95, 1, 5, 3.4445, -4.775, 2.0315, 0,
+                         1) == L.MUON_ERR_STATE
+    assert lib.muon_destroy(h) == 0

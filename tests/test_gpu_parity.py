@@ -1,0 +1,147 @@
+"""Parity of libmuon (through its C ABI) with the float64 oracle on the GPU.
+
+Sizes here are ones the oracle finishes in seconds while spanning several
+128 x 256 tensor-core tiles, 64 x 64 element-wise tiles and ragged tails.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import (check_against_oracle, gpu_step, oracle_step, relF,
+                         to_np)
+from newton_schulz_06_gb300.inputs import random_case, workload, make_state
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def case(rows, cols, seed, **kw):
+    W, G, M = random_case(rows, cols, seed, device=DEV, **kw)
+    return [W, G, M]
+
+
+def test_single_matrix_256x512_f32():
+    """The single fp32 matrix workload: G, M ~ N(0,1), W ~ N(0, 0.02)."""
+    wl = workload("single_256x512_f32")
+    Ws, Gs, Ms = make_state(wl, DEV)
+    trip = [Ws[0], Gs[0], Ms[0]]
+    inp, wexp, oexp, _ = gpu_step([trip])
+    ref = oracle_step(inp[0])
+    errs = check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref)
+    print("256x512 f32", errs)
+
+
+@pytest.mark.parametrize("rows,cols", [(8, 16), (16, 8), (100, 37), (37, 100),
+                                       (130, 130), (200, 333), (333, 200),
+                                       (257, 129), (576, 1024), (1024, 576),
+                                       (384, 1000)])
+def test_ragged_shapes_bf16(rows, cols):
+    trip = case(rows, cols, 1)
+    inp, wexp, oexp, _ = gpu_step([trip])
+    ref = oracle_step(inp[0])
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref)
+
+
+@pytest.mark.parametrize("nesterov", [False, True])
+def test_f32_grad_bf16_weight_nesterov_flag(nesterov):
+    trip = case(192, 320, 2, g_dtype=torch.float32)
+    inp, wexp, oexp, _ = gpu_step([trip], nesterov=nesterov)
+    ref = oracle_step(inp[0], nesterov=nesterov)
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref)
+
+
+def test_grouped_matches_oracle_and_standalone_bitexact():
+    shapes = [(256, 768), (768, 256), (512, 512), (130, 390), (64, 64)]
+    trips = [case(r, c, 10 + i) for i, (r, c) in enumerate(shapes)]
+    clones = [[t.clone() for t in tr] for tr in trips]
+    inp, wexp, oexp, _ = gpu_step(trips)
+    for i, tr in enumerate(trips):
+        ref = oracle_step(inp[i])
+        check_against_oracle(tr, inp[i], wexp[i], oexp[i], ref)
+    # each matrix stepped alone gives the same bits
+    for i, tr in enumerate(clones):
+        _, w1, o1, _ = gpu_step([tr])
+        assert torch.equal(o1[0], oexp[i]), shapes[i]
+        assert torch.equal(tr[0], trips[i][0]) and torch.equal(tr[2], trips[i][2])
+
+
+def test_groups_from_a_small_workspace_bitexact():
+    shapes = [(256, 512), (512, 256), (384, 384), (128, 640)]
+    trips = [case(r, c, 30 + i) for i, (r, c) in enumerate(shapes)]
+    clones = [[t.clone() for t in tr] for tr in trips]
+    _, _, o_big, opt = gpu_step(trips)
+    mn, full = opt.workspace_size()
+    _, _, o_small, opt2 = gpu_step(clones, max_workspace=mn)
+    assert opt2.plan_info()["groups"] > 1
+    for a, b in zip(o_big, o_small):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("rows,cols,nb", [(256, 1024, 4), (1024, 512, 4),
+                                          (300, 600, 3), (128, 2048, 8)])
+def test_blockwise_matches_oracle(rows, cols, nb):
+    trip = case(rows, cols, 40)
+    inp, wexp, oexp, _ = gpu_step([trip], mode="blockwise", nb=nb)
+    ref = oracle_step(inp[0], mode="blockwise", nb=nb)
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref,
+                         mode="blockwise", nb=nb)
+
+
+def test_blockwise_nb1_is_full_bitexact():
+    t1 = case(320, 640, 50)
+    t2 = [t.clone() for t in t1]
+    _, _, o1, _ = gpu_step([t1])
+    _, _, o2, _ = gpu_step([t2], mode="blockwise", nb=1)
+    assert torch.equal(o1[0], o2[0]) and torch.equal(t1[0], t2[0])
+
+
+def test_blockwise_block_is_full_on_the_copied_block_bitexact():
+    t = case(256, 1024, 51)
+    blk = [x[:, 512:768].contiguous() for x in t]
+    _, _, o_all, _ = gpu_step([t], mode="blockwise", nb=4)
+    _, _, o_blk, _ = gpu_step([blk])
+    assert torch.equal(o_all[0][:, 512:768], o_blk[0])
+
+
+def test_transpose_invariance_bitexact():
+    t = case(192, 448, 60)
+    tt = [x.t().contiguous() for x in t]
+    _, _, o1, _ = gpu_step([t])
+    _, _, o2, _ = gpu_step([tt])
+    assert torch.equal(o1[0], o2[0].t())
+
+
+def test_zero_gradient_leaves_weight_unchanged():
+    W, G, M = case(160, 288, 70, momentum="zero")
+    G.zero_()
+    W0 = W.clone()
+    _, wexp, oexp, _ = gpu_step([[W, G, M]])
+    assert torch.equal(W, W0)
+    assert torch.count_nonzero(oexp[0]) == 0
+    assert not torch.isnan(wexp[0]).any()
+
+
+def test_repeat_runs_bitexact():
+    t1 = case(300, 700, 80)
+    t2 = [x.clone() for x in t1]
+    _, _, o1, _ = gpu_step([t1], steps=2)
+    _, _, o2, _ = gpu_step([t2], steps=2)
+    assert torch.equal(o1[0], o2[0]) and torch.equal(t1[0], t2[0])
+    assert torch.equal(t1[2], t2[2])
+
+
+def test_ns_steps_and_coefficients_are_honoured():
+    trip = case(256, 384, 90)
+    coeffs = (2.0, -1.5, 0.5)
+    inp, wexp, oexp, _ = gpu_step([trip], ns_steps=3, coeffs=coeffs)
+    ref = oracle_step(inp[0], ns_steps=3, coeffs=coeffs)
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref)
+
+
+def test_output_singular_values_in_band():
+    """Normalised singular values >= 1.5e-3 map into p^5's band."""
+    trip = case(256, 1024, 95, momentum="zero")
+    inp, _, oexp, _ = gpu_step([trip], nesterov=False)
+    s_out = np.linalg.svd(to_np(oexp[0]), compute_uv=False)
+    assert s_out.min() > 0.6818 - 0.03 and s_out.max() < 1.2024 + 0.03
