@@ -1,0 +1,414 @@
+"""Benchmark of the Muon optimizer step (libmuon on one GB300 per rank).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+A step is one full Muon step (momentum, normalisation, five Newton-Schulz
+iterations, weight update) over every matrix of the workload, with a fresh
+synthetic gradient written before each step (outside the timed events).
+The metric is Muon-step TFLOP/s in useful FLOPs (symmetric products counted
+on their upper triangle); GEMM-equivalent TFLOP/s, % of the measured dense
+bf16 peak, ms/step and matrices/s are reported beside it.  L2 is flushed
+(a 512 MiB write) before every timed step.  Prints one JSON line on rank 0.
+
+With N > 1 (torchrun) every rank runs the whole workload on its own GPU as an
+independent replica (weak scaling); value = all ranks' FLOPs / the slowest
+rank's time.  --impl reference times the float64 CPU oracle instead, on a
+bounded sample of the same workload, with the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("Muon-step TFLOP/s (useful & GEMM-equiv) and % bf16 peak; "
+          "ms/step per layer set")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,"
+         "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        mx = max(r[1] for r in rows)
+        loaded = [r for r in rows if r[0] > 0.5 * mx] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[2])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows)}
+
+
+def traffic_for(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    src = os.path.join(ROOT, "newton_schulz_06_gb300", "csrc", "ns_kernels.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    ent = d.get(kernel)
+    if not ent or ent.get("source_sha") != h:
+        return None
+    return ent.get("bytes_per_launch_full_workload")
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x: float) -> float:
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(wl, max_flops=2.2e12):
+    """A bounded sample of the workload for the CPU oracle: its matrices in
+    order until about `max_flops` GEMM-equivalent FLOPs (at least one)."""
+    from newton_schulz_06_gb300 import flops
+    picked, tot = [], 0
+    for i, s in enumerate(wl.shapes):
+        f = flops.gemm_equiv_flops([s], mode=wl.mode, nb=wl.nb)
+        if picked and tot + f > max_flops:
+            continue
+        picked.append(i)
+        tot += f
+        if tot >= max_flops:
+            break
+    return picked
+
+
+def time_oracle(wl, idx_list, host_inputs, reps=1):
+    """Seconds per oracle step over the sampled matrices, useful FLOPs."""
+    import numpy as np
+    import oracle
+    from newton_schulz_06_gb300 import flops
+    a, b, c = (float(np.float32(x)) for x in (3.4445, -4.7750, 2.0315))
+    useful = flops.useful_flops([wl.shapes[i] for i in idx_list],
+                                mode=wl.mode, nb=wl.nb)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        for W, G, M in host_inputs:
+            oracle.muon_step(W, G, M, lr=0.02, beta=float(np.float32(0.95)),
+                             nesterov=True, ns_steps=5, a=a, b=b, c=c,
+                             mode=wl.mode, nb=wl.nb)
+    return (time.perf_counter() - t0) / reps, useful
+
+
+def host_sample(wl, idx_list):
+    """Float64 host copies of the sampled matrices' first-step inputs,
+    generated on the CPU from the same seeded recipe."""
+    import torch
+    from newton_schulz_06_gb300 import inputs as I
+    out = []
+    for i in idx_list:
+        r, c = wl.shapes[i]
+        W = I.make_weight((r, c), wl.w_dtype, "cpu", wl.name, i)
+        M = I.make_momentum((r, c), wl.init_momentum, "cpu", wl.name, i)
+        G = torch.empty((r, c), dtype=wl.g_dtype)
+        I.fill_grad(G, wl, i, 0)
+        out.append(tuple(t.to(torch.float64).numpy() for t in (W, G, M)))
+    return out
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return None
+    from newton_schulz_06_gb300 import flops
+    idx = oracle_sample(wl)
+    host = host_sample(wl, idx)
+    full_useful = flops.useful_flops(wl.shapes, mode=wl.mode, nb=wl.nb)
+    times = []
+    for k in range(args.warmup + args.steps):
+        dt, useful = time_oracle(wl, idx, host)
+        if k >= args.warmup:
+            times.append(dt)
+    sec = statistics.mean(times)
+    tflops = useful / sec / 1e12
+    sample = (f"{len(idx)} of {wl.n_matrices} matrices "
+              f"({useful / full_useful:.3%} of the step's useful FLOPs), "
+              f"one float64 oracle step each per timed step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": sec * 1e3 * full_useful / useful,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "matrices": wl.n_matrices,
+                   "mode": wl.mode, "nb": wl.nb, "ns_steps": 5},
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s",
+                         "cores": cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def run_ours(args, wl, world, rank, local, pg):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from newton_schulz_06_gb300 import MUON_BLOCKWISE, MUON_FULL, Muon, flops
+    from newton_schulz_06_gb300 import inputs as I
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    peaks, peak_kind = load_peaks()
+    Ws, Gs, Ms = I.make_state(wl, dev)
+    trips = list(zip(Ws, Gs, Ms))
+    opt = Muon(trips)
+    mode = MUON_BLOCKWISE if wl.mode == "blockwise" else MUON_FULL
+    opt.ensure_workspace(mode, wl.nb, args.max_workspace)
+    info = opt.plan_info(mode, wl.nb)
+    useful = flops.useful_flops(wl.shapes, mode=wl.mode, nb=wl.nb)
+    gemm_eq = flops.gemm_equiv_flops(wl.shapes, mode=wl.mode, nb=wl.nb)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fresh_grads(step):
+        for i, G in enumerate(Gs):
+            if wl.grad == "log_scale_step" or step == 0:
+                I.fill_grad(G, wl, i, step)
+
+    kw = dict(lr=0.02, beta=0.95, nesterov=True, ns_steps=5, mode=mode,
+              nb=wl.nb)
+    for k in range(args.warmup):
+        fresh_grads(k + 1)
+        opt.step(**kw)
+    opt.sync()
+    torch.cuda.synchronize()
+
+    opt.set_profiling(True)
+    stage_tot = {}
+    ev = [(torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    barrier(pg)
+    torch.cuda.synchronize()
+    sampler.start()
+    wall0 = time.perf_counter()
+    launches = 0
+    for k in range(args.steps):
+        fresh_grads(args.warmup + k + 1)
+        flush.zero_()
+        ev[k][0].record(stream)
+        opt.step(**kw)
+        ev[k][1].record(stream)
+        launches += opt.last_launch_count()
+        opt.sync()
+        for name, (ms, n) in opt.stage_times().items():
+            t, c = stage_tot.get(name, (0.0, 0))
+            stage_tot[name] = (t + ms, c + n)
+    torch.cuda.synchronize()
+    barrier(pg)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(step_ms)
+    ms = max_over_ranks(pg, ms)
+    opt.set_profiling(False)
+
+    # end to end through the public API with host buffers: H2D of the
+    # step's gradients from pinned memory, the step, D2H of the weights
+    pinned_g = [torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
+                for G in Gs]
+    for i, G in enumerate(Gs):
+        pinned_g[i].copy_(G)
+    pinned_w = [torch.empty(W.shape, dtype=W.dtype, pin_memory=True)
+                for W in Ws]
+    h2d = sum(t.numel() * t.element_size() for t in pinned_g)
+    d2h = sum(t.numel() * t.element_size() for t in pinned_w)
+    e2e_ms = []
+    for k in range(max(3, min(args.steps, 10))):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for G, P in zip(Gs, pinned_g):
+            G.copy_(P, non_blocking=True)
+        opt.step(**kw)
+        for W, P in zip(Ws, pinned_w):
+            P.copy_(W, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e = statistics.mean(e2e_ms)
+    e2e = max_over_ranks(pg, e2e)
+
+    # dominant tensor-core kernel: per-launch algorithmic FLOPs / event time
+    units = []
+    for r, c in wl.shapes:
+        units += flops.unit_shapes(r, c, wl.mode, wl.nb)
+    per_launch = {
+        "gemm": sum(2 * m * m * n for m, n in units),
+        "syrk1": sum(m * (m + 1) * n for m, n in units),
+        "syrk2": sum(m * (m + 1) * m for m, n in units),
+    }
+    dom = max(per_launch, key=lambda k: stage_tot.get(k, (0, 1))[0])
+    t_dom, n_dom = stage_tot[dom]
+    avg_launch_s = t_dom / n_dom / 1e3
+    achieved = per_launch[dom] / avg_launch_s / 1e12
+    peak = peaks["bf16_tflops"]
+    kname = {"gemm": "ns_kernel<2>", "syrk1": "ns_kernel<0>",
+             "syrk2": "ns_kernel<1>"}[dom]
+    roofline = {"bound": "tensor", "kernel": kname, "stage": dom,
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_kind": f"{peak_kind} dense bf16 (burst)",
+                "traffic": traffic_for(kname),
+                "avg_launch_ms": t_dom / n_dom}
+
+    value = world * useful / (ms / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "matrices": wl.n_matrices,
+                   "elements": wl.n_elements, "mode": wl.mode, "nb": wl.nb,
+                   "ns_steps": 5, "groups": info["groups"],
+                   "l2": "flushed (512 MiB write) before every timed step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "gemm_equiv_tflops": world * gemm_eq / (ms / 1e3) / 1e12,
+        "pct_bf16_peak_useful": 100.0 * useful / (ms / 1e3) / 1e12 / peak,
+        "pct_bf16_peak_gemm_equiv": 100.0 * gemm_eq / (ms / 1e3) / 1e12 / peak,
+        "matrices_per_s": world * wl.n_matrices / (ms / 1e3),
+        "useful_tflop_per_step": useful / 1e12,
+        "gemm_equiv_tflop_per_step": gemm_eq / 1e12,
+        "stage_ms_per_step": {k: v[0] / args.steps for k, v in stage_tot.items()},
+        "wall_s_timed_region": wall,
+        "clocks": clocks,
+        "e2e": {"value": world * useful / (e2e / 1e3) / 1e12,
+                "unit": "TFLOP/s", "ms_per_step": e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "roofline": roofline,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        idx = oracle_sample(wl)
+        host = host_sample(wl, idx)
+        dt, u = time_oracle(wl, idx, host)
+        full_useful = flops.useful_flops(wl.shapes, mode=wl.mode, nb=wl.nb)
+        line["cpu_baseline"] = {
+            "value": u / dt / 1e12, "unit": "TFLOP/s", "cores": cores(),
+            "kind": "oracle",
+            "sample": (f"{len(idx)} of {wl.n_matrices} matrices "
+                       f"({u / full_useful:.3%} of the step's useful FLOPs), "
+                       f"one float64 oracle step, {dt:.1f} s")}
+    opt.close()
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="square_4096_bf16")
+    ap.add_argument("--max-workspace", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from newton_schulz_06_gb300 import inputs as I
+    wl = I.workload(args.workload)
+    world, rank, local, pg = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, wl, world, rank)
+    else:
+        line = run_ours(args, wl, world, rank, local, pg)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

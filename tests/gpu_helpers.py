@@ -8,7 +8,12 @@ compare with the tolerances of the step:
     update computes before it is stored (bf16 rounding of a N(0, 0.02)
     weight alone is ~1.7e-3), plus a bit-exact check that the stored bf16
     weight is the round-to-nearest-even of that fp32 value; fp32 weights are
-    compared directly;
+    compared directly.  The weight error is the O error scaled by
+    r = lr*scale*||O|| / ||W||, so the 1e-3 gate holds where r <= 1/30 (every
+    model-sized matrix); for small test matrices with a larger r the gate is
+    3e-2 * r.  Independently of size, the fp32 weight must equal
+    W - lr*scale*O_gpu within fp32 rounding (the update applied exactly the
+    exported O);
   * momentum: fp32 M = fma(beta, M, G) against the float64 value, within
     one fp32 rounding.
 """
@@ -89,7 +94,18 @@ def check_against_oracle(triple, inp, wexp, oexp, ref, *, mode="full", nb=1):
     assert errs["O"] <= O_TOL, errs
     w32 = to_np(wexp)
     errs["W"] = relF(w32, ref["W"])
-    assert errs["W"] <= W_TOL, errs
+    W_in = inp[0]
+    step = np.linalg.norm(ref["W"] - W_in)
+    ratio = step / max(np.linalg.norm(ref["W"]), 1e-300)
+    w_tol = max(W_TOL, O_TOL * ratio)
+    errs["W_tol"] = w_tol
+    assert errs["W"] <= w_tol, errs
+    # the update applied the exported O exactly (fp32 fma, one rounding)
+    if step > 0:
+        lr_s = step / max(np.linalg.norm(ref["O"]), 1e-300)
+        implied = W_in - lr_s * O_gpu
+        slack = 2.0 ** -22 * (np.abs(W_in) + np.abs(lr_s * O_gpu)) + 1e-12
+        assert np.all(np.abs(w32 - implied) <= slack * 4), "update != W - lr*s*O"
     if W.dtype == torch.bfloat16:
         assert torch.equal(W, wexp.to(torch.bfloat16)), "stored W != RNE(fp32)"
     else:
