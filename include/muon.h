@@ -179,6 +179,45 @@ typedef struct {
 } muon_plan_info;
 MUON_API int muon_get_plan_info(muon_handle h, int mode, int nb, muon_plan_info* out);
 
+/* ---- step without a workspace ------------------------------------------ */
+
+/* One Muon step (full mode) on ONE matrix without any workspace: the plan
+ * tables and every intermediate (partial sums, the two iterates X, and A, B)
+ * live in a fixed 32 MiB array inside the library.  This is for callers who
+ * cannot call cudaMalloc or hand over a buffer: a plugin whose host owns all
+ * device memory through a pool it does not expose, a process whose caching
+ * allocator has already reserved the GPU, or a hot loop that cannot afford
+ * cudaMalloc's implicit device synchronisation.  The paper has no
+ * counterpart of this entry point; it is a convenience of this library.
+ *
+ *   param          one matrix as for muon_register_params (device pointers;
+ *                  W and M updated in place, G read only)
+ *   lr ... c       as for muon_step
+ *   cuda_stream    stream for the work (NULL = legacy default stream); the
+ *                  CUDA device is the caller's current device
+ *   err, err_len   optional buffer that receives a message on error
+ *
+ * Limits and behaviour:
+ *   - The matrix must fit the fixed array: roughly 4 bytes per element of
+ *     the matrix plus 4 bytes per element of its m x m square (m = short
+ *     side), plus small tables, at most 33554432 bytes in total (a 1024 x
+ *     4096 matrix fits, a 2048 x 2048 does not).  Larger matrices are
+ *     rejected with MUON_ERR_UNSUPPORTED and a message before any GPU work.
+ *   - The array exists once per device that loads this code and is held
+ *     until the process exits.  The first call on a device resolves its
+ *     address (cudaGetSymbolAddress) with that device current.
+ *   - Every call reuses the same array and overwrites what the previous
+ *     call left there; calls whose GPU work overlaps (different streams or
+ *     threads) race and give wrong results.  Queue them on one stream.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.  The work is
+ *     queued asynchronously; a bounded GPU wait that runs out makes the
+ *     kernels return early, which this entry point cannot report (use the
+ *     handle-based muon_step and muon_sync where that report matters). */
+MUON_API int muon_step_noalloc(const muon_param* param, float lr, float beta,
+                               int nesterov, int ns_steps, float a, float b,
+                               float c, void* cuda_stream, char* err,
+                               size_t err_len);
+
 #ifdef __cplusplus
 }
 #endif

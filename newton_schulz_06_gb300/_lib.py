@@ -33,7 +33,8 @@ EXPORTS = ("muon_create", "muon_set_stream", "muon_register_params",
            "muon_workspace_size", "muon_set_workspace", "muon_step",
            "muon_sync", "muon_destroy", "muon_last_error",
            "muon_set_profiling", "muon_stage_times", "muon_last_launch_count",
-           "muon_debug_set_exports", "muon_get_plan_info")
+           "muon_debug_set_exports", "muon_get_plan_info",
+           "muon_step_noalloc")
 
 
 class MuonParam(ctypes.Structure):
@@ -95,6 +96,8 @@ def lib() -> ctypes.CDLL:
         "muon_debug_set_exports": [H, i32, ctypes.POINTER(vp),
                                    ctypes.POINTER(vp)],
         "muon_get_plan_info": [H, i32, i32, ctypes.POINTER(MuonPlanInfo)],
+        "muon_step_noalloc": [ctypes.POINTER(MuonParam), f32, f32, i32, i32,
+                              f32, f32, f32, vp, ctypes.c_char_p, sz],
     }
     for name, args in sig.items():
         fn = getattr(L, name)

@@ -21,7 +21,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmuon.so")
-SOURCES = ["ew_kernels.cu", "ns_kernels.cu", "muon_api.cpp"]
+SOURCES = ["ew_kernels.cu", "ns_kernels.cu", "muon_api.cpp", "muon_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "muon_internal.h"),
            os.path.join(ROOT, "include", "muon.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
