@@ -100,17 +100,23 @@ class ClockSampler:
                 "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows)}
 
 
-def traffic_for(kernel: str):
+def source_sha(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+    on the current source of that kernel and on this workload; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
-    src = os.path.join(ROOT, "newton_schulz_06_gb300", "csrc", "ns_kernels.cu")
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    ent = d.get(kernel)
-    if not ent or ent.get("source_sha") != h:
+    ent = json.load(open(p)).get(kernel)
+    if not ent or ent.get("workload") != workload:
+        return None
+    if ent.get("source_sha") != source_sha(ent.get("source_files", [])):
         return None
     return ent.get("bytes_per_launch_full_workload")
 
@@ -337,13 +343,14 @@ def run_ours(args, wl, world, rank, local, pg):
     avg_launch_s = t_dom / n_dom / 1e3
     achieved = per_launch[dom] / avg_launch_s / 1e12
     peak = peaks["bf16_tflops"]
-    kname = {"gemm": "ns_kernel<2>", "syrk1": "ns_kernel<0>",
-             "syrk2": "ns_kernel<1>"}[dom]
+    op = {"gemm": 2, "syrk1": 0, "syrk2": 1}[dom]
+    pair = os.environ.get("MUON_CTA_GROUP", "2") != "1"
+    kname = f"ns2_kernel<{op}>" if pair else f"ns_kernel<{op}>"
     roofline = {"bound": "tensor", "kernel": kname, "stage": dom,
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
                 "peak_kind": f"{peak_kind} dense bf16 (burst)",
-                "traffic": traffic_for(kname),
+                "traffic": traffic_for(kname, wl.name),
                 "avg_launch_ms": t_dom / n_dom}
 
     value = world * useful / (ms / 1e3) / 1e12

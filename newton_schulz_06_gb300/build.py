@@ -21,8 +21,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmuon.so")
-SOURCES = ["ew_kernels.cu", "ns_kernels.cu", "muon_api.cpp", "muon_noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "muon_internal.h"),
+SOURCES = ["ew_kernels.cu", "ns_kernels.cu", "ns2_kernels.cu", "muon_api.cpp",
+           "muon_noalloc.cu"]
+HEADERS = [os.path.join(CSRC, "muon_internal.h"), os.path.join(CSRC, "tc_ptx.cuh"),
            os.path.join(ROOT, "include", "muon.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -94,6 +94,8 @@ struct muon_ctx {
     int last_launch_count = 0;
     unsigned long long wait_limit_ns = 2000000000ull;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    bool pair = true;          // CTA-pair kernels (256 x 256 tiles)
+    int max_pairs = 0;
 };
 
 namespace {
@@ -126,23 +128,34 @@ struct DeviceGuard {
 size_t elem_size(int dtype) { return dtype == MUON_F32 ? 4 : 2; }
 
 // Per-unit work counts shared by planning and plan statistics.
-void unit_tiles(const UnitDesc& u, int64_t* syrk, int64_t* gemm,
+//   single-CTA tiles: 128 x 256 (symmetric: 128-column halves below the
+//   diagonal or past m skipped); CTA-pair tiles: 256 x 256 (symmetric:
+//   ti <= tj on the 256 grid).
+void unit_tiles(const UnitDesc& u, bool pair, int64_t* syrk, int64_t* gemm,
                 int64_t* useful, int64_t* executed) {
     const int64_t m = u.m, n = u.n;
-    const int64_t T = ceil_div(m, BM);
-    int64_t s = 0, ex = 0;
-    for (int64_t ti = 0; ti < T; ++ti)
-        for (int64_t tj = 0; tj < ceil_div(T, 2); ++tj) {
-            const int64_t bl = 2 * tj, br = 2 * tj + 1;
-            const int nl = (bl < T && bl >= ti) + (br < T && br >= ti);
-            if (!nl) continue;
-            ++s;
-            ex += 2 * BM * 128 * nl * (ceil_div(n, BK) * BK + ceil_div(m, BK) * BK);
+    const int64_t kn = ceil_div(n, BK) * BK, km = ceil_div(m, BK) * BK;
+    int64_t s = 0, g = 0, ex = 0;
+    if (pair) {
+        const int64_t T2 = ceil_div(m, 256);
+        s = T2 * (T2 + 1) / 2;
+        g = T2 * ceil_div(n, 256);
+        ex = s * 2 * 256 * 256 * (kn + km) + g * 2 * 256 * 256 * km;
+    } else {
+        const int64_t T = ceil_div(m, BM);
+        for (int64_t ti = 0; ti < T; ++ti)
+            for (int64_t tj = 0; tj < ceil_div(T, 2); ++tj) {
+                const int64_t bl = 2 * tj, br = 2 * tj + 1;
+                const int nl = (bl < T && bl >= ti) + (br < T && br >= ti);
+                if (!nl) continue;
+                ++s;
+                ex += 2 * BM * 128 * nl * (kn + km);
+            }
+        g = T * ceil_div(n, BN);
+        for (int64_t tj = 0; tj < ceil_div(n, BN); ++tj) {
+            const int64_t nl = std::min<int64_t>(BN, align_up(n - tj * BN, 16));
+            ex += T * 2 * BM * nl * km;
         }
-    const int64_t g = T * ceil_div(n, BN);
-    for (int64_t tj = 0; tj < ceil_div(n, BN); ++tj) {
-        const int64_t nl = std::min<int64_t>(BN, align_up(n - tj * BN, 16));
-        ex += T * 2 * BM * nl * ceil_div(m, BK) * BK;
     }
     *syrk = s;
     *gemm = g;
@@ -195,8 +208,12 @@ int build_units(muon_ctx* h, int mode, int nb, std::vector<UnitDesc>* out) {
 size_t meta_bound(const std::vector<UnitDesc>& units) {
     size_t b = 0;
     for (const UnitDesc& u : units) {
-        int64_t s, g, x, y;
-        unit_tiles(u, &s, &g, &x, &y);
+        // the larger of the two tilings bounds either
+        int64_t s, g, x, y, s2, g2;
+        unit_tiles(u, false, &s, &g, &x, &y);
+        unit_tiles(u, true, &s2, &g2, &x, &y);
+        s = std::max(s, s2);
+        g = std::max(g, g2);
         b += sizeof(EwUnit) + sizeof(NsUnit) + 5 * 256 +
              size_t(2 * s + g) * sizeof(TileItem);
     }
@@ -370,40 +387,68 @@ int build_plan(muon_ctx* h, int mode, int nb) {
 
             // tile lists
             const int li = i - g.u0;
-            const int64_t T = ceil_div(u.m, BM);
             const int kx = static_cast<int>(ceil_div(u.n, BK));
             const int km = static_cast<int>(ceil_div(u.m, BK));
-            for (int64_t ti = 0; ti < T; ++ti)
-                for (int64_t tj = 0; tj < ceil_div(T, 2); ++tj) {
-                    const int64_t bl = 2 * tj, br = 2 * tj + 1;
-                    const bool lneed = bl < T && bl >= ti;
-                    const bool rneed = br < T && br >= ti;
-                    if (!lneed && !rneed) continue;
-                    TileItem t;
-                    t.unit = li;
-                    t.ti = static_cast<int16_t>(ti);
-                    t.tj = static_cast<int16_t>(tj);
-                    t.n_off = lneed ? 0 : 128;
-                    t.n_len = static_cast<int16_t>(128 * (int(lneed) + int(rneed)));
-                    t.k_blocks = kx;
-                    tsx.push_back(t);
-                    t.k_blocks = km;
-                    tsa.push_back(t);
-                }
-            for (int64_t ti = 0; ti < T; ++ti)
-                for (int64_t tj = 0; tj < ceil_div(u.n, BN); ++tj) {
-                    TileItem t;
-                    t.unit = li;
-                    t.ti = static_cast<int16_t>(ti);
-                    t.tj = static_cast<int16_t>(tj);
-                    t.n_off = 0;
-                    t.n_len = static_cast<int16_t>(
-                        std::min<int64_t>(BN, align_up(u.n - tj * BN, 16)));
-                    t.k_blocks = km;
-                    tg.push_back(t);
-                }
+            if (h->pair) {
+                const int64_t T2 = ceil_div(u.m, 256);
+                for (int64_t ti = 0; ti < T2; ++ti)
+                    for (int64_t tj = ti; tj < T2; ++tj) {
+                        TileItem t;
+                        t.unit = li;
+                        t.ti = static_cast<int16_t>(ti);
+                        t.tj = static_cast<int16_t>(tj);
+                        t.n_off = 0;
+                        t.n_len = 256;
+                        t.k_blocks = kx;
+                        tsx.push_back(t);
+                        t.k_blocks = km;
+                        tsa.push_back(t);
+                    }
+                for (int64_t ti = 0; ti < T2; ++ti)
+                    for (int64_t tj = 0; tj < ceil_div(u.n, 256); ++tj) {
+                        TileItem t;
+                        t.unit = li;
+                        t.ti = static_cast<int16_t>(ti);
+                        t.tj = static_cast<int16_t>(tj);
+                        t.n_off = 0;
+                        t.n_len = 256;
+                        t.k_blocks = km;
+                        tg.push_back(t);
+                    }
+            } else {
+                const int64_t T = ceil_div(u.m, BM);
+                for (int64_t ti = 0; ti < T; ++ti)
+                    for (int64_t tj = 0; tj < ceil_div(T, 2); ++tj) {
+                        const int64_t bl = 2 * tj, br = 2 * tj + 1;
+                        const bool lneed = bl < T && bl >= ti;
+                        const bool rneed = br < T && br >= ti;
+                        if (!lneed && !rneed) continue;
+                        TileItem t;
+                        t.unit = li;
+                        t.ti = static_cast<int16_t>(ti);
+                        t.tj = static_cast<int16_t>(tj);
+                        t.n_off = lneed ? 0 : 128;
+                        t.n_len = static_cast<int16_t>(128 * (int(lneed) + int(rneed)));
+                        t.k_blocks = kx;
+                        tsx.push_back(t);
+                        t.k_blocks = km;
+                        tsa.push_back(t);
+                    }
+                for (int64_t ti = 0; ti < T; ++ti)
+                    for (int64_t tj = 0; tj < ceil_div(u.n, BN); ++tj) {
+                        TileItem t;
+                        t.unit = li;
+                        t.ti = static_cast<int16_t>(ti);
+                        t.tj = static_cast<int16_t>(tj);
+                        t.n_off = 0;
+                        t.n_len = static_cast<int16_t>(
+                            std::min<int64_t>(BN, align_up(u.n - tj * BN, 16)));
+                        t.k_blocks = km;
+                        tg.push_back(t);
+                    }
+            }
             int64_t s, gg, us, ex;
-            unit_tiles(u, &s, &gg, &us, &ex);
+            unit_tiles(u, h->pair, &s, &gg, &us, &ex);
             P.useful_flops_iter += us;
             P.executed_flops_iter += ex;
         }
@@ -457,10 +502,13 @@ extern "C" {
 int muon_create(muon_handle* out, int device, void* cuda_stream) {
     if (!out) return fail(nullptr, MUON_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
+    const char* cg = std::getenv("MUON_CTA_GROUP");
+    const bool pair = !(cg && std::string(cg) == "1");
     if (device == MUON_HOST_ONLY) {
         muon_ctx* h = new muon_ctx();
         h->device = MUON_HOST_ONLY;
         h->num_sms = 148;
+        h->pair = pair;
         *out = h;
         return MUON_OK;
     }
@@ -492,6 +540,14 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
         return fail(nullptr, MUON_ERR_CUDA, "cuTensorMapEncodeTiled not available");
     }
     h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    h->pair = pair;
+    if (pair) {
+        h->max_pairs = ns_pair_max_clusters();
+        if (h->max_pairs < 1) {
+            delete h;
+            return fail(nullptr, MUON_ERR_CUDA, "no CTA pair fits on the device");
+        }
+    }
     if (const char* s = std::getenv("MUON_WAIT_LIMIT_MS")) {
         const long long ms = std::atoll(s);
         if (ms > 0) h->wait_limit_ns = static_cast<unsigned long long>(ms) * 1000000ull;
@@ -645,9 +701,11 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
             for (const auto& q : seq) {
                 L.tiles = reinterpret_cast<const TileItem*>(ws + q.off);
                 L.num_tiles = q.n;
-                const int grid = std::min(q.n, h->num_sms);
                 if (!begin(q.st)) return fail(h, MUON_ERR_CUDA, "event create");
-                e = launch_ns(q.op, L, grid, h->stream);
+                if (h->pair)
+                    e = launch_ns_pair(q.op, L, std::min(q.n, h->max_pairs), h->stream);
+                else
+                    e = launch_ns(q.op, L, std::min(q.n, h->num_sms), h->stream);
                 end();
                 if (e != cudaSuccess) return cuda_fail(h, e, "tensor-core stage launch");
             }
@@ -755,7 +813,7 @@ int muon_get_plan_info(muon_handle h, int mode, int nb, muon_plan_info* out) {
     out->units = static_cast<int64_t>(units.size());
     for (const UnitDesc& u : units) {
         int64_t s, g, us, ex;
-        unit_tiles(u, &s, &g, &us, &ex);
+        unit_tiles(u, h->pair, &s, &g, &us, &ex);
         out->syrk_tiles += s;
         out->gemm_tiles += g;
         out->ew_tiles += u.ew_tiles;

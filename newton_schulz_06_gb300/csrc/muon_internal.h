@@ -101,5 +101,8 @@ cudaError_t launch_ew_normalise(const EwLaunch& p, int grid, cudaStream_t s);
 cudaError_t launch_ew_update(const EwLaunch& p, int grid, cudaStream_t s);
 cudaError_t launch_ns(NsOp op, const NsLaunch& p, int grid, cudaStream_t s);
 size_t ns_smem_bytes();
+// CTA-pair (cta_group::2) kernels on 256 x 256 tiles; `pairs` clusters of 2.
+cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, cudaStream_t s);
+int ns_pair_max_clusters();
 
 }  // namespace muon

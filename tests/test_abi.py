@@ -47,22 +47,35 @@ def _planner(shapes, **kw):
     return HostPlanner(shapes, **kw)
 
 
-def _syrk_tiles(m):
+def _syrk_tiles(m, pair):
+    if pair:
+        T2 = -(-m // 256)
+        return sum(1 for ti in range(T2) for tj in range(T2) if tj >= ti)
     T = -(-m // 128)
     return sum(1 for ti in range(T) for tj in range(-(-T // 2))
                if any(2 * tj + h < T and 2 * tj + h >= ti for h in (0, 1)))
 
 
+@pytest.mark.parametrize("pair", [True, False])
 @pytest.mark.parametrize("shape", [(4096, 4096), (768, 2048), (2048, 768),
                                    (576, 7168), (100, 37), (8, 16)])
-def test_plan_tile_counts(L, shape):
+def test_plan_tile_counts(L, shape, pair, monkeypatch):
+    monkeypatch.setenv("MUON_CTA_GROUP", "2" if pair else "1")
     p = _planner([shape])
     info = p.plan_info()
     m, n = min(shape), max(shape)
+    rows = 256 if pair else 128
     assert info["units"] == 1 and info["groups"] == 1
-    assert info["syrk_tiles"] == _syrk_tiles(m)
-    assert info["gemm_tiles"] == (-(-m // 128)) * (-(-n // 256))
+    assert info["syrk_tiles"] == _syrk_tiles(m, pair)
+    assert info["gemm_tiles"] == (-(-m // rows)) * (-(-n // 256))
     assert info["ew_tiles"] == (-(-m // 64)) * (-(-n // 64))
+    # executed FLOPs: every tile's MACs over the zero-padded K
+    kn, km = -(-n // 64) * 64, -(-m // 64) * 64
+    if pair:
+        ex = 2 * 256 * 256 * (info["syrk_tiles"] * (kn + km) +
+                              info["gemm_tiles"] * km)
+        assert info["executed_flops"] == ex
+    assert info["executed_flops"] >= info["useful_flops"]
 
 
 def test_useful_flops_match_formula(L):
