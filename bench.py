@@ -403,11 +403,16 @@ def main():
     ap.add_argument("--workload", default="square_4096_bf16")
     ap.add_argument("--max-workspace", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--max-matrices", type=int, default=None,
+                    help="profiling aid: keep only the first N matrices")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     from newton_schulz_06_gb300 import inputs as I
     wl = I.workload(args.workload)
+    if args.max_matrices:
+        wl.shapes = wl.shapes[:args.max_matrices]
+        wl.name = f"{wl.name}[:{args.max_matrices}]"
     world, rank, local, pg = dist_setup(args)
     if args.impl == "reference":
         line = run_reference(args, wl, world, rank)

@@ -152,11 +152,21 @@ ew_momentum_kernel(const EwLaunch p) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int xr = i + 16 * k;
+            float xv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int xc = j4 + e;
                 const float v = U.transposed ? sU[xc][xr] : sU[xr][xc];
                 acc = fmaf(v, v, acc);
+                xv[e] = v;
+            }
+            if (p.write_x) {
+                // unnormalised iterate bf16(U), X orientation; the first
+                // iteration applies 1/(||U||+eps)
+                const int gr = g.xr0 + xr, gc = g.xc0 + j4;
+                int nx = (gr < U.m) ? min(4, U.n - gc) : 0;
+                nx = max(nx, 0);
+                st4(U.x[0], MUON_BF16, static_cast<int64_t>(gr) * U.ld_x + gc, nx, true, xv);
             }
         }
         const float s = block_sum(acc, red);

@@ -95,6 +95,8 @@ struct muon_ctx {
     unsigned long long wait_limit_ns = 2000000000ull;
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     bool pair = true;          // CTA-pair kernels (256 x 256 tiles)
+    bool fuse = true;          // pair mode: normalisation fused into iteration 1
+    bool fuse_update = false;  // pair mode: update fused into the last GEMM
     int max_pairs = 0;
 };
 
@@ -362,6 +364,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
             const size_t ga = pr.g_dtype == MUON_F32 ? 16 : 8;
             e.vec_ok = (u.cols % 4 == 0) && (pr.ld_w % 4 == 0) && (pr.ld_g % 4 == 0) &&
                        (pr.ld_m % 4 == 0) && al(e.w, wa) && al(e.g, ga) && al(e.mom, 16);
+            e.vec16 = al(e.w, 16) && ((pr.ld_w * elem_size(pr.w_dtype)) % 16 == 0);
             e.tiles_n = static_cast<int32_t>(ceil_div(u.n, EW_TILE));
             e.tile_base = tile_base;
             e.tile_count = u.ew_tiles;
@@ -473,11 +476,11 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         // stash scratch offsets in the group (reuse fields via locals below)
         (void)part_off;
     }
+    // pageable source: the copy is staged before cudaMemcpyAsync returns,
+    // so `meta` may go out of scope; stream order protects earlier steps
     cudaError_t e = cudaMemcpyAsync(h->ws, meta.data(), meta.size(),
                                     cudaMemcpyHostToDevice, h->stream);
     if (e != cudaSuccess) return cuda_fail(h, e, "metadata upload");
-    e = cudaStreamSynchronize(h->stream);
-    if (e != cudaSuccess) return cuda_fail(h, e, "metadata upload sync");
     P.mode = mode;
     P.nb = (mode == MUON_BLOCKWISE) ? nb : 1;
     P.ws = h->ws;
@@ -504,6 +507,10 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     *out = nullptr;
     const char* cg = std::getenv("MUON_CTA_GROUP");
     const bool pair = !(cg && std::string(cg) == "1");
+    const char* fz = std::getenv("MUON_FUSE");
+    const bool fuse = !(fz && std::string(fz) == "0");
+    const char* fu = std::getenv("MUON_FUSE_UPDATE");
+    const bool fuse_update = fuse && fu && std::string(fu) == "1";
     if (device == MUON_HOST_ONLY) {
         muon_ctx* h = new muon_ctx();
         h->device = MUON_HOST_ONLY;
@@ -541,6 +548,8 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     }
     h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     h->pair = pair;
+    h->fuse = fuse;
+    h->fuse_update = fuse_update;
     if (pair) {
         h->max_pairs = ns_pair_max_clusters();
         if (h->max_pairs < 1) {
@@ -659,7 +668,7 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         const int nu = g.u1 - g.u0;
         const size_t inv_off = P.scratch_off;
         const size_t part_off = align_up(inv_off + size_t(nu) * 4, 256);
-        EwLaunch ew;
+        EwLaunch ew{};
         ew.units = reinterpret_cast<const EwUnit*>(ws + g.ew_off);
         ew.num_units = nu;
         ew.num_tiles = g.ew_tiles;
@@ -671,6 +680,8 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         ew.src = 0;
         ew.eps = NORM_EPS;
         const int ew_grid = static_cast<int>(std::min<int64_t>(g.ew_tiles, ew_grid_cap));
+        const bool fused = h->pair && h->fuse;
+        ew.write_x = fused ? 1 : 0;
         cudaError_t e;
         if (!begin(ST_MOMENTUM)) return fail(h, MUON_ERR_CUDA, "event create");
         e = launch_ew_momentum(ew, ew_grid, h->stream);
@@ -680,20 +691,27 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         e = launch_ew_norm(ew, h->stream);
         end();
         if (e != cudaSuccess) return cuda_fail(h, e, "norm launch");
-        if (!begin(ST_NORMALISE)) return fail(h, MUON_ERR_CUDA, "event create");
-        e = launch_ew_normalise(ew, ew_grid, h->stream);
-        end();
-        if (e != cudaSuccess) return cuda_fail(h, e, "normalise launch");
-        NsLaunch L;
+        if (!fused) {
+            if (!begin(ST_NORMALISE)) return fail(h, MUON_ERR_CUDA, "event create");
+            e = launch_ew_normalise(ew, ew_grid, h->stream);
+            end();
+            if (e != cudaSuccess) return cuda_fail(h, e, "normalise launch");
+        }
+        NsLaunch L{};
         L.units = reinterpret_cast<const NsUnit*>(ws + g.ns_off);
         L.a = a;
         L.b = b;
         L.c = c;
         L.wait_limit_ns = h->wait_limit_ns;
         L.err = err_word;
+        L.inv_norm = ew.inv_norm;
+        L.ew = ew.units;
+        L.lr = lr;
         int cur = 0;
         for (int s = 0; s < ns_steps; ++s) {
             L.src = cur;
+            L.first = (fused && s == 0) ? 1 : 0;
+            L.last = (fused && h->fuse_update && s == ns_steps - 1) ? 1 : 0;
             const struct { NsOp op; size_t off; int n; int st; } seq[3] = {
                 {OP_SYRK_X, g.t_sx_off, g.n_sx, ST_SYRK1},
                 {OP_SYRK_A, g.t_sa_off, g.n_sa, ST_SYRK2},
@@ -711,11 +729,13 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
             }
             cur ^= 1;
         }
-        ew.src = cur;
-        if (!begin(ST_UPDATE)) return fail(h, MUON_ERR_CUDA, "event create");
-        e = launch_ew_update(ew, ew_grid, h->stream);
-        end();
-        if (e != cudaSuccess) return cuda_fail(h, e, "update launch");
+        if (!(fused && h->fuse_update)) {
+            ew.src = cur;
+            if (!begin(ST_UPDATE)) return fail(h, MUON_ERR_CUDA, "event create");
+            e = launch_ew_update(ew, ew_grid, h->stream);
+            end();
+            if (e != cudaSuccess) return cuda_fail(h, e, "update launch");
+        }
     }
     h->last_launch_count = count;
     return MUON_OK;
@@ -834,3 +854,45 @@ int muon_get_plan_info(muon_handle h, int mode, int nb, muon_plan_info* out) {
 }
 
 }  // extern "C"
+
+namespace muon {
+
+// One full-mode step of one matrix with the plan tables and intermediates in
+// a caller-supplied device region (used by the no-workspace entry point).
+// Same planner, kernels and launch sequence as muon_step, so the results are
+// bit-identical to a handle-based step of the same matrix.  Needs the region
+// to hold the matrix in a single group; allocates nothing.
+int step_in_region(const muon_param& prm, float lr, float beta, int nesterov, int ns_steps,
+                   float a, float b, float c, void* region, size_t region_bytes,
+                   cudaStream_t stream, std::string* err) {
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) {
+        *err = cudaGetErrorString(ce);
+        return MUON_ERR_CUDA;
+    }
+    muon_handle h = nullptr;
+    int rc = muon_create(&h, dev, stream);
+    if (rc) {
+        *err = muon_last_error(nullptr);
+        return rc;
+    }
+    rc = muon_register_params(h, 1, &prm);
+    size_t mn = 0, full = 0;
+    if (!rc) rc = muon_workspace_size(h, MUON_FULL, 1, &mn, &full);
+    if (!rc && full > region_bytes) {
+        rc = fail(h, MUON_ERR_UNSUPPORTED,
+                  "matrix " + std::to_string(prm.rows) + "x" + std::to_string(prm.cols) +
+                      " needs " + std::to_string(full) +
+                      " bytes of scratch; the fixed scratch of muon_step_noalloc holds " +
+                      std::to_string(region_bytes) +
+                      " bytes (use muon_step with a workspace instead)");
+    }
+    if (!rc) rc = muon_set_workspace(h, region, region_bytes);
+    if (!rc) rc = muon_step(h, lr, beta, nesterov, ns_steps, a, b, c, MUON_FULL, 1);
+    if (rc) *err = h->err;
+    muon_destroy(h);
+    return rc;
+}
+
+}  // namespace muon

@@ -43,7 +43,7 @@ struct EwUnit {
     int32_t tiles_n;         // 64-tiles along n (X orientation)
     int64_t tile_base;       // first global element-wise tile of the unit
     int64_t tile_count;
-    float lr_scale_unused;   // kept for alignment
+    int32_t vec16;           // W rows allow 16-byte vector access
     float shape_scale;
 };
 
@@ -79,10 +79,20 @@ struct NsLaunch {
     float a, b, c;
     unsigned long long wait_limit_ns;
     int* err;                // device error word
+    // Fused first and last iterations (CTA-pair kernels only).
+    //   first: X holds the unnormalised bf16(U); inv_norm[unit] = 1/(||U||+eps)
+    //          scales the SYRK-1 result by inv^2 and the GEMM result by inv;
+    //   last:  the GEMM does not store X; it applies the update to W using
+    //          ew[unit] (W pointers, orientation, shape scale) and lr.
+    const float* inv_norm;
+    const EwUnit* ew;
+    int32_t first, last;
+    float lr;
 };
 
 struct EwLaunch {
     const EwUnit* units;
+    int32_t write_x;         // momentum pass also stores bf16(U) into x[0]
     int32_t num_units;
     int64_t num_tiles;       // total element-wise tiles of the group
     float* partial;          // one fp32 sum of squares per tile

@@ -145,3 +145,20 @@ def test_output_singular_values_in_band():
     inp, _, oexp, _ = gpu_step([trip], nesterov=False)
     s_out = np.linalg.svd(to_np(oexp[0]), compute_uv=False)
     assert s_out.min() > 0.6818 - 0.03 and s_out.max() < 1.2024 + 0.03
+
+
+@pytest.mark.parametrize("fuse_env", [{"MUON_FUSE": "0"},
+                                      {"MUON_FUSE_UPDATE": "1"},
+                                      {"MUON_CTA_GROUP": "1"}])
+def test_alternative_pipelines_match_oracle(fuse_env, monkeypatch):
+    """The unfused pipeline, the update fused into the last GEMM, and the
+    single-CTA kernels all meet the same tolerances."""
+    for k, v in fuse_env.items():
+        monkeypatch.setenv(k, v)
+    shapes = [(256, 640), (640, 256), (300, 300), (96, 1000)]
+    trips = [case(r, c, 200 + i, w_dtype=torch.float32 if i == 2 else torch.bfloat16)
+             for i, (r, c) in enumerate(shapes)]
+    inp, wexp, oexp, _ = gpu_step(trips)
+    for i, tr in enumerate(trips):
+        ref = oracle_step(inp[i])
+        check_against_oracle(tr, inp[i], wexp[i], oexp[i], ref)
