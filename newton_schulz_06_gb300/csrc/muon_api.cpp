@@ -260,14 +260,17 @@ bool make_groups(const std::vector<UnitDesc>& units, size_t scratch,
 }
 
 int encode_map(muon_ctx* h, CUtensorMap* tm, void* base, int64_t inner,
-               int64_t outer, int64_t ld) {
+               int64_t outer, int64_t ld, uint32_t box = 64) {
     cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
     cuuint64_t strides[1] = {cuuint64_t(ld) * 2};
-    cuuint32_t box[2] = {64, 64};
+    cuuint32_t boxd[2] = {box, box};
     cuuint32_t es[2] = {1, 1};
+    // {64, 64} boxes: 128-byte rows, 128-byte swizzle (operand tiles);
+    // {32, 32} boxes: 64-byte rows, 64-byte swizzle (epilogue blocks)
+    const CUtensorMapSwizzle sw =
+        box == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     CUresult r = h->encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
-                           strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B,
+                           strides, boxd, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -378,6 +381,10 @@ int build_plan(muon_ctx* h, int mode, int nb) {
             if ((rc = encode_map(h, &ns.tm_x[1], xb1, u.n, u.m, u.ld_x))) return rc;
             if ((rc = encode_map(h, &ns.tm_a, ab, u.m, u.m, u.ld_mm))) return rc;
             if ((rc = encode_map(h, &ns.tm_b, bb, u.m, u.m, u.ld_mm))) return rc;
+            if ((rc = encode_map(h, &ns.te_x[0], xb0, u.n, u.m, u.ld_x, 32))) return rc;
+            if ((rc = encode_map(h, &ns.te_x[1], xb1, u.n, u.m, u.ld_x, 32))) return rc;
+            if ((rc = encode_map(h, &ns.te_a, ab, u.m, u.m, u.ld_mm, 32))) return rc;
+            if ((rc = encode_map(h, &ns.te_b, bb, u.m, u.m, u.ld_mm, 32))) return rc;
             ns.x[0] = e.x[0];
             ns.x[1] = e.x[1];
             ns.a = reinterpret_cast<__nv_bfloat16*>(ab);

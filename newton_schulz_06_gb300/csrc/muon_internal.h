@@ -53,6 +53,11 @@ struct alignas(128) NsUnit {
     CUtensorMap tm_x[2];     // X ping/pong: dims {n, m}, box {64, 64}
     CUtensorMap tm_a;        // A = X X^T : dims {m, m}, box {64, 64}
     CUtensorMap tm_b;        // B = bA+cAA: dims {m, m}, box {64, 64}
+    // The same four matrices with {32, 32} boxes and 64-byte swizzle, for the
+    // epilogue's TMA loads (A, X) and TMA stores (A, B, X').
+    CUtensorMap te_x[2];
+    CUtensorMap te_a;
+    CUtensorMap te_b;
     __nv_bfloat16* x[2];
     __nv_bfloat16* a;
     __nv_bfloat16* b;

@@ -39,9 +39,11 @@ constexpr int P_BOX = 64 * 64 * 2;                 // one {64,64} box
 constexpr int P_TMEM_COLS = 512;
 constexpr int P_EPI_WARPS = 8;                     // 2 per TMEM lane group
 constexpr int P_THREADS = 64 + 32 * P_EPI_WARPS;
-constexpr int T_PITCH = 40;                        // bf16 per transpose row
-constexpr int P_EPI_BYTES = P_EPI_WARPS * 32 * T_PITCH * 2;  // 32x32 per warp
-constexpr int P_SMEM = P_STAGES * (P_A_BYTES + P_B_BYTES) + 1024 + 256 + P_EPI_BYTES;
+constexpr int P_BLK = 32 * 32 * 2;                 // one 32x32 bf16 block
+constexpr int P_EPI_BYTES = P_EPI_WARPS * 2 * P_BLK;   // input + staging per warp
+constexpr int P_STAGE_BYTES = P_STAGES * (P_A_BYTES + P_B_BYTES);
+constexpr int P_EPI_OFF = P_STAGE_BYTES + 1024;    // after the barrier block
+constexpr int P_SMEM = P_EPI_OFF + P_EPI_BYTES + 1024;
 constexpr uint32_t P_TX_BYTES = 2 * (P_A_BYTES + P_B_BYTES);   // both CTAs
 
 __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -77,30 +79,13 @@ __device__ __forceinline__ int k_extent(const NsUnit& U) {
     return OP == OP_SYRK_X ? U.n : U.m;
 }
 
-// 32 consecutive bf16 of one row, as four 16-byte words; zeros where the
-// row is invalid or the columns run past `limit`.
-__device__ __forceinline__ void load_row32(const __nv_bfloat16* row, int c0, int limit,
-                                           bool row_ok, uint4 (&q)[4]) {
-    if (row_ok && c0 + 32 <= limit) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) q[k] = *reinterpret_cast<const uint4*>(row + c0 + 8 * k);
-    } else {
-        __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(q);
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-            h[e] = (row_ok && c0 + e < limit) ? row[c0 + e] : __float2bfloat16_rn(0.f);
-    }
-}
-
-__device__ __forceinline__ float bf16_at(const uint4 (&q)[4], int e) {
-    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(q)[e]);
-}
-
 // Tile-constant fields of a unit, copied into registers once per tile (the
 // kernels store through pointers the compiler cannot tell apart from the
 // tables, so fields read from the tables would be reloaded after every
 // store).
 struct EpiUnit {
+    const CUtensorMap* te_in;    // epilogue input blocks (GEMM: X, SYRK-2: A)
+    const CUtensorMap* te_out;   // output blocks (A, B or X')
     int m, n;
     int64_t ld_x, ld_mm;
     const __nv_bfloat16* xin;    // GEMM: current iterate
@@ -120,6 +105,8 @@ template <int OP>
 __device__ __forceinline__ EpiUnit load_epi_unit(const NsLaunch& p, int unit) {
     const NsUnit* U = p.units + unit;
     EpiUnit e;
+    e.te_in = (OP == OP_GEMM_BX) ? &U->te_x[p.src] : &U->te_a;
+    e.te_out = (OP == OP_SYRK_X) ? &U->te_a : (OP == OP_SYRK_A) ? &U->te_b : &U->te_x[p.src ^ 1];
     e.m = U->m;
     e.n = U->n;
     e.ld_x = U->ld_x;
@@ -216,100 +203,59 @@ __device__ __forceinline__ void w_store8(const EpiUnit& u, int64_t row, int c0, 
     }
 }
 
-// Symmetric stages, one 32 x 32 block: this warp's rows r0w.., columns
-// gc0..; lane = row.  Element (gi, gc) is stored when gc >= gi and mirrored
-// to (gc, gi) when gc > gi, so each element of the m x m result is written
-// once and the result is exactly symmetric.  The mirror goes through a
-// shared-memory transpose so that its global stores are 16-byte vectors
-// covering whole 64-byte row segments.
-template <int OP>
-__device__ __forceinline__ void syrk_block(const EpiUnit& u, const NsLaunch& p, float scale,
-                                           int r0w, int gc0, int lane, float (&v)[32],
-                                           const uint4 (&ain)[4], __nv_bfloat16* sT) {
-    const int m = u.m;
-    const int gi = r0w + lane;
-    const int64_t ld = u.ld_mm;
-#pragma unroll
-    for (int e = 0; e < 32; ++e)
-        v[e] = (OP == OP_SYRK_A) ? fmaf(p.b, bf16_at(ain, e), p.c * v[e]) : v[e] * scale;
-    if (gc0 >= m || r0w >= m || gc0 + 31 < r0w) return;      // warp-uniform
-    if (gi < m && gc0 + 31 >= gi) {
-        __nv_bfloat16* row = u.out + static_cast<int64_t>(gi) * ld;
-        if (gc0 >= gi && gc0 + 32 <= m) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float o[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = v[8 * q + e];
-                store8_bf16(row + gc0 + 8 * q, o);
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int gc = gc0 + e;
-                if (gc < m && gc >= gi) row[gc] = __float2bfloat16_rn(v[e]);
-            }
-        }
-    }
-    if (gc0 + 31 <= r0w) return;                              // nothing to mirror
-#pragma unroll
-    for (int e = 0; e < 32; ++e) sT[e * T_PITCH + lane] = __float2bfloat16_rn(v[e]);
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int jj = 8 * i + (lane >> 2);
-        const int R = gc0 + jj;
-        const int C0 = r0w + (lane & 3) * 8;
-        const uint4 q = *reinterpret_cast<const uint4*>(sT + jj * T_PITCH + (lane & 3) * 8);
-        __nv_bfloat16* dst = u.out + static_cast<int64_t>(R) * ld + C0;
-        if (R < m && C0 + 8 <= m && R > C0 + 7) {
-            *reinterpret_cast<uint4*>(dst) = q;
-        } else if (R < m) {
-            const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&q);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (C0 + k < m && R > C0 + k) dst[k] = h[k];
-        }
-    }
-    __syncwarp();
+// Byte offset of 16-byte chunk q of row r in a 32 x 32 bf16 block laid out
+// with the TMA's 64-byte swizzle (64-byte rows; chunk index XOR (r / 2) % 4).
+__device__ __forceinline__ uint32_t sw64(int r, int q) {
+    return static_cast<uint32_t>(r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
 }
 
-// GEMM stage, one 32 x 32 block: X' = scale * (a X + D); in the last
-// iteration O = bf16(scale * (a X + D)) is applied to W instead of stored:
-// W <- W - lr * shape_scale * O (W in its own orientation).
-__device__ __forceinline__ void gemm_block(const EpiUnit& u, const NsLaunch& p, float scale,
-                                           int r0w, int gc0, int lane, const float (&v)[32],
-                                           const uint4 (&xin)[4], __nv_bfloat16* sT) {
+__device__ __forceinline__ void st_row_bf16(uint8_t* blk, int r, const float (&v)[32]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(v[8 * q + 2 * k], v[8 * q + 2 * k + 1]);
+        *reinterpret_cast<uint4*>(blk + sw64(r, q)) = w;
+    }
+}
+
+__device__ __forceinline__ void ld_row_bf16(const uint8_t* blk, int r, float (&v)[32]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 w = *reinterpret_cast<const uint4*>(blk + sw64(r, q));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __bfloat1622float2(h[k]);
+            v[8 * q + 2 * k] = f.x;
+            v[8 * q + 2 * k + 1] = f.y;
+        }
+    }
+}
+
+// Column `c` of the block written from this lane's row values: element
+// (row e, column c) = v[e], i.e. the transpose of the lane-per-row block.
+__device__ __forceinline__ void st_col_bf16(uint8_t* blk, int c, const float (&v)[32]) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+        *reinterpret_cast<__nv_bfloat16*>(blk + sw64(e, c >> 3) + (c & 7) * 2) =
+            __float2bfloat16_rn(v[e]);
+}
+
+// GEMM last iteration with the update fused (optional path): O in bf16,
+// W <- W - lr * shape_scale * O in W's orientation, through global memory.
+__device__ __forceinline__ void gemm_update_block(const EpiUnit& u, int r0w, int gc0, int lane,
+                                                  const float (&o_in)[32], uint8_t* stage) {
     const int m = u.m, n = u.n;
     const int gi = r0w + lane;
     const bool row_ok = gi < m;
     float o[32];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) o[e] = scale * fmaf(p.a, bf16_at(xin, e), v[e]);
-    if (!p.last) {
-        if (!row_ok || gc0 >= n) return;
-        __nv_bfloat16* xout = u.xout + static_cast<int64_t>(gi) * u.ld_x;
-        if (gc0 + 32 <= n) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float t[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) t[e] = o[8 * q + e];
-                store8_bf16(xout + gc0 + 8 * q, t);
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-                if (gc0 + e < n) xout[gc0 + e] = __float2bfloat16_rn(o[e]);
-        }
-        return;
-    }
-#pragma unroll
-    for (int e = 0; e < 32; ++e) o[e] = __bfloat162float(__float2bfloat16_rn(o[e]));
+    for (int e = 0; e < 32; ++e) o[e] = __bfloat162float(__float2bfloat16_rn(o_in[e]));
     if (gc0 >= n || r0w >= m) return;                         // warp-uniform
     if (!u.transposed) {
         if (!row_ok) return;
-        // all four W loads of the chunk in flight before any store
         float w[4][8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -331,8 +277,7 @@ __device__ __forceinline__ void gemm_block(const EpiUnit& u, const NsLaunch& p, 
         return;
     }
     // transposed unit: W[gc][gi]; transpose O through shared memory
-#pragma unroll
-    for (int e = 0; e < 32; ++e) sT[e * T_PITCH + lane] = __float2bfloat16_rn(o[e]);
+    st_col_bf16(stage, lane, o);
     __syncwarp();
     float w[4][8];
 #pragma unroll
@@ -348,7 +293,7 @@ __device__ __forceinline__ void gemm_block(const EpiUnit& u, const NsLaunch& p, 
         const int R = gc0 + jj;
         const int C0 = r0w + (lane & 3) * 8;
         if (R < n && C0 < m) {
-            const uint4 q = *reinterpret_cast<const uint4*>(sT + jj * T_PITCH + (lane & 3) * 8);
+            const uint4 q = *reinterpret_cast<const uint4*>(stage + sw64(jj, lane & 3));
             const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&q);
             float t[8];
 #pragma unroll
@@ -359,6 +304,25 @@ __device__ __forceinline__ void gemm_block(const EpiUnit& u, const NsLaunch& p, 
             w_store8(u, R, C0, min(8, m - C0), w[i], t);
         }
     }
+    __syncwarp();
+}
+
+// Issues (lane 0) the TMA store of the staged 32 x 32 block at (x, y) after
+// every lane's shared-memory writes are ordered before it.
+__device__ __forceinline__ void store_block(const CUtensorMap* tm, uint8_t* stage, int x, int y,
+                                            int lane) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(tm, smem_u32(stage), x, y);
+        bulk_commit();
+    }
+}
+
+// Before staging new data: lane 0 waits until the previous TMA store has
+// read the staging block.
+__device__ __forceinline__ void stage_free(int lane) {
+    if (lane == 0) bulk_wait_read0();
     __syncwarp();
 }
 
@@ -376,7 +340,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     uint64_t* tfull_bar = bars + 2 * P_STAGES;
     uint64_t* tempty_bar = bars + 2 * P_STAGES + 2;
     uint64_t* drain_bar = bars + 2 * P_STAGES + 4;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * P_STAGES + 5);
+    uint64_t* in_bar = bars + 2 * P_STAGES + 5;               // one per epilogue warp
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_bar + P_EPI_WARPS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -395,6 +360,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             mbar_init(smem_u32(&tempty_bar[a]), 2 * P_EPI_WARPS);
         }
         mbar_init(smem_u32(drain_bar), 1);
+        for (int w = 0; w < P_EPI_WARPS; ++w) mbar_init(smem_u32(&in_bar[w]), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -518,60 +484,135 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         }
     } else {
         // -------------------------------------------- epilogue (both CTAs)
-        // warps 2..9: lane group warp % 4 (TMEM rounds), column half
-        // (warp - 2) / 4 (chunks 4h .. 4h + 3 of the 256 columns)
+        // warps 2..9: lane group warp % 4 (TMEM rows), column half
+        // (warp - 2) / 4 (chunks 4h .. 4h + 3 of the 256 columns).  Blocks of
+        // 32 x 32 go out through a swizzled shared-memory stage and TMA stores
+        // (which also clip at the matrix edge); the epilogue's input blocks
+        // (X for the GEMM, A for SYRK-2) come in by TMA one block ahead.
+        const int ew = warp - 2;
         const int lg = warp & 3;
-        const int half = (warp - 2) >> 2;
-        __nv_bfloat16* sT = reinterpret_cast<__nv_bfloat16*>(
-                                reinterpret_cast<uint8_t*>(bars) + 256) +
-                            (warp - 2) * 32 * T_PITCH;
+        const int half = ew >> 2;
+        uint8_t* epi = smem + P_EPI_OFF + ew * 2 * P_BLK;
+        uint8_t* s_in = epi;
+        uint8_t* s_st = epi + P_BLK;
+        const uint32_t inb = smem_u32(&in_bar[ew]);
+        uint32_t in_phase = 0;
+        bool in_pending = false;      // an input block load is in flight
         uint32_t tempty_leader[2];
         tempty_leader[0] = map_to_rank(smem_u32(&tempty_bar[0]), 0);
         tempty_leader[1] = map_to_rank(smem_u32(&tempty_bar[1]), 0);
         int local = 0;
-        for (int it = pair; it < p.num_tiles; it += npairs, ++local) {
+        bool ok = true;
+        for (int it = pair; ok && it < p.num_tiles; it += npairs, ++local) {
             const TileItem t = p.tiles[it];
             const EpiUnit u = load_epi_unit<OP>(p, t.unit);
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             const int r0w = t.ti * 256 + static_cast<int>(rank) * P_HALF + lg * 32;
-            const int gi = r0w + lane;
             const int col0 = t.tj * 256 + half * 128;
+            const int lim_c = (OP == OP_GEMM_BX) ? u.n : u.m;
             float scale = 1.f;
             if (p.first && OP != OP_SYRK_A) {
                 const float inv = p.inv_norm[t.unit];
                 scale = (OP == OP_SYRK_X) ? inv * inv : inv;
             }
-            // epilogue input rows (GEMM: X; SYRK-2: A), prefetched a chunk
-            // ahead; the first chunk is in flight while the main loop runs
-            const __nv_bfloat16* in_row =
-                (OP == OP_GEMM_BX) ? u.xin + static_cast<int64_t>(gi) * u.ld_x
-                                   : u.ain + static_cast<int64_t>(gi) * u.ld_mm;
-            const int in_limit = (OP == OP_GEMM_BX) ? u.n : u.m;
-            const bool row_ok = gi < u.m;
-            uint4 pre[2][4];
-            if (OP != OP_SYRK_X) load_row32(in_row, col0, in_limit, row_ok, pre[0]);
-            const bool ok = wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag,
-                                         p.err, limit);
-            if (!__all_sync(0xffffffffu, ok)) break;
+            // which of the 4 blocks this warp stores (warp-uniform)
+            int need[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int gc0 = col0 + 32 * c;
+                bool nd = r0w < u.m && gc0 < lim_c;
+                if (OP != OP_GEMM_BX) nd = nd && gc0 >= r0w;      // upper blocks only
+                need[c] = nd;
+            }
+            int nxt = 0;
+            while (nxt < 4 && !need[nxt]) ++nxt;
+            const bool uses_in = (OP != OP_SYRK_X);
+            if (uses_in && nxt < 4) {
+                in_pending = true;
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    mbar_expect_tx(inb, P_BLK);
+                    tma_load_2d(smem_u32(s_in), u.te_in, inb, col0 + 32 * nxt, r0w);
+                }
+            }
+            ok = wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.err, limit);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) +
                                    acc * 256 + half * 128;
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < 4; ++c) {
-                if (OP != OP_SYRK_X && c + 1 < 4)
-                    load_row32(in_row, col0 + 32 * (c + 1), in_limit, row_ok, pre[(c + 1) & 1]);
+                if (!need[c]) continue;
+                const int gc0 = col0 + 32 * c;
                 float v[32];
                 tmem_ld32(tbase + 32 * c, v);
-                if (OP == OP_GEMM_BX)
-                    gemm_block(u, p, scale, r0w, col0 + 32 * c, lane, v, pre[c & 1], sT);
-                else
-                    syrk_block<OP>(u, p, scale, r0w, col0 + 32 * c, lane, v, pre[c & 1], sT);
+                if (uses_in) {
+                    const bool got = wait_bounded(inb, in_phase, abort_flag, p.err, limit);
+                    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                    in_phase ^= 1;
+                    in_pending = false;
+                    float x[32];
+                    ld_row_bf16(s_in, lane, x);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        v[e] = (OP == OP_SYRK_A) ? fmaf(p.b, x[e], p.c * v[e])
+                                                 : scale * fmaf(p.a, x[e], v[e]);
+                    __syncwarp();      // every lane's reads of s_in are done
+                    nxt = c + 1;
+                    while (nxt < 4 && !need[nxt]) ++nxt;
+                    if (nxt < 4) {
+                        in_pending = true;
+                        if (lane == 0) {
+                            fence_proxy_async_smem();
+                            mbar_expect_tx(inb, P_BLK);
+                            tma_load_2d(smem_u32(s_in), u.te_in, inb, col0 + 32 * nxt, r0w);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] *= scale;
+                }
+                if (OP == OP_GEMM_BX) {
+                    if (p.last) {
+                        stage_free(lane);
+                        gemm_update_block(u, r0w, gc0, lane, v, s_st);
+                    } else {
+                        stage_free(lane);
+                        st_row_bf16(s_st, lane, v);
+                        store_block(u.te_out, s_st, gc0, r0w, lane);
+                    }
+                } else if (gc0 == r0w) {
+                    // diagonal block: upper part as computed, lower part
+                    // mirrored from the upper, so the block is symmetric
+                    stage_free(lane);
+                    st_col_bf16(s_st, lane, v);
+                    __syncwarp();
+                    float mir[32];
+                    ld_row_bf16(s_st, lane, mir);
+                    __syncwarp();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (e < lane) v[e] = mir[e];
+                    st_row_bf16(s_st, lane, v);
+                    store_block(u.te_out, s_st, gc0, r0w, lane);
+                } else {
+                    stage_free(lane);
+                    st_row_bf16(s_st, lane, v);
+                    store_block(u.te_out, s_st, gc0, r0w, lane);
+                    stage_free(lane);
+                    st_col_bf16(s_st, lane, v);
+                    store_block(u.te_out, s_st, r0w, gc0, lane);   // mirror
+                }
             }
+            if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(tempty_leader[acc]);
+            if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader[acc]);
         }
+        // after an abort: let an input load in flight land before leaving
+        if (in_pending) wait_quiet(inb, in_phase, limit);
+        if (lane == 0) bulk_wait_all0();
     }
 
     tc_fence_before();
