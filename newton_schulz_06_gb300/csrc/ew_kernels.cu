@@ -118,78 +118,142 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return s;   // valid in thread 0
 }
 
-// Pass 1: M <- beta*M + G, U as above; one fp32 sum of U^2 per tile.
-__global__ void __launch_bounds__(EW_THREADS)
+// Tile-constant fields of a unit in registers (the kernels store through
+// pointers the compiler cannot tell apart from the unit table).
+struct EwU {
+    void* w;
+    const void* g;
+    float* mom;
+    float* w_dbg;
+    __nv_bfloat16* o_dbg;
+    __nv_bfloat16* x[2];
+    int64_t ld_w, ld_g, ld_m, ld_dbg, tile_base, tile_end;
+    int rows, cols, m, n, ld_x, w_dtype, g_dtype, transposed, vec, tiles_n;
+    float shape_scale;
+};
+
+__device__ __forceinline__ EwU load_ewu(const EwUnit* __restrict__ P) {
+    EwU u;
+    u.w = P->w; u.g = P->g; u.mom = P->mom; u.w_dbg = P->w_dbg; u.o_dbg = P->o_dbg;
+    u.x[0] = P->x[0]; u.x[1] = P->x[1];
+    u.ld_w = P->ld_w; u.ld_g = P->ld_g; u.ld_m = P->ld_m; u.ld_dbg = P->ld_dbg;
+    u.tile_base = P->tile_base; u.tile_end = P->tile_base + P->tile_count;
+    u.rows = P->rows; u.cols = P->cols; u.m = P->m; u.n = P->n; u.ld_x = P->ld_x;
+    u.w_dtype = P->w_dtype; u.g_dtype = P->g_dtype; u.transposed = P->transposed;
+    u.vec = P->vec_ok; u.tiles_n = P->tiles_n; u.shape_scale = P->shape_scale;
+    return u;
+}
+
+__device__ __forceinline__ TileGeom geom_of(const EwU& U, int64_t t) {
+    TileGeom g;
+    g.u = 0;
+    const int64_t local = t - U.tile_base;
+    const int tr = static_cast<int>(local / U.tiles_n);
+    const int tc = static_cast<int>(local - static_cast<int64_t>(tr) * U.tiles_n);
+    g.xr0 = tr * EW_TILE;
+    g.xc0 = tc * EW_TILE;
+    g.wr0 = U.transposed ? g.xc0 : g.xr0;
+    g.wc0 = U.transposed ? g.xr0 : g.xc0;
+    return g;
+}
+
+// Pass 1: M <- beta*M + G; U as above; per tile and warp one fp32 sum of U^2
+// taken in the X orientation (short side first) in a fixed order, so that a
+// matrix and its transpose give the same sums.  With write_x the
+// unnormalised iterate bf16(U) is stored in the X orientation as well.
+// Thread (i, j4) owns rows i + 16k (k = 0..3), columns j4 .. j4 + 3 of a
+// 64 x 64 tile; only transposed units go through shared memory.
+__global__ void __launch_bounds__(EW_THREADS, 4)
 ew_momentum_kernel(const EwLaunch p) {
     __shared__ float sU[EW_TILE][EW_TILE + 1];
-    __shared__ float red[EW_THREADS / 32];
+    __shared__ float red[2][EW_THREADS / 32];
     const int i = threadIdx.x >> 4;          // 0..15
     const int j4 = (threadIdx.x & 15) * 4;   // 0..60
-    for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-        const int u = find_unit(p.units, p.num_units, t);
-        const EwUnit& U = p.units[u];
-        const TileGeom g = tile_geom(U, u, t);
-        const bool vec = U.vec_ok != 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (blockIdx.x >= p.num_tiles) return;
+    int u = find_unit(p.units, p.num_units, blockIdx.x);
+    EwU U = load_ewu(p.units + u);
+    int parity = 0;
+    // grid-stride: concurrent blocks work on neighbouring tiles
+    for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, parity ^= 1) {
+        while (t >= U.tile_end) U = load_ewu(p.units + (++u));
+        const TileGeom g = geom_of(U, t);
+        float uv[4][4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int r = i + 16 * k;
-            const int wr = g.wr0 + r, wc = g.wc0 + j4;
+            const int wr = g.wr0 + i + 16 * k, wc = g.wc0 + j4;
             int nval = (wr < U.rows) ? min(4, U.cols - wc) : 0;
             nval = max(nval, 0);
-            float mv[4], gv[4], uv[4];
-            ld4(U.mom, MUON_F32, wr * U.ld_m + wc, nval, vec, mv);
-            ld4(U.g, U.g_dtype, wr * U.ld_g + wc, nval, vec, gv);
+            float mv[4], gv[4];
+            ld4(U.mom, MUON_F32, wr * U.ld_m + wc, nval, U.vec, mv);
+            ld4(U.g, U.g_dtype, wr * U.ld_g + wc, nval, U.vec, gv);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 mv[e] = fmaf(p.beta, mv[e], gv[e]);
-                uv[e] = p.nesterov ? fmaf(p.beta, mv[e], gv[e]) : mv[e];
-                sU[r][j4 + e] = e < nval ? uv[e] : 0.f;
+                uv[k][e] = e < nval ? (p.nesterov ? fmaf(p.beta, mv[e], gv[e]) : mv[e]) : 0.f;
             }
-            st4(U.mom, MUON_F32, wr * U.ld_m + wc, nval, vec, mv);
+            st4(U.mom, MUON_F32, wr * U.ld_m + wc, nval, U.vec, mv);
         }
-        __syncthreads();
+        if (U.transposed) {            // block-uniform
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sU[i + 16 * k][j4 + e] = uv[k][e];
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) uv[k][e] = sU[j4 + e][i + 16 * k];
+            __syncthreads();
+        }
+        // uv now holds X(i + 16k, j4 + e) of this tile
         float acc = 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int xr = i + 16 * k;
-            float xv[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int xc = j4 + e;
-                const float v = U.transposed ? sU[xc][xr] : sU[xr][xc];
-                acc = fmaf(v, v, acc);
-                xv[e] = v;
-            }
+            for (int e = 0; e < 4; ++e) acc = fmaf(uv[k][e], uv[k][e], acc);
             if (p.write_x) {
-                // unnormalised iterate bf16(U), X orientation; the first
-                // iteration applies 1/(||U||+eps)
-                const int gr = g.xr0 + xr, gc = g.xc0 + j4;
+                const int gr = g.xr0 + i + 16 * k, gc = g.xc0 + j4;
                 int nx = (gr < U.m) ? min(4, U.n - gc) : 0;
                 nx = max(nx, 0);
-                st4(U.x[0], MUON_BF16, static_cast<int64_t>(gr) * U.ld_x + gc, nx, true, xv);
+                st4(U.x[0], MUON_BF16, static_cast<int64_t>(gr) * U.ld_x + gc, nx, true,
+                    uv[k]);
             }
         }
-        const float s = block_sum(acc, red);
-        if (threadIdx.x == 0) p.partial[t] = s;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) red[parity][warp] = acc;
         __syncthreads();
+        if (threadIdx.x == 0) {
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < EW_THREADS / 32; ++w) s += red[parity][w];
+            p.partial[t] = s;
+        }
     }
 }
 
 // Per unit: ||U||_F from its tile sums in a fixed order (fp64), then
-// inv_norm = 1 / (||U|| + eps).  One warp per unit.
+// inv_norm = 1 / (||U|| + eps).  One block per unit: thread k sums tiles
+// k, k + 256, ... in order, then a fixed tree combines the 256 sums.
 __global__ void __launch_bounds__(256) ew_norm_kernel(const EwLaunch p) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (warp >= p.num_units) return;
-    const EwUnit& U = p.units[warp];
+    __shared__ double red[256];
+    const int u = blockIdx.x;
+    const EwUnit& U = p.units[u];
+    const int64_t base = U.tile_base * EW_PARTIALS_PER_TILE;
+    const int64_t count = U.tile_count * EW_PARTIALS_PER_TILE;
     double s = 0.0;
-    for (int64_t k = lane; k < U.tile_count; k += 32)
-        s += static_cast<double>(p.partial[U.tile_base + k]);
+    for (int64_t k = threadIdx.x; k < count; k += 256)
+        s += static_cast<double>(p.partial[base + k]);
+    red[threadIdx.x] = s;
+    __syncthreads();
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0)
-        p.inv_norm[warp] = static_cast<float>(1.0 / (sqrt(s) + (double)p.eps));
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0)
+        p.inv_norm[u] = static_cast<float>(1.0 / (sqrt(red[0]) + (double)p.eps));
 }
 
 // Pass 2: X0 = bf16(U * inv_norm) in the X orientation.
@@ -297,9 +361,7 @@ cudaError_t launch_ew_momentum(const EwLaunch& p, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_ew_norm(const EwLaunch& p, cudaStream_t s) {
-    const int warps_per_block = 8;
-    const int grid = (p.num_units + warps_per_block - 1) / warps_per_block;
-    ew_norm_kernel<<<grid, 32 * warps_per_block, 0, s>>>(p);
+    ew_norm_kernel<<<p.num_units, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -13,6 +13,7 @@
 // every unit's intermediates at once; they run one after another.
 #include <algorithm>
 #include <cmath>
+#include <queue>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -55,6 +56,9 @@ struct GroupDesc {
     size_t ew_off = 0, ns_off = 0;           // metadata offsets in ws
     size_t t_sx_off = 0, t_sa_off = 0, t_g_off = 0;
     int n_sx = 0, n_sa = 0, n_g = 0;
+    // CTA-pair schedules: per-pair offsets into the tile lists
+    size_t o_sx_off = 0, o_sa_off = 0, o_g_off = 0;
+    int p_sx = 0, p_sa = 0, p_g = 0;
     int64_t ew_tiles = 0;
 };
 
@@ -200,7 +204,7 @@ int build_units(muon_ctx* h, int mode, int nb, std::vector<UnitDesc>* out) {
             u.mm_bytes = align_up(size_t(u.m) * u.ld_mm * 2, 1024);
             u.buf_bytes = 2 * u.x_bytes + 2 * u.mm_bytes;
             u.ew_tiles = ceil_div(u.m, EW_TILE) * ceil_div(u.n, EW_TILE);
-            u.need = u.buf_bytes + size_t(u.ew_tiles) * 4 + 4;
+            u.need = u.buf_bytes + size_t(u.ew_tiles) * 4 * EW_PARTIALS_PER_TILE + 4;
             out->push_back(u);
         }
     }
@@ -216,8 +220,9 @@ size_t meta_bound(const std::vector<UnitDesc>& units) {
         unit_tiles(u, true, &s2, &g2, &x, &y);
         s = std::max(s, s2);
         g = std::max(g, g2);
-        b += sizeof(EwUnit) + sizeof(NsUnit) + 5 * 256 +
-             size_t(2 * s + g) * sizeof(TileItem);
+        // tile lists (twice: tiles may be split in halves) and pair offsets
+        b += sizeof(EwUnit) + sizeof(NsUnit) + 8 * 256 +
+             2 * size_t(2 * s + g) * sizeof(TileItem) + 3 * 4 * 1024;
     }
     return align_up(b, 1024);
 }
@@ -287,6 +292,60 @@ void sort_tiles(std::vector<TileItem>* v) {
     });
 }
 
+// Longest-processing-time schedule of tiles over `P` CTA pairs: the costliest
+// remaining tile goes to the least-loaded pair.  With allow_split, a
+// full-width tile that would push that pair past the average load is split
+// into two 128-column halves (each output element is still computed by one
+// pair in one K order, so a split changes no result); measured on GB300 the
+// halves run too slowly for this to pay (they need 1.5x the operand traffic
+// per FLOP), so the planner does not split.  Rewrites *v in pair-major
+// order; off[p] .. off[p + 1] are pair p's tiles.
+void lpt_schedule(std::vector<TileItem>* v, int P, bool allow_split,
+                  std::vector<int32_t>* off) {
+    struct It {
+        TileItem t;
+        int64_t cost, seq;
+    };
+    auto cost_of = [](const TileItem& t) { return int64_t(t.k_blocks) * t.n_len; };
+    auto cmp = [](const It& a, const It& b) {
+        return a.cost != b.cost ? a.cost < b.cost : a.seq > b.seq;
+    };
+    std::priority_queue<It, std::vector<It>, decltype(cmp)> q(cmp);
+    int64_t seq = 0, total = 0;
+    for (const TileItem& t : *v) {
+        q.push({t, cost_of(t), seq++});
+        total += cost_of(t);
+    }
+    const double target = P > 0 ? double(total) / P : 0.0;
+    using Load = std::pair<int64_t, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> loads;
+    for (int p = 0; p < P; ++p) loads.push({0, p});
+    std::vector<std::vector<TileItem>> lists(P);
+    while (!q.empty()) {
+        const It it = q.top();
+        q.pop();
+        const Load l = loads.top();
+        if (allow_split && it.t.n_len == 256 && double(l.first + it.cost) > target * 1.001) {
+            TileItem a = it.t, b = it.t;
+            a.n_len = b.n_len = 128;
+            b.n_off = static_cast<int16_t>(it.t.n_off + 128);
+            q.push({a, it.cost / 2, seq++});
+            q.push({b, it.cost / 2, seq++});
+            continue;
+        }
+        loads.pop();
+        lists[l.second].push_back(it.t);
+        loads.push({l.first + it.cost, l.second});
+    }
+    v->clear();
+    off->assign(P + 1, 0);
+    for (int p = 0; p < P; ++p) {
+        (*off)[p] = static_cast<int32_t>(v->size());
+        v->insert(v->end(), lists[p].begin(), lists[p].end());
+    }
+    (*off)[P] = static_cast<int32_t>(v->size());
+}
+
 int build_plan(muon_ctx* h, int mode, int nb) {
     Plan& P = h->plan;
     P = Plan();
@@ -317,7 +376,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         for (int i = g.u0; i < g.u1; ++i) tiles += P.units[i].ew_tiles;
         g.ew_tiles = tiles;
         const size_t part_off = align_up(inv_off + size_t(nu) * 4, 256);
-        size_t buf_off = align_up(part_off + size_t(tiles) * 4, 1024);
+        size_t buf_off = align_up(part_off + size_t(tiles) * 4 * EW_PARTIALS_PER_TILE, 1024);
 
         off = align_up(off, 256);
         g.ew_off = off;
@@ -465,18 +524,33 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         sort_tiles(&tsx);
         sort_tiles(&tsa);
         sort_tiles(&tg);
-        auto put = [&](const std::vector<TileItem>& v, size_t* o, int* n) {
+        const int64_t base_sx = static_cast<int64_t>(tsx.size());
+        const int64_t base_g = static_cast<int64_t>(tg.size());
+        auto put = [&](std::vector<TileItem>& v, size_t* o, int* n, size_t* oo, int* np) {
+            *oo = 0;
+            *np = 0;
+            if (h->pair) {
+                const int pairs = std::max(1, std::min(h->max_pairs,
+                                                       static_cast<int>(v.size())));
+                std::vector<int32_t> offs;
+                lpt_schedule(&v, pairs, false, &offs);
+                off = align_up(off, 256);
+                *oo = off;
+                *np = pairs;
+                std::memcpy(meta.data() + off, offs.data(), offs.size() * sizeof(int32_t));
+                off += offs.size() * sizeof(int32_t);
+            }
             off = align_up(off, 256);
             *o = off;
             *n = static_cast<int>(v.size());
             if (!v.empty()) std::memcpy(meta.data() + off, v.data(), v.size() * sizeof(TileItem));
             off += v.size() * sizeof(TileItem);
         };
-        put(tsx, &g.t_sx_off, &g.n_sx);
-        put(tsa, &g.t_sa_off, &g.n_sa);
-        put(tg, &g.t_g_off, &g.n_g);
-        P.syrk_tiles += g.n_sx;
-        P.gemm_tiles += g.n_g;
+        put(tsx, &g.t_sx_off, &g.n_sx, &g.o_sx_off, &g.p_sx);
+        put(tsa, &g.t_sa_off, &g.n_sa, &g.o_sa_off, &g.p_sa);
+        put(tg, &g.t_g_off, &g.n_g, &g.o_g_off, &g.p_g);
+        P.syrk_tiles += base_sx;
+        P.gemm_tiles += base_g;
         P.ew_tiles += g.ew_tiles;
         if (off > P.scratch_off)
             return fail(h, MUON_ERR_STATE, "internal: metadata exceeds its bound");
@@ -522,6 +596,7 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
         muon_ctx* h = new muon_ctx();
         h->device = MUON_HOST_ONLY;
         h->num_sms = 148;
+        h->max_pairs = 74;
         h->pair = pair;
         *out = h;
         return MUON_OK;
@@ -719,16 +794,17 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
             L.src = cur;
             L.first = (fused && s == 0) ? 1 : 0;
             L.last = (fused && h->fuse_update && s == ns_steps - 1) ? 1 : 0;
-            const struct { NsOp op; size_t off; int n; int st; } seq[3] = {
-                {OP_SYRK_X, g.t_sx_off, g.n_sx, ST_SYRK1},
-                {OP_SYRK_A, g.t_sa_off, g.n_sa, ST_SYRK2},
-                {OP_GEMM_BX, g.t_g_off, g.n_g, ST_GEMM}};
+            const struct { NsOp op; size_t off; int n; int st; size_t oo; int np; } seq[3] = {
+                {OP_SYRK_X, g.t_sx_off, g.n_sx, ST_SYRK1, g.o_sx_off, g.p_sx},
+                {OP_SYRK_A, g.t_sa_off, g.n_sa, ST_SYRK2, g.o_sa_off, g.p_sa},
+                {OP_GEMM_BX, g.t_g_off, g.n_g, ST_GEMM, g.o_g_off, g.p_g}};
             for (const auto& q : seq) {
                 L.tiles = reinterpret_cast<const TileItem*>(ws + q.off);
                 L.num_tiles = q.n;
+                L.pair_off = h->pair ? reinterpret_cast<const int32_t*>(ws + q.oo) : nullptr;
                 if (!begin(q.st)) return fail(h, MUON_ERR_CUDA, "event create");
                 if (h->pair)
-                    e = launch_ns_pair(q.op, L, std::min(q.n, h->max_pairs), h->stream);
+                    e = launch_ns_pair(q.op, L, q.np, h->stream);
                 else
                     e = launch_ns(q.op, L, std::min(q.n, h->num_sms), h->stream);
                 end();

@@ -12,6 +12,8 @@ namespace muon {
 // Tile edge of the element-wise stages (momentum, normalise, update).
 constexpr int EW_TILE = 64;
 constexpr int EW_THREADS = 256;
+// The momentum pass writes one fp32 sum of squares per tile.
+constexpr int EW_PARTIALS_PER_TILE = 1;
 
 // Tensor-core stages: one CTA computes a BM x BN output tile, K in BK steps.
 constexpr int BM = 128;
@@ -93,6 +95,10 @@ struct NsLaunch {
     const EwUnit* ew;
     int32_t first, last;
     float lr;
+    // CTA-pair kernels: pair p processes tiles [pair_off[p], pair_off[p+1])
+    // (a cost-balanced schedule built by the planner); nullptr = pair p takes
+    // tiles p, p + pairs, ...
+    const int32_t* pair_off;
 };
 
 struct EwLaunch {

@@ -44,7 +44,6 @@ constexpr int P_EPI_BYTES = P_EPI_WARPS * 2 * P_BLK;   // input + staging per wa
 constexpr int P_STAGE_BYTES = P_STAGES * (P_A_BYTES + P_B_BYTES);
 constexpr int P_EPI_OFF = P_STAGE_BYTES + 1024;    // after the barrier block
 constexpr int P_SMEM = P_EPI_OFF + P_EPI_BYTES + 1024;
-constexpr uint32_t P_TX_BYTES = 2 * (P_A_BYTES + P_B_BYTES);   // both CTAs
 
 __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
@@ -326,6 +325,24 @@ __device__ __forceinline__ void stage_free(int lane) {
     __syncwarp();
 }
 
+// The tiles of pair `pair`: a planner-built range, or a stride over all.
+struct TileRange {
+    int begin, end, step;
+};
+__device__ __forceinline__ TileRange tile_range(const NsLaunch& p, int pair, int npairs) {
+    TileRange r;
+    if (p.pair_off) {
+        r.begin = p.pair_off[pair];
+        r.end = p.pair_off[pair + 1];
+        r.step = 1;
+    } else {
+        r.begin = pair;
+        r.end = p.num_tiles;
+        r.step = npairs;
+    }
+    return r;
+}
+
 template <int OP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     ns2_kernel(const __grid_constant__ NsLaunch p) {
@@ -387,7 +404,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             int issued[P_STAGES];
             for (int s = 0; s < P_STAGES; ++s) issued[s] = 0;
             bool ok = true;
-            for (int it = pair; ok && it < p.num_tiles; it += npairs) {
+            const TileRange tr = tile_range(p, pair, npairs);
+            for (int it = tr.begin; ok && it < tr.end; it += tr.step) {
                 const TileItem t = p.tiles[it];
                 const NsUnit* U = p.units + t.unit;
                 const void* tmA;
@@ -397,7 +415,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 else { tmA = &U->tm_b; tmB = &U->tm_x[p.src]; }
                 const int kblocks = (k_extent<OP>(*U) + BK - 1) / BK;
                 const int r0 = t.ti * 256 + static_cast<int>(rank) * P_HALF;
-                const int b0 = t.tj * 256 + static_cast<int>(rank) * P_HALF;
+                // N = n_len columns split evenly over the pair (64 or 128 each)
+                const int hb = t.n_len >> 1;
+                const int b0 = t.tj * 256 + t.n_off + static_cast<int>(rank) * hb;
+                const uint32_t tx_bytes = 2u * (P_A_BYTES + hb * BK * 2);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag,
                                       p.err, limit)) {
@@ -405,7 +426,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                         break;
                     }
                     const uint32_t fb_local = smem_u32(&full_bar[stage]);
-                    if (rank == 0) mbar_expect_tx(fb_local, P_TX_BYTES);
+                    if (rank == 0) mbar_expect_tx(fb_local, tx_bytes);
                     const uint32_t fb = map_to_rank(fb_local, 0);
                     const uint32_t a_dst = smem_u32(sA + stage * P_A_BYTES);
                     const uint32_t b_dst = smem_u32(sB + stage * P_B_BYTES);
@@ -414,10 +435,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                     tma_load_2d_pair(a_dst + P_BOX, tmA, fb, k0, r0 + 64);
                     if (OP == OP_GEMM_BX) {
                         tma_load_2d_pair(b_dst, tmB, fb, b0, k0);
-                        tma_load_2d_pair(b_dst + P_BOX, tmB, fb, b0 + 64, k0);
+                        if (hb > 64) tma_load_2d_pair(b_dst + P_BOX, tmB, fb, b0 + 64, k0);
                     } else {
                         tma_load_2d_pair(b_dst, tmB, fb, k0, b0);
-                        tma_load_2d_pair(b_dst + P_BOX, tmB, fb, k0, b0 + 64);
+                        if (hb > 64) tma_load_2d_pair(b_dst + P_BOX, tmB, fb, k0, b0 + 64);
                     }
                     issued[stage] = static_cast<int>(phase) + 1;
                     if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
@@ -439,9 +460,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             int local = 0;
             bool ok = true;
             bool any = false;
-            const uint32_t idesc = instr_desc(256, 256, OP == OP_GEMM_BX ? 1 : 0);
-            for (int it = pair; ok && it < p.num_tiles; it += npairs, ++local) {
+            const TileRange tr = tile_range(p, pair, npairs);
+            for (int it = tr.begin; ok && it < tr.end; it += tr.step, ++local) {
                 const TileItem t = p.tiles[it];
+                const uint32_t idesc = instr_desc(256, t.n_len, OP == OP_GEMM_BX ? 1 : 0);
                 const NsUnit* U = p.units + t.unit;
                 const int kblocks = (k_extent<OP>(*U) + BK - 1) / BK;
                 const int acc = local & 1;
@@ -452,7 +474,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * 256;
+                const uint32_t d_tmem = tmem_base + acc * 256 + t.n_off;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag, p.err,
                                       limit)) {
@@ -503,7 +525,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         tempty_leader[1] = map_to_rank(smem_u32(&tempty_bar[1]), 0);
         int local = 0;
         bool ok = true;
-        for (int it = pair; ok && it < p.num_tiles; it += npairs, ++local) {
+        const TileRange tr = tile_range(p, pair, npairs);
+        for (int it = tr.begin; ok && it < tr.end; it += tr.step, ++local) {
             const TileItem t = p.tiles[it];
             const EpiUnit u = load_epi_unit<OP>(p, t.unit);
             const int acc = local & 1;
@@ -521,7 +544,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int gc0 = col0 + 32 * c;
-                bool nd = r0w < u.m && gc0 < lim_c;
+                const int rel = half * 128 + 32 * c;          // column within the tile
+                bool nd = r0w < u.m && gc0 < lim_c && rel >= t.n_off &&
+                          rel < t.n_off + t.n_len;
                 if (OP != OP_GEMM_BX) nd = nd && gc0 >= r0w;      // upper blocks only
                 need[c] = nd;
             }
