@@ -169,6 +169,14 @@ MUON_API int muon_last_launch_count(muon_handle h);
 MUON_API int muon_debug_set_exports(muon_handle h, int n, float* const* w_f32,
                            void* const* o_bf16);
 
+/* Failure-path check of the kernels' bounded waits: launches one block that
+ * waits on a barrier nothing arrives at, with a limit of `limit_ms`
+ * (1..10000) milliseconds, and reads the device error word `err_word` (a
+ * caller-owned device int).  Returns MUON_ERR_TIMEOUT when the wait ran out
+ * and reported it as the tensor-core kernels do (the expected outcome); the
+ * CUDA context stays usable.  Makes no other change. */
+MUON_API int muon_debug_wait_timeout(muon_handle h, int* err_word, int limit_ms);
+
 /* Plan statistics for `mode`/`nb`: number of units (matrices or blocks),
  * groups, and tiles of the symmetric-product and GEMM stages. */
 typedef struct {

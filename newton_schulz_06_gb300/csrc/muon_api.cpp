@@ -101,6 +101,7 @@ struct muon_ctx {
     bool pair = true;          // CTA-pair kernels (256 x 256 tiles)
     bool fuse = true;          // pair mode: normalisation fused into iteration 1
     bool fuse_update = false;  // pair mode: update fused into the last GEMM
+    int stages = 6;            // pair mode: TMA pipeline depth (4..6)
     int max_pairs = 0;
 };
 
@@ -632,6 +633,10 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     h->pair = pair;
     h->fuse = fuse;
     h->fuse_update = fuse_update;
+    if (const char* st = std::getenv("MUON_STAGES")) {
+        const int v = std::atoi(st);
+        if (v >= 4 && v <= 6) h->stages = v;
+    }
     if (pair) {
         h->max_pairs = ns_pair_max_clusters();
         if (h->max_pairs < 1) {
@@ -804,7 +809,7 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
                 L.pair_off = h->pair ? reinterpret_cast<const int32_t*>(ws + q.oo) : nullptr;
                 if (!begin(q.st)) return fail(h, MUON_ERR_CUDA, "event create");
                 if (h->pair)
-                    e = launch_ns_pair(q.op, L, q.np, h->stream);
+                    e = launch_ns_pair(q.op, L, q.np, h->stages, h->stream);
                 else
                     e = launch_ns(q.op, L, std::min(q.n, h->num_sms), h->stream);
                 end();
@@ -903,6 +908,26 @@ int muon_debug_set_exports(muon_handle h, int n, float* const* w_f32, void* cons
     }
     h->plan.valid = false;
     return MUON_OK;
+}
+
+int muon_debug_wait_timeout(muon_handle h, int* err_word, int limit_ms) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (h->device == MUON_HOST_ONLY) return fail(h, MUON_ERR_STATE, "host-only handle");
+    if (!err_word || limit_ms < 1 || limit_ms > 10000)
+        return fail(h, MUON_ERR_INVALID_ARG, "need an error word and 1 <= limit_ms <= 10000");
+    DeviceGuard guard(h->device);
+    cudaError_t e = cudaMemsetAsync(err_word, 0, sizeof(int), h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "error word clear");
+    e = launch_wait_timeout_check(err_word, static_cast<unsigned long long>(limit_ms) * 1000000ull,
+                                  h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "wait check launch");
+    e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "wait check sync");
+    int word = 0;
+    e = cudaMemcpy(&word, err_word, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(h, e, "wait check read");
+    if (word == DEV_ERR_TIMEOUT) return fail(h, MUON_ERR_TIMEOUT, "bounded wait ran out (expected)");
+    return fail(h, MUON_ERR_STATE, "the bounded wait did not report a timeout");
 }
 
 int muon_get_plan_info(muon_handle h, int mode, int nb, muon_plan_info* out) {

@@ -123,7 +123,9 @@ cudaError_t launch_ew_update(const EwLaunch& p, int grid, cudaStream_t s);
 cudaError_t launch_ns(NsOp op, const NsLaunch& p, int grid, cudaStream_t s);
 size_t ns_smem_bytes();
 // CTA-pair (cta_group::2) kernels on 256 x 256 tiles; `pairs` clusters of 2.
-cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, cudaStream_t s);
+cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, int stages, cudaStream_t s);
 int ns_pair_max_clusters();
+// One-block kernel whose bounded wait must run out (failure-path check).
+cudaError_t launch_wait_timeout_check(int* err, unsigned long long limit_ns, cudaStream_t s);
 
 }  // namespace muon

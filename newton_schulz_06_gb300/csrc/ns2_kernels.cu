@@ -31,7 +31,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int P_STAGES = 6;
+constexpr int P_STAGES_MAX = 6;
 constexpr int P_HALF = 128;                        // rows per CTA
 constexpr int P_A_BYTES = P_HALF * BK * 2;         // 16 KB
 constexpr int P_B_BYTES = P_HALF * BK * 2;         // 16 KB
@@ -41,9 +41,9 @@ constexpr int P_EPI_WARPS = 8;                     // 2 per TMEM lane group
 constexpr int P_THREADS = 64 + 32 * P_EPI_WARPS;
 constexpr int P_BLK = 32 * 32 * 2;                 // one 32x32 bf16 block
 constexpr int P_EPI_BYTES = P_EPI_WARPS * 2 * P_BLK;   // input + staging per warp
-constexpr int P_STAGE_BYTES = P_STAGES * (P_A_BYTES + P_B_BYTES);
-constexpr int P_EPI_OFF = P_STAGE_BYTES + 1024;    // after the barrier block
-constexpr int P_SMEM = P_EPI_OFF + P_EPI_BYTES + 1024;
+// Shared memory of a kernel with ST pipeline stages.
+template <int ST> __host__ __device__ constexpr int p_epi_off() { return ST * (P_A_BYTES + P_B_BYTES) + 1024; }
+template <int ST> __host__ __device__ constexpr int p_smem() { return p_epi_off<ST>() + P_EPI_BYTES + 1024; }
 
 __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
@@ -343,9 +343,10 @@ __device__ __forceinline__ TileRange tile_range(const NsLaunch& p, int pair, int
     return r;
 }
 
-template <int OP>
+template <int OP, int P_STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     ns2_kernel(const __grid_constant__ NsLaunch p) {
+    constexpr int P_EPI_OFF = p_epi_off<P_STAGES>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -650,19 +651,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     }
 }
 
-template <int OP>
-cudaError_t launch_pair_op(const NsLaunch& p, int pairs, cudaStream_t s) {
+template <int OP, int ST>
+cudaError_t launch_pair_st(const NsLaunch& p, int pairs, cudaStream_t s) {
     static int attr_done[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
         cudaError_t e = cudaFuncSetAttribute(
-            ns2_kernel<OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
+            ns2_kernel<OP, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize, p_smem<ST>());
         if (e != cudaSuccess) return e;
         attr_done[dev] = 1;
     }
-    ns2_kernel<OP><<<2 * pairs, P_THREADS, P_SMEM, s>>>(p);
+    ns2_kernel<OP, ST><<<2 * pairs, P_THREADS, p_smem<ST>(), s>>>(p);
     return cudaGetLastError();
+}
+
+template <int OP>
+cudaError_t launch_pair_op(const NsLaunch& p, int pairs, int stages, cudaStream_t s) {
+    switch (stages) {
+        case 4: return launch_pair_st<OP, 4>(p, pairs, s);
+        case 5: return launch_pair_st<OP, 5>(p, pairs, s);
+        default: return launch_pair_st<OP, 6>(p, pairs, s);
+    }
 }
 
 }  // namespace
@@ -672,17 +682,18 @@ int ns_pair_max_clusters() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (cached[dev]) return cached[dev];
-    cudaError_t e = cudaFuncSetAttribute(ns2_kernel<OP_GEMM_BX>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(ns2_kernel<OP_GEMM_BX, P_STAGES_MAX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         p_smem<P_STAGES_MAX>());
     if (e != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
     cfg.blockDim = dim3(P_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = P_SMEM;
+    cfg.dynamicSmemBytes = p_smem<P_STAGES_MAX>();
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, ns2_kernel<OP_GEMM_BX>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, ns2_kernel<OP_GEMM_BX, P_STAGES_MAX>, &cfg);
     if (e != cudaSuccess || n <= 0) {
         cudaGetLastError();
         n = sms / 2;
@@ -691,13 +702,41 @@ int ns_pair_max_clusters() {
     return n;
 }
 
-cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, cudaStream_t s) {
+cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, int stages,
+                           cudaStream_t s) {
     switch (op) {
-        case OP_SYRK_X: return launch_pair_op<OP_SYRK_X>(p, pairs, s);
-        case OP_SYRK_A: return launch_pair_op<OP_SYRK_A>(p, pairs, s);
-        case OP_GEMM_BX: return launch_pair_op<OP_GEMM_BX>(p, pairs, s);
+        case OP_SYRK_X: return launch_pair_op<OP_SYRK_X>(p, pairs, stages, s);
+        case OP_SYRK_A: return launch_pair_op<OP_SYRK_A>(p, pairs, stages, s);
+        case OP_GEMM_BX: return launch_pair_op<OP_GEMM_BX>(p, pairs, stages, s);
     }
     return cudaErrorInvalidValue;
+}
+
+}  // namespace muon
+
+// ---------------------------------------------------------------------------
+// Failure-path check of the bounded wait: one thread waits on an mbarrier
+// that nothing ever arrives at; after `limit_ns` the wait records
+// DEV_ERR_TIMEOUT in *err and returns, leaving the context usable.
+namespace muon {
+namespace {
+
+__global__ void wait_timeout_kernel(int* err, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // phase 0 never completes: no thread arrives
+    ptx::wait_bounded(ptx::smem_u32(&bar), 0, &abort_flag, err, limit_ns);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_timeout_check(int* err, unsigned long long limit_ns, cudaStream_t s) {
+    wait_timeout_kernel<<<1, 32, 0, s>>>(err, limit_ns);
+    return cudaGetLastError();
 }
 
 }  // namespace muon
