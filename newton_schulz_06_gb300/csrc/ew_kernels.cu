@@ -18,12 +18,14 @@
 namespace muon {
 namespace {
 
-__device__ __forceinline__ int find_unit(const EwUnit* __restrict__ units,
-                                         int n, int64_t t) {
+// Unit of tile t: binary search in the compact tile_base array (a few cache
+// lines, L1-resident after the first tiles).
+__device__ __forceinline__ int find_unit(const int64_t* __restrict__ tile_base, int n,
+                                         int64_t t) {
     int lo = 0, hi = n - 1;
     while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (units[mid].tile_base <= t) lo = mid; else hi = mid - 1;
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(tile_base + mid) <= t) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
@@ -165,18 +167,23 @@ __device__ __forceinline__ TileGeom geom_of(const EwU& U, int64_t t) {
 // 64 x 64 tile; only transposed units go through shared memory.
 __global__ void __launch_bounds__(EW_THREADS, 4)
 ew_momentum_kernel(const EwLaunch p) {
+    grid_dependency_wait();
+    allow_dependent_launch();
     __shared__ float sU[EW_TILE][EW_TILE + 1];
     __shared__ float red[2][EW_THREADS / 32];
     const int i = threadIdx.x >> 4;          // 0..15
     const int j4 = (threadIdx.x & 15) * 4;   // 0..60
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (blockIdx.x >= p.num_tiles) return;
-    int u = find_unit(p.units, p.num_units, blockIdx.x);
+    int u = find_unit(p.tile_base, p.num_units, blockIdx.x);
     EwU U = load_ewu(p.units + u);
     int parity = 0;
     // grid-stride: concurrent blocks work on neighbouring tiles
     for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, parity ^= 1) {
-        while (t >= U.tile_end) U = load_ewu(p.units + (++u));
+        if (t >= U.tile_end) {
+            u = find_unit(p.tile_base, p.num_units, t);
+            U = load_ewu(p.units + u);
+        }
         const TileGeom g = geom_of(U, t);
         float uv[4][4];
 #pragma unroll
@@ -237,6 +244,8 @@ ew_momentum_kernel(const EwLaunch p) {
 // inv_norm = 1 / (||U|| + eps).  One block per unit: thread k sums tiles
 // k, k + 256, ... in order, then a fixed tree combines the 256 sums.
 __global__ void __launch_bounds__(256) ew_norm_kernel(const EwLaunch p) {
+    grid_dependency_wait();
+    allow_dependent_launch();
     __shared__ double red[256];
     const int u = blockIdx.x;
     const EwUnit& U = p.units[u];
@@ -259,11 +268,13 @@ __global__ void __launch_bounds__(256) ew_norm_kernel(const EwLaunch p) {
 // Pass 2: X0 = bf16(U * inv_norm) in the X orientation.
 __global__ void __launch_bounds__(EW_THREADS)
 ew_normalise_kernel(const EwLaunch p) {
+    grid_dependency_wait();
+    allow_dependent_launch();
     __shared__ float sU[EW_TILE][EW_TILE + 1];
     const int i = threadIdx.x >> 4;
     const int j4 = (threadIdx.x & 15) * 4;
     for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-        const int u = find_unit(p.units, p.num_units, t);
+        const int u = find_unit(p.tile_base, p.num_units, t);
         const EwUnit& U = p.units[u];
         const TileGeom g = tile_geom(U, u, t);
         const bool vec = U.vec_ok != 0;
@@ -306,11 +317,13 @@ ew_normalise_kernel(const EwLaunch p) {
 // Update: W <- W - lr*scale*O with O read from the final iterate.
 __global__ void __launch_bounds__(EW_THREADS)
 ew_update_kernel(const EwLaunch p) {
+    grid_dependency_wait();
+    allow_dependent_launch();
     __shared__ float sX[EW_TILE][EW_TILE + 1];
     const int i = threadIdx.x >> 4;
     const int j4 = (threadIdx.x & 15) * 4;
     for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-        const int u = find_unit(p.units, p.num_units, t);
+        const int u = find_unit(p.tile_base, p.num_units, t);
         const EwUnit& U = p.units[u];
         const TileGeom g = tile_geom(U, u, t);
         const bool vec = U.vec_ok != 0;
@@ -355,24 +368,26 @@ ew_update_kernel(const EwLaunch p) {
 
 }  // namespace
 
+namespace {
+bool g_programmatic = true;
+}
+void set_programmatic_launch(bool on) { g_programmatic = on; }
+bool programmatic_launch() { return g_programmatic; }
+
 cudaError_t launch_ew_momentum(const EwLaunch& p, int grid, cudaStream_t s) {
-    ew_momentum_kernel<<<grid, EW_THREADS, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(ew_momentum_kernel, dim3(grid), dim3(EW_THREADS), 0, s, p);
 }
 
 cudaError_t launch_ew_norm(const EwLaunch& p, cudaStream_t s) {
-    ew_norm_kernel<<<p.num_units, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(ew_norm_kernel, dim3(p.num_units), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_ew_normalise(const EwLaunch& p, int grid, cudaStream_t s) {
-    ew_normalise_kernel<<<grid, EW_THREADS, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(ew_normalise_kernel, dim3(grid), dim3(EW_THREADS), 0, s, p);
 }
 
 cudaError_t launch_ew_update(const EwLaunch& p, int grid, cudaStream_t s) {
-    ew_update_kernel<<<grid, EW_THREADS, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(ew_update_kernel, dim3(grid), dim3(EW_THREADS), 0, s, p);
 }
 
 }  // namespace muon

@@ -54,6 +54,7 @@ struct UnitDesc {
 struct GroupDesc {
     int u0 = 0, u1 = 0;                      // unit range [u0, u1)
     size_t ew_off = 0, ns_off = 0;           // metadata offsets in ws
+    size_t tb_off = 0;                       // int64 tile_base[units + 1]
     size_t t_sx_off = 0, t_sa_off = 0, t_g_off = 0;
     int n_sx = 0, n_sa = 0, n_g = 0;
     // CTA-pair schedules: per-pair offsets into the tile lists
@@ -380,6 +381,9 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         size_t buf_off = align_up(part_off + size_t(tiles) * 4 * EW_PARTIALS_PER_TILE, 1024);
 
         off = align_up(off, 256);
+        g.tb_off = off;
+        off += sizeof(int64_t) * (nu + 1);
+        off = align_up(off, 256);
         g.ew_off = off;
         off += sizeof(EwUnit) * nu;
         off = align_up(off, 256);
@@ -431,6 +435,9 @@ int build_plan(muon_ctx* h, int mode, int nb) {
             e.tiles_n = static_cast<int32_t>(ceil_div(u.n, EW_TILE));
             e.tile_base = tile_base;
             e.tile_count = u.ew_tiles;
+            reinterpret_cast<int64_t*>(meta.data() + g.tb_off)[i - g.u0] = tile_base;
+            reinterpret_cast<int64_t*>(meta.data() + g.tb_off)[i - g.u0 + 1] =
+                tile_base + u.ew_tiles;
             e.shape_scale = u.scale;
             tile_base += u.ew_tiles;
             std::memcpy(meta.data() + g.ew_off + sizeof(EwUnit) * (i - g.u0), &e, sizeof(e));
@@ -633,6 +640,7 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     h->pair = pair;
     h->fuse = fuse;
     h->fuse_update = fuse_update;
+    if (const char* pd = std::getenv("MUON_PDL")) set_programmatic_launch(std::string(pd) != "0");
     if (const char* st = std::getenv("MUON_STAGES")) {
         const int v = std::atoi(st);
         if (v >= 4 && v <= 6) h->stages = v;
@@ -757,6 +765,7 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         const size_t part_off = align_up(inv_off + size_t(nu) * 4, 256);
         EwLaunch ew{};
         ew.units = reinterpret_cast<const EwUnit*>(ws + g.ew_off);
+        ew.tile_base = reinterpret_cast<const int64_t*>(ws + g.tb_off);
         ew.num_units = nu;
         ew.num_tiles = g.ew_tiles;
         ew.partial = reinterpret_cast<float*>(ws + part_off);

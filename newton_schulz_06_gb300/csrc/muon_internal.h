@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace muon {
 
 // Tile edge of the element-wise stages (momentum, normalise, update).
@@ -103,6 +105,7 @@ struct NsLaunch {
 
 struct EwLaunch {
     const EwUnit* units;
+    const int64_t* tile_base;   // units' first tiles, num_units + 1 entries
     int32_t write_x;         // momentum pass also stores bf16(U) into x[0]
     int32_t num_units;
     int64_t num_tiles;       // total element-wise tiles of the group
@@ -114,6 +117,40 @@ struct EwLaunch {
     int32_t src;             // X buffer holding the final iterate (update)
     float eps;
 };
+
+// Programmatic dependent launch: kernels are launched so that they may start
+// while the previous kernel in the stream finishes; each kernel waits
+// (griddepcontrol.wait) before it touches memory that kernel wrote.
+void set_programmatic_launch(bool on);
+bool programmatic_launch();
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic_launch() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+#ifdef __CUDACC__
+// Waits until the grids this kernel depends on have completed and their
+// writes are visible (no-op without programmatic launch).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel in the stream start launching its blocks.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
 
 // Launch wrappers (defined in the .cu files).  Return cudaGetLastError().
 cudaError_t launch_ew_momentum(const EwLaunch& p, int grid, cudaStream_t s);

@@ -394,6 +394,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     tc_fence_before();
     cluster_sync_all();      // peer barriers initialised before any remote use
     tc_fence_after();
+    // everything above overlaps the previous kernel's tail; from here on the
+    // kernel reads what earlier kernels wrote
+    grid_dependency_wait();
+    allow_dependent_launch();
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t limit = p.wait_limit_ns;
 
@@ -662,8 +666,8 @@ cudaError_t launch_pair_st(const NsLaunch& p, int pairs, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_done[dev] = 1;
     }
-    ns2_kernel<OP, ST><<<2 * pairs, P_THREADS, p_smem<ST>(), s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(ns2_kernel<OP, ST>, dim3(2 * pairs), dim3(P_THREADS), p_smem<ST>(), s,
+                         p);
 }
 
 template <int OP>

@@ -343,6 +343,8 @@ ns_kernel(const __grid_constant__ NsLaunch p) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    grid_dependency_wait();
+    allow_dependent_launch();
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t limit = p.wait_limit_ns;
 
@@ -542,8 +544,7 @@ cudaError_t launch_op(const NsLaunch& p, int grid, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_done[dev] = 1;
     }
-    ns_kernel<OP><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(ns_kernel<OP>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, p);
 }
 
 }  // namespace
