@@ -180,10 +180,7 @@ ew_momentum_kernel(const EwLaunch p) {
     int parity = 0;
     // grid-stride: concurrent blocks work on neighbouring tiles
     for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, parity ^= 1) {
-        if (t >= U.tile_end) {
-            u = find_unit(p.tile_base, p.num_units, t);
-            U = load_ewu(p.units + u);
-        }
+        while (t >= U.tile_end) U = load_ewu(p.units + (++u));
         const TileGeom g = geom_of(U, t);
         float uv[4][4];
 #pragma unroll

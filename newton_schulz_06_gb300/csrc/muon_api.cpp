@@ -55,6 +55,7 @@ struct GroupDesc {
     int u0 = 0, u1 = 0;                      // unit range [u0, u1)
     size_t ew_off = 0, ns_off = 0;           // metadata offsets in ws
     size_t tb_off = 0;                       // int64 tile_base[units + 1]
+    bool w_tma = true;                       // every unit's W fits te_w
     size_t t_sx_off = 0, t_sa_off = 0, t_g_off = 0;
     int n_sx = 0, n_sa = 0, n_g = 0;
     // CTA-pair schedules: per-pair offsets into the tile lists
@@ -101,7 +102,10 @@ struct muon_ctx {
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     bool pair = true;          // CTA-pair kernels (256 x 256 tiles)
     bool fuse = true;          // pair mode: normalisation fused into iteration 1
-    bool fuse_update = false;  // pair mode: update fused into the last GEMM
+    // pair mode: 0 = separate update pass, 1 = update folded into the last
+    // GEMM through registers, 2 = folded in through TMA-loaded W blocks
+    // (groups whose weights are all bf16 and 16-byte aligned; else pass 0)
+    int fuse_update = 2;
     int stages = 6;            // pair mode: TMA pipeline depth (4..6)
     int max_pairs = 0;
 };
@@ -452,6 +456,15 @@ int build_plan(muon_ctx* h, int mode, int nb) {
             if ((rc = encode_map(h, &ns.te_x[1], xb1, u.n, u.m, u.ld_x, 32))) return rc;
             if ((rc = encode_map(h, &ns.te_a, ab, u.m, u.m, u.ld_mm, 32))) return rc;
             if ((rc = encode_map(h, &ns.te_b, bb, u.m, u.m, u.ld_mm, 32))) return rc;
+            {
+                const bool ok = pr.w_dtype == MUON_BF16 && al(e.w, 16) && (pr.ld_w % 8 == 0);
+                if (ok) {
+                    if ((rc = encode_map(h, &ns.te_w, e.w, u.cols, u.rows, pr.ld_w, 32)))
+                        return rc;
+                } else {
+                    g.w_tma = false;
+                }
+            }
             ns.x[0] = e.x[0];
             ns.x[1] = e.x[1];
             ns.a = reinterpret_cast<__nv_bfloat16*>(ab);
@@ -599,7 +612,10 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     const char* fz = std::getenv("MUON_FUSE");
     const bool fuse = !(fz && std::string(fz) == "0");
     const char* fu = std::getenv("MUON_FUSE_UPDATE");
-    const bool fuse_update = fuse && fu && std::string(fu) == "1";
+    int fuse_update = 2;
+    if (fu) fuse_update = std::atoi(fu);
+    if (fuse_update < 0 || fuse_update > 2) fuse_update = 2;
+    if (!fuse) fuse_update = 0;
     if (device == MUON_HOST_ONLY) {
         muon_ctx* h = new muon_ctx();
         h->device = MUON_HOST_ONLY;
@@ -807,7 +823,10 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         for (int s = 0; s < ns_steps; ++s) {
             L.src = cur;
             L.first = (fused && s == 0) ? 1 : 0;
-            L.last = (fused && h->fuse_update && s == ns_steps - 1) ? 1 : 0;
+            const bool last = s == ns_steps - 1;
+            const bool upd_regs = fused && h->fuse_update == 1;
+            const bool upd_tma = fused && h->fuse_update == 2 && g.w_tma;
+            L.last = (last && (upd_regs || upd_tma)) ? 1 : 0;
             const struct { NsOp op; size_t off; int n; int st; size_t oo; int np; } seq[3] = {
                 {OP_SYRK_X, g.t_sx_off, g.n_sx, ST_SYRK1, g.o_sx_off, g.p_sx},
                 {OP_SYRK_A, g.t_sa_off, g.n_sa, ST_SYRK2, g.o_sa_off, g.p_sa},
@@ -817,7 +836,9 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
                 L.num_tiles = q.n;
                 L.pair_off = h->pair ? reinterpret_cast<const int32_t*>(ws + q.oo) : nullptr;
                 if (!begin(q.st)) return fail(h, MUON_ERR_CUDA, "event create");
-                if (h->pair)
+                if (h->pair && q.op == OP_GEMM_BX && L.last && upd_tma)
+                    e = launch_ns_pair_update(L, q.np, h->stream);
+                else if (h->pair)
                     e = launch_ns_pair(q.op, L, q.np, h->stages, h->stream);
                 else
                     e = launch_ns(q.op, L, std::min(q.n, h->num_sms), h->stream);
@@ -826,7 +847,9 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
             }
             cur ^= 1;
         }
-        if (!(fused && h->fuse_update)) {
+        const bool update_folded =
+            fused && (h->fuse_update == 1 || (h->fuse_update == 2 && g.w_tma));
+        if (!update_folded) {
             ew.src = cur;
             if (!begin(ST_UPDATE)) return fail(h, MUON_ERR_CUDA, "event create");
             e = launch_ew_update(ew, ew_grid, h->stream);

@@ -62,6 +62,9 @@ struct alignas(128) NsUnit {
     CUtensorMap te_x[2];
     CUtensorMap te_a;
     CUtensorMap te_b;
+    // The unit's weight W (bf16, W orientation, {32, 32} boxes, 64-byte
+    // swizzle) when the update is folded into the last GEMM (else unused).
+    CUtensorMap te_w;
     __nv_bfloat16* x[2];
     __nv_bfloat16* a;
     __nv_bfloat16* b;
@@ -161,6 +164,8 @@ cudaError_t launch_ns(NsOp op, const NsLaunch& p, int grid, cudaStream_t s);
 size_t ns_smem_bytes();
 // CTA-pair (cta_group::2) kernels on 256 x 256 tiles; `pairs` clusters of 2.
 cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, int stages, cudaStream_t s);
+// Last GEMM with W <- W - lr*scale*O folded in (W blocks by TMA; bf16 W).
+cudaError_t launch_ns_pair_update(const NsLaunch& p, int pairs, cudaStream_t s);
 int ns_pair_max_clusters();
 // One-block kernel whose bounded wait must run out (failure-path check).
 cudaError_t launch_wait_timeout_check(int* err, unsigned long long limit_ns, cudaStream_t s);

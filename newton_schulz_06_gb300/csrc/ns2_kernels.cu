@@ -40,10 +40,16 @@ constexpr int P_TMEM_COLS = 512;
 constexpr int P_EPI_WARPS = 8;                     // 2 per TMEM lane group
 constexpr int P_THREADS = 64 + 32 * P_EPI_WARPS;
 constexpr int P_BLK = 32 * 32 * 2;                 // one 32x32 bf16 block
-constexpr int P_EPI_BYTES = P_EPI_WARPS * 2 * P_BLK;   // input + staging per warp
+// per epilogue warp: input and staging blocks (+ a W block when the update is
+// folded into the last GEMM)
+template <int FW> __host__ __device__ constexpr int p_epi_bytes() {
+    return P_EPI_WARPS * (FW ? 3 : 2) * P_BLK;
+}
 // Shared memory of a kernel with ST pipeline stages.
 template <int ST> __host__ __device__ constexpr int p_epi_off() { return ST * (P_A_BYTES + P_B_BYTES) + 1024; }
-template <int ST> __host__ __device__ constexpr int p_smem() { return p_epi_off<ST>() + P_EPI_BYTES + 1024; }
+template <int ST, int FW> __host__ __device__ constexpr int p_smem() {
+    return p_epi_off<ST>() + p_epi_bytes<FW>() + 1024;
+}
 
 __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
@@ -85,6 +91,7 @@ __device__ __forceinline__ int k_extent(const NsUnit& U) {
 struct EpiUnit {
     const CUtensorMap* te_in;    // epilogue input blocks (GEMM: X, SYRK-2: A)
     const CUtensorMap* te_out;   // output blocks (A, B or X')
+    const CUtensorMap* te_w;     // weight blocks (update folded into the last GEMM)
     int m, n;
     int64_t ld_x, ld_mm;
     const __nv_bfloat16* xin;    // GEMM: current iterate
@@ -106,6 +113,7 @@ __device__ __forceinline__ EpiUnit load_epi_unit(const NsLaunch& p, int unit) {
     EpiUnit e;
     e.te_in = (OP == OP_GEMM_BX) ? &U->te_x[p.src] : &U->te_a;
     e.te_out = (OP == OP_SYRK_X) ? &U->te_a : (OP == OP_SYRK_A) ? &U->te_b : &U->te_x[p.src ^ 1];
+    e.te_w = &U->te_w;
     e.m = U->m;
     e.n = U->n;
     e.ld_x = U->ld_x;
@@ -325,6 +333,65 @@ __device__ __forceinline__ void stage_free(int lane) {
     __syncwarp();
 }
 
+// Lane 0: TMA loads of the epilogue input block at (x, y) and, when the
+// update is folded in (FW), of the matching W block (at (x, y) in the
+// weight's orientation, or (y, x) for a transposed unit), on one barrier.
+template <int FW>
+__device__ __forceinline__ void issue_inputs(const EpiUnit& u, uint8_t* s_in, uint8_t* s_w,
+                                             uint32_t bar, int x, int y) {
+    fence_proxy_async_smem();
+    mbar_expect_tx(bar, FW ? 2 * P_BLK : P_BLK);
+    tma_load_2d(smem_u32(s_in), u.te_in, bar, x, y);
+    if (FW) {
+        if (u.transposed) tma_load_2d(smem_u32(s_w), u.te_w, bar, y, x);
+        else tma_load_2d(smem_u32(s_w), u.te_w, bar, x, y);
+    }
+}
+
+// The update folded into the last GEMM, one 32 x 32 block: O = bf16(v) (the
+// final iterate), W <- W - lr * shape_scale * O in W's own orientation, the
+// new W staged in `stage` and TMA-stored.  Same arithmetic as the separate
+// update pass (fp32 fma on the bf16 O, stored with round-to-nearest-even).
+__device__ __forceinline__ void fused_update_block(const EpiUnit& u, int r0w, int gc0, int lane,
+                                                   const float (&v)[32], const uint8_t* s_w,
+                                                   uint8_t* stage) {
+    float o[32], w[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) o[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
+    int wrow, wcol0, wrows, wcols;      // this lane's W row segment
+    if (!u.transposed) {
+        ld_row_bf16(s_w, lane, w);
+        wrow = r0w + lane;
+        wcol0 = gc0;
+        wrows = u.m;
+        wcols = u.n;
+    } else {
+        // O^T through the stage: lane jj then owns W row gc0 + jj
+        st_col_bf16(stage, lane, o);
+        __syncwarp();
+        ld_row_bf16(stage, lane, o);
+        ld_row_bf16(s_w, lane, w);
+        __syncwarp();                   // all reads of the stage are done
+        wrow = gc0 + lane;
+        wcol0 = r0w;
+        wrows = u.n;
+        wcols = u.m;
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) w[e] = fmaf(-u.step, o[e], w[e]);
+    st_row_bf16(stage, lane, w);
+    if ((u.w_dbg || u.o_dbg) && wrow < wrows) {
+        const int64_t doff = static_cast<int64_t>(wrow) * u.ld_dbg + wcol0;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            if (wcol0 + e >= wcols) break;
+            if (u.w_dbg) u.w_dbg[doff + e] = w[e];
+            if (u.o_dbg) u.o_dbg[doff + e] = __float2bfloat16_rn(o[e]);
+        }
+    }
+    store_block(u.te_w, stage, u.transposed ? r0w : gc0, u.transposed ? gc0 : r0w, lane);
+}
+
 // The tiles of pair `pair`: a planner-built range, or a stride over all.
 struct TileRange {
     int begin, end, step;
@@ -343,7 +410,7 @@ __device__ __forceinline__ TileRange tile_range(const NsLaunch& p, int pair, int
     return r;
 }
 
-template <int OP, int P_STAGES>
+template <int OP, int P_STAGES, int FW>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     ns2_kernel(const __grid_constant__ NsLaunch p) {
     constexpr int P_EPI_OFF = p_epi_off<P_STAGES>();
@@ -360,6 +427,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     uint64_t* drain_bar = bars + 2 * P_STAGES + 4;
     uint64_t* in_bar = bars + 2 * P_STAGES + 5;               // one per epilogue warp
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_bar + P_EPI_WARPS);
+    constexpr int EPI_BLKS = FW ? 3 : 2;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -519,9 +587,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         const int ew = warp - 2;
         const int lg = warp & 3;
         const int half = ew >> 2;
-        uint8_t* epi = smem + P_EPI_OFF + ew * 2 * P_BLK;
+        uint8_t* epi = smem + P_EPI_OFF + ew * EPI_BLKS * P_BLK;
         uint8_t* s_in = epi;
         uint8_t* s_st = epi + P_BLK;
+        uint8_t* s_w = epi + 2 * P_BLK;          // FW only
         const uint32_t inb = smem_u32(&in_bar[ew]);
         uint32_t in_phase = 0;
         bool in_pending = false;      // an input block load is in flight
@@ -560,11 +629,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             const bool uses_in = (OP != OP_SYRK_X);
             if (uses_in && nxt < 4) {
                 in_pending = true;
-                if (lane == 0) {
-                    fence_proxy_async_smem();
-                    mbar_expect_tx(inb, P_BLK);
-                    tma_load_2d(smem_u32(s_in), u.te_in, inb, col0 + 32 * nxt, r0w);
-                }
+                if (lane == 0) issue_inputs<FW>(u, s_in, s_w, inb, col0 + 32 * nxt, r0w);
             }
             ok = wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.err, limit);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -588,17 +653,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                     for (int e = 0; e < 32; ++e)
                         v[e] = (OP == OP_SYRK_A) ? fmaf(p.b, x[e], p.c * v[e])
                                                  : scale * fmaf(p.a, x[e], v[e]);
-                    __syncwarp();      // every lane's reads of s_in are done
+                    if (FW) {
+                        // W <- W - lr*scale*O, O = bf16(v); then s_w is free
+                        stage_free(lane);
+                        fused_update_block(u, r0w, gc0, lane, v, s_w, s_st);
+                    }
+                    __syncwarp();      // every lane's reads of s_in (and s_w) are done
                     nxt = c + 1;
                     while (nxt < 4 && !need[nxt]) ++nxt;
                     if (nxt < 4) {
                         in_pending = true;
-                        if (lane == 0) {
-                            fence_proxy_async_smem();
-                            mbar_expect_tx(inb, P_BLK);
-                            tma_load_2d(smem_u32(s_in), u.te_in, inb, col0 + 32 * nxt, r0w);
-                        }
+                        if (lane == 0)
+                            issue_inputs<FW>(u, s_in, s_w, inb, col0 + 32 * nxt, r0w);
                     }
+                    if (FW) continue;  // the W block is stored; no X' output
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] *= scale;
@@ -655,27 +723,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     }
 }
 
-template <int OP, int ST>
+template <int OP, int ST, int FW>
 cudaError_t launch_pair_st(const NsLaunch& p, int pairs, cudaStream_t s) {
     static int attr_done[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(
-            ns2_kernel<OP, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize, p_smem<ST>());
+        cudaError_t e = cudaFuncSetAttribute(ns2_kernel<OP, ST, FW>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             p_smem<ST, FW>());
         if (e != cudaSuccess) return e;
         attr_done[dev] = 1;
     }
-    return launch_kernel(ns2_kernel<OP, ST>, dim3(2 * pairs), dim3(P_THREADS), p_smem<ST>(), s,
-                         p);
+    return launch_kernel(ns2_kernel<OP, ST, FW>, dim3(2 * pairs), dim3(P_THREADS),
+                         p_smem<ST, FW>(), s, p);
 }
 
 template <int OP>
 cudaError_t launch_pair_op(const NsLaunch& p, int pairs, int stages, cudaStream_t s) {
     switch (stages) {
-        case 4: return launch_pair_st<OP, 4>(p, pairs, s);
-        case 5: return launch_pair_st<OP, 5>(p, pairs, s);
-        default: return launch_pair_st<OP, 6>(p, pairs, s);
+        case 4: return launch_pair_st<OP, 4, 0>(p, pairs, s);
+        case 5: return launch_pair_st<OP, 5, 0>(p, pairs, s);
+        default: return launch_pair_st<OP, 6, 0>(p, pairs, s);
     }
 }
 
@@ -686,18 +755,18 @@ int ns_pair_max_clusters() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (cached[dev]) return cached[dev];
-    cudaError_t e = cudaFuncSetAttribute(ns2_kernel<OP_GEMM_BX, P_STAGES_MAX>,
+    cudaError_t e = cudaFuncSetAttribute(ns2_kernel<OP_GEMM_BX, P_STAGES_MAX, 0>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         p_smem<P_STAGES_MAX>());
+                                         p_smem<P_STAGES_MAX, 0>());
     if (e != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
     cfg.blockDim = dim3(P_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = p_smem<P_STAGES_MAX>();
+    cfg.dynamicSmemBytes = p_smem<P_STAGES_MAX, 0>();
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, ns2_kernel<OP_GEMM_BX, P_STAGES_MAX>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, ns2_kernel<OP_GEMM_BX, P_STAGES_MAX, 0>, &cfg);
     if (e != cudaSuccess || n <= 0) {
         cudaGetLastError();
         n = sms / 2;
@@ -714,6 +783,12 @@ cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, int stages,
         case OP_GEMM_BX: return launch_pair_op<OP_GEMM_BX>(p, pairs, stages, s);
     }
     return cudaErrorInvalidValue;
+}
+
+// The last GEMM with the update folded in through TMA-loaded W blocks: five
+// pipeline stages leave room for a third 2 KB block per epilogue warp.
+cudaError_t launch_ns_pair_update(const NsLaunch& p, int pairs, cudaStream_t s) {
+    return launch_pair_st<OP_GEMM_BX, 5, 1>(p, pairs, s);
 }
 
 }  // namespace muon

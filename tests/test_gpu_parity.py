@@ -148,6 +148,7 @@ def test_output_singular_values_in_band():
 
 
 @pytest.mark.parametrize("fuse_env", [{"MUON_FUSE": "0"},
+                                      {"MUON_FUSE_UPDATE": "0"},
                                       {"MUON_FUSE_UPDATE": "1"},
                                       {"MUON_CTA_GROUP": "1"}])
 def test_alternative_pipelines_match_oracle(fuse_env, monkeypatch):
@@ -162,3 +163,17 @@ def test_alternative_pipelines_match_oracle(fuse_env, monkeypatch):
     for i, tr in enumerate(trips):
         ref = oracle_step(inp[i])
         check_against_oracle(tr, inp[i], wexp[i], oexp[i], ref)
+
+
+def test_update_folded_into_gemm_matches_separate_pass_bitexact(monkeypatch):
+    """The update folded into the last GEMM (TMA-loaded W blocks) and the
+    separate update pass apply the same arithmetic: identical bits."""
+    shapes = [(256, 640), (640, 256), (300, 300), (96, 1000), (768, 2048)]
+    trips = [case(r, c, 300 + i) for i, (r, c) in enumerate(shapes)]
+    clones = [[t.clone() for t in tr] for tr in trips]
+    _, w1, o1, _ = gpu_step(trips)
+    monkeypatch.setenv("MUON_FUSE_UPDATE", "0")
+    _, w2, o2, _ = gpu_step(clones)
+    for i in range(len(shapes)):
+        assert torch.equal(trips[i][0], clones[i][0]), shapes[i]
+        assert torch.equal(w1[i], w2[i]) and torch.equal(o1[i], o2[i]), shapes[i]
