@@ -619,8 +619,8 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     if (device == MUON_HOST_ONLY) {
         muon_ctx* h = new muon_ctx();
         h->device = MUON_HOST_ONLY;
-        h->num_sms = 148;
-        h->max_pairs = 74;
+        h->num_sms = 152;
+        h->max_pairs = 76;
         h->pair = pair;
         *out = h;
         return MUON_OK;
