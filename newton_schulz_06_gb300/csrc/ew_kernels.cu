@@ -183,20 +183,72 @@ ew_momentum_kernel(const EwLaunch p) {
         while (t >= U.tile_end) U = load_ewu(p.units + (++u));
         const TileGeom g = geom_of(U, t);
         float uv[4][4];
+        float mv[4][4], gv[4][4];
+        int nval[4];
+        const bool interior =
+            U.vec && g.wr0 + EW_TILE <= U.rows && g.wc0 + EW_TILE <= U.cols;  // block-uniform
+        if (interior) {
+            // branch-free: the thread's four 16-byte M loads and four G loads
+            // are issued back to back; M and G are streamed (touched once)
+            const int64_t r0 = g.wr0 + i;
+            const float* mp = U.mom + r0 * U.ld_m + g.wc0 + j4;
+            float4 mq[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mq[k] = __ldcs(reinterpret_cast<const float4*>(mp + 16 * k * U.ld_m));
+            if (U.g_dtype == MUON_BF16) {
+                const __nv_bfloat16* gp =
+                    static_cast<const __nv_bfloat16*>(U.g) + r0 * U.ld_g + g.wc0 + j4;
+                uint2 gq[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    gq[k] = __ldcs(reinterpret_cast<const uint2*>(gp + 16 * k * U.ld_g));
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 lo = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&gq[k].x));
+                    const float2 hi = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&gq[k].y));
+                    gv[k][0] = lo.x; gv[k][1] = lo.y; gv[k][2] = hi.x; gv[k][3] = hi.y;
+                }
+            } else {
+                const float* gp = static_cast<const float*>(U.g) + r0 * U.ld_g + g.wc0 + j4;
+                float4 gq[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    gq[k] = __ldcs(reinterpret_cast<const float4*>(gp + 16 * k * U.ld_g));
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    gv[k][0] = gq[k].x; gv[k][1] = gq[k].y; gv[k][2] = gq[k].z; gv[k][3] = gq[k].w;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                mv[k][0] = mq[k].x; mv[k][1] = mq[k].y; mv[k][2] = mq[k].z; mv[k][3] = mq[k].w;
+                nval[k] = 4;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int wr = g.wr0 + i + 16 * k, wc = g.wc0 + j4;
+                nval[k] = max((wr < U.rows) ? min(4, U.cols - wc) : 0, 0);
+                ld4(U.mom, MUON_F32, wr * U.ld_m + wc, nval[k], U.vec, mv[k]);
+                ld4(U.g, U.g_dtype, wr * U.ld_g + wc, nval[k], U.vec, gv[k]);
+            }
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int wr = g.wr0 + i + 16 * k, wc = g.wc0 + j4;
-            int nval = (wr < U.rows) ? min(4, U.cols - wc) : 0;
-            nval = max(nval, 0);
-            float mv[4], gv[4];
-            ld4(U.mom, MUON_F32, wr * U.ld_m + wc, nval, U.vec, mv);
-            ld4(U.g, U.g_dtype, wr * U.ld_g + wc, nval, U.vec, gv);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                mv[e] = fmaf(p.beta, mv[e], gv[e]);
-                uv[k][e] = e < nval ? (p.nesterov ? fmaf(p.beta, mv[e], gv[e]) : mv[e]) : 0.f;
+                mv[k][e] = fmaf(p.beta, mv[k][e], gv[k][e]);
+                uv[k][e] = e < nval[k] ? (p.nesterov ? fmaf(p.beta, mv[k][e], gv[k][e])
+                                                     : mv[k][e])
+                                       : 0.f;
             }
-            st4(U.mom, MUON_F32, wr * U.ld_m + wc, nval, U.vec, mv);
+            if (interior)
+                __stcs(reinterpret_cast<float4*>(U.mom + static_cast<int64_t>(wr) * U.ld_m + wc),
+                       make_float4(mv[k][0], mv[k][1], mv[k][2], mv[k][3]));
+            else
+                st4(U.mom, MUON_F32, wr * U.ld_m + wc, nval[k], U.vec, mv[k]);
         }
         if (U.transposed) {            // block-uniform
 #pragma unroll

@@ -106,7 +106,7 @@ struct muon_ctx {
     // GEMM through registers, 2 = folded in through TMA-loaded W blocks
     // (groups whose weights are all bf16 and 16-byte aligned; else pass 0)
     int fuse_update = 2;
-    int stages = 6;            // pair mode: TMA pipeline depth (4..6)
+    int stages = 5;            // pair mode: TMA pipeline depth (4 or 5)
     int max_pairs = 0;
 };
 
@@ -659,7 +659,7 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     if (const char* pd = std::getenv("MUON_PDL")) set_programmatic_launch(std::string(pd) != "0");
     if (const char* st = std::getenv("MUON_STAGES")) {
         const int v = std::atoi(st);
-        if (v >= 4 && v <= 6) h->stages = v;
+        if (v >= 4 && v <= 5) h->stages = v;
     }
     if (pair) {
         h->max_pairs = ns_pair_max_clusters();

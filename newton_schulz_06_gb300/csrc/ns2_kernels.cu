@@ -31,7 +31,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int P_STAGES_MAX = 6;
+constexpr int P_STAGES_MAX = 5;
 constexpr int P_HALF = 128;                        // rows per CTA
 constexpr int P_A_BYTES = P_HALF * BK * 2;         // 16 KB
 constexpr int P_B_BYTES = P_HALF * BK * 2;         // 16 KB
@@ -40,10 +40,17 @@ constexpr int P_TMEM_COLS = 512;
 constexpr int P_EPI_WARPS = 8;                     // 2 per TMEM lane group
 constexpr int P_THREADS = 64 + 32 * P_EPI_WARPS;
 constexpr int P_BLK = 32 * 32 * 2;                 // one 32x32 bf16 block
-// per epilogue warp: input and staging blocks (+ a W block when the update is
-// folded into the last GEMM)
+// Per epilogue warp: two input slots (an X or A block, plus a W block when
+// the update is folded into the last GEMM), so inputs arrive two blocks
+// ahead, and two staging blocks, so a block is staged while the previous
+// one's TMA store still reads its own.
+constexpr int P_IN_SLOTS = 2;
+template <int FW> __host__ __device__ constexpr int p_in_blk() { return FW ? 2 * P_BLK : P_BLK; }
+template <int FW> __host__ __device__ constexpr int p_epi_warp_bytes() {
+    return P_IN_SLOTS * p_in_blk<FW>() + 2 * P_BLK;
+}
 template <int FW> __host__ __device__ constexpr int p_epi_bytes() {
-    return P_EPI_WARPS * (FW ? 3 : 2) * P_BLK;
+    return P_EPI_WARPS * p_epi_warp_bytes<FW>();
 }
 // Shared memory of a kernel with ST pipeline stages.
 template <int ST> __host__ __device__ constexpr int p_epi_off() { return ST * (P_A_BYTES + P_B_BYTES) + 1024; }
@@ -333,18 +340,29 @@ __device__ __forceinline__ void stage_free(int lane) {
     __syncwarp();
 }
 
-// Lane 0: TMA loads of the epilogue input block at (x, y) and, when the
-// update is folded in (FW), of the matching W block (at (x, y) in the
-// weight's orientation, or (y, x) for a transposed unit), on one barrier.
+// The next of the warp's two staging blocks.  Every use ends with exactly
+// one TMA store (one bulk group), so the buffers alternate with the groups:
+// once at most one group (the other buffer's) still reads shared memory,
+// this buffer is free.
+__device__ __forceinline__ uint8_t* next_stage(uint8_t* st0, uint32_t& st_seq, int lane) {
+    if (lane == 0) bulk_wait_read1();
+    __syncwarp();
+    return st0 + (st_seq++ & 1u) * P_BLK;
+}
+
+// Lane 0: TMA loads of the epilogue input block at (x, y) into input slot
+// `slot` and, when the update is folded in (FW), of the matching W block (at
+// (x, y) in the weight's orientation, or (y, x) for a transposed unit),
+// both on the slot's barrier.
 template <int FW>
-__device__ __forceinline__ void issue_inputs(const EpiUnit& u, uint8_t* s_in, uint8_t* s_w,
-                                             uint32_t bar, int x, int y) {
+__device__ __forceinline__ void issue_inputs(const EpiUnit& u, uint8_t* slot, uint32_t bar,
+                                             int x, int y) {
     fence_proxy_async_smem();
-    mbar_expect_tx(bar, FW ? 2 * P_BLK : P_BLK);
-    tma_load_2d(smem_u32(s_in), u.te_in, bar, x, y);
+    mbar_expect_tx(bar, p_in_blk<FW>());
+    tma_load_2d(smem_u32(slot), u.te_in, bar, x, y);
     if (FW) {
-        if (u.transposed) tma_load_2d(smem_u32(s_w), u.te_w, bar, y, x);
-        else tma_load_2d(smem_u32(s_w), u.te_w, bar, x, y);
+        if (u.transposed) tma_load_2d(smem_u32(slot + P_BLK), u.te_w, bar, y, x);
+        else tma_load_2d(smem_u32(slot + P_BLK), u.te_w, bar, x, y);
     }
 }
 
@@ -425,9 +443,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     uint64_t* tfull_bar = bars + 2 * P_STAGES;
     uint64_t* tempty_bar = bars + 2 * P_STAGES + 2;
     uint64_t* drain_bar = bars + 2 * P_STAGES + 4;
-    uint64_t* in_bar = bars + 2 * P_STAGES + 5;               // one per epilogue warp
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_bar + P_EPI_WARPS);
-    constexpr int EPI_BLKS = FW ? 3 : 2;
+    uint64_t* in_bar = bars + 2 * P_STAGES + 5;    // P_IN_SLOTS per epilogue warp
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_bar + P_IN_SLOTS * P_EPI_WARPS);
+    static_assert(p_smem<P_STAGES, FW>() <= 232448, "shared memory per CTA");
+    static_assert((2 * P_STAGES + 5 + P_IN_SLOTS * P_EPI_WARPS) * 8 + 8 <= 1024,
+                  "barrier area");
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -446,7 +466,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             mbar_init(smem_u32(&tempty_bar[a]), 2 * P_EPI_WARPS);
         }
         mbar_init(smem_u32(drain_bar), 1);
-        for (int w = 0; w < P_EPI_WARPS; ++w) mbar_init(smem_u32(&in_bar[w]), 1);
+        for (int w = 0; w < P_IN_SLOTS * P_EPI_WARPS; ++w) mbar_init(smem_u32(&in_bar[w]), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -581,19 +601,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         // -------------------------------------------- epilogue (both CTAs)
         // warps 2..9: lane group warp % 4 (TMEM rows), column half
         // (warp - 2) / 4 (chunks 4h .. 4h + 3 of the 256 columns).  Blocks of
-        // 32 x 32 go out through a swizzled shared-memory stage and TMA stores
-        // (which also clip at the matrix edge); the epilogue's input blocks
-        // (X for the GEMM, A for SYRK-2) come in by TMA one block ahead.
+        // 32 x 32 go out through two alternating swizzled shared-memory
+        // stages and TMA stores (which also clip at the matrix edge); the
+        // epilogue's input blocks (X for the GEMM, A for SYRK-2, plus W when
+        // the update is folded in) come in by TMA two blocks ahead, the first
+        // two of a tile while its main loop still runs.
         const int ew = warp - 2;
         const int lg = warp & 3;
         const int half = ew >> 2;
-        uint8_t* epi = smem + P_EPI_OFF + ew * EPI_BLKS * P_BLK;
-        uint8_t* s_in = epi;
-        uint8_t* s_st = epi + P_BLK;
-        uint8_t* s_w = epi + 2 * P_BLK;          // FW only
-        const uint32_t inb = smem_u32(&in_bar[ew]);
-        uint32_t in_phase = 0;
-        bool in_pending = false;      // an input block load is in flight
+        uint8_t* epi = smem + P_EPI_OFF + ew * p_epi_warp_bytes<FW>();
+        uint8_t* s_in = epi;                                   // P_IN_SLOTS slots
+        uint8_t* s_st = epi + P_IN_SLOTS * p_in_blk<FW>();     // two staging blocks
+        uint32_t in_seq = 0;     // input loads issued by this warp
+        uint32_t in_use = 0;     // input loads consumed
+        uint32_t st_seq = 0;     // staging blocks used
         uint32_t tempty_leader[2];
         tempty_leader[0] = map_to_rank(smem_u32(&tempty_bar[0]), 0);
         tempty_leader[1] = map_to_rank(smem_u32(&tempty_bar[1]), 0);
@@ -613,8 +634,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 const float inv = p.inv_norm[t.unit];
                 scale = (OP == OP_SYRK_X) ? inv * inv : inv;
             }
-            // which of the 4 blocks this warp stores (warp-uniform)
-            int need[4];
+            // which of the 4 blocks this warp stores (warp-uniform), in order
+            int order[4];
+            int n_need = 0;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int gc0 = col0 + 32 * c;
@@ -622,51 +644,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 bool nd = r0w < u.m && gc0 < lim_c && rel >= t.n_off &&
                           rel < t.n_off + t.n_len;
                 if (OP != OP_GEMM_BX) nd = nd && gc0 >= r0w;      // upper blocks only
-                need[c] = nd;
+                if (nd) order[n_need++] = c;
             }
-            int nxt = 0;
-            while (nxt < 4 && !need[nxt]) ++nxt;
             const bool uses_in = (OP != OP_SYRK_X);
-            if (uses_in && nxt < 4) {
-                in_pending = true;
-                if (lane == 0) issue_inputs<FW>(u, s_in, s_w, inb, col0 + 32 * nxt, r0w);
-            }
+            auto issue = [&](int k) {       // input of the k-th needed block
+                const uint32_t sl = in_seq & 1u;
+                if (lane == 0)
+                    issue_inputs<FW>(u, s_in + sl * p_in_blk<FW>(),
+                                     smem_u32(&in_bar[P_IN_SLOTS * ew + sl]),
+                                     col0 + 32 * order[k], r0w);
+                ++in_seq;
+            };
+            if (uses_in)
+                for (int k = 0; k < n_need && k < P_IN_SLOTS; ++k) issue(k);
             ok = wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.err, limit);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) +
                                    acc * 256 + half * 128;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                if (!need[c]) continue;
+            for (int k = 0; k < n_need; ++k) {
+                const int c = order[k];
                 const int gc0 = col0 + 32 * c;
                 float v[32];
                 tmem_ld32(tbase + 32 * c, v);
                 if (uses_in) {
-                    const bool got = wait_bounded(inb, in_phase, abort_flag, p.err, limit);
+                    const uint32_t sl = in_use & 1u;
+                    const uint8_t* slot = s_in + sl * p_in_blk<FW>();
+                    const bool got = wait_bounded(smem_u32(&in_bar[P_IN_SLOTS * ew + sl]),
+                                                  (in_use >> 1) & 1u, abort_flag, p.err, limit);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-                    in_phase ^= 1;
-                    in_pending = false;
+                    ++in_use;
                     float x[32];
-                    ld_row_bf16(s_in, lane, x);
+                    ld_row_bf16(slot, lane, x);
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         v[e] = (OP == OP_SYRK_A) ? fmaf(p.b, x[e], p.c * v[e])
                                                  : scale * fmaf(p.a, x[e], v[e]);
                     if (FW) {
-                        // W <- W - lr*scale*O, O = bf16(v); then s_w is free
-                        stage_free(lane);
-                        fused_update_block(u, r0w, gc0, lane, v, s_w, s_st);
+                        // W <- W - lr*scale*O, O = bf16(v); no X' output
+                        fused_update_block(u, r0w, gc0, lane, v, slot + P_BLK,
+                                           next_stage(s_st, st_seq, lane));
                     }
-                    __syncwarp();      // every lane's reads of s_in (and s_w) are done
-                    nxt = c + 1;
-                    while (nxt < 4 && !need[nxt]) ++nxt;
-                    if (nxt < 4) {
-                        in_pending = true;
-                        if (lane == 0)
-                            issue_inputs<FW>(u, s_in, s_w, inb, col0 + 32 * nxt, r0w);
-                    }
-                    if (FW) continue;  // the W block is stored; no X' output
+                    __syncwarp();      // every lane's reads of the slot are done
+                    if (k + P_IN_SLOTS < n_need) issue(k + P_IN_SLOTS);
+                    if (FW) continue;
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] *= scale;
@@ -674,33 +696,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 if (OP == OP_GEMM_BX) {
                     if (p.last) {
                         stage_free(lane);
-                        gemm_update_block(u, r0w, gc0, lane, v, s_st);
+                        gemm_update_block(u, r0w, gc0, lane, v, s_st + (st_seq & 1u) * P_BLK);
                     } else {
-                        stage_free(lane);
-                        st_row_bf16(s_st, lane, v);
-                        store_block(u.te_out, s_st, gc0, r0w, lane);
+                        uint8_t* st = next_stage(s_st, st_seq, lane);
+                        st_row_bf16(st, lane, v);
+                        store_block(u.te_out, st, gc0, r0w, lane);
                     }
                 } else if (gc0 == r0w) {
                     // diagonal block: upper part as computed, lower part
                     // mirrored from the upper, so the block is symmetric
-                    stage_free(lane);
-                    st_col_bf16(s_st, lane, v);
+                    uint8_t* st = next_stage(s_st, st_seq, lane);
+                    st_col_bf16(st, lane, v);
                     __syncwarp();
                     float mir[32];
-                    ld_row_bf16(s_st, lane, mir);
+                    ld_row_bf16(st, lane, mir);
                     __syncwarp();
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         if (e < lane) v[e] = mir[e];
-                    st_row_bf16(s_st, lane, v);
-                    store_block(u.te_out, s_st, gc0, r0w, lane);
+                    st_row_bf16(st, lane, v);
+                    store_block(u.te_out, st, gc0, r0w, lane);
                 } else {
-                    stage_free(lane);
-                    st_row_bf16(s_st, lane, v);
-                    store_block(u.te_out, s_st, gc0, r0w, lane);
-                    stage_free(lane);
-                    st_col_bf16(s_st, lane, v);
-                    store_block(u.te_out, s_st, r0w, gc0, lane);   // mirror
+                    uint8_t* st = next_stage(s_st, st_seq, lane);
+                    st_row_bf16(st, lane, v);
+                    store_block(u.te_out, st, gc0, r0w, lane);
+                    st = next_stage(s_st, st_seq, lane);
+                    st_col_bf16(st, lane, v);
+                    store_block(u.te_out, st, r0w, gc0, lane);   // mirror
                 }
             }
             if (!__all_sync(0xffffffffu, ok)) break;
@@ -708,8 +730,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader[acc]);
         }
-        // after an abort: let an input load in flight land before leaving
-        if (in_pending) wait_quiet(inb, in_phase, limit);
+        // after an abort: let input loads in flight land before leaving
+        for (uint32_t q = in_use; q != in_seq; ++q)
+            wait_quiet(smem_u32(&in_bar[P_IN_SLOTS * ew + (q & 1u)]), (q >> 1) & 1u, limit);
         if (lane == 0) bulk_wait_all0();
     }
 
@@ -743,8 +766,7 @@ template <int OP>
 cudaError_t launch_pair_op(const NsLaunch& p, int pairs, int stages, cudaStream_t s) {
     switch (stages) {
         case 4: return launch_pair_st<OP, 4, 0>(p, pairs, s);
-        case 5: return launch_pair_st<OP, 5, 0>(p, pairs, s);
-        default: return launch_pair_st<OP, 6, 0>(p, pairs, s);
+        default: return launch_pair_st<OP, 5, 0>(p, pairs, s);
     }
 }
 
@@ -785,10 +807,10 @@ cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, int stages,
     return cudaErrorInvalidValue;
 }
 
-// The last GEMM with the update folded in through TMA-loaded W blocks: five
-// pipeline stages leave room for a third 2 KB block per epilogue warp.
+// The last GEMM with the update folded in through TMA-loaded W blocks: four
+// pipeline stages leave room for the W blocks of both input slots.
 cudaError_t launch_ns_pair_update(const NsLaunch& p, int pairs, cudaStream_t s) {
-    return launch_pair_st<OP_GEMM_BX, 5, 1>(p, pairs, s);
+    return launch_pair_st<OP_GEMM_BX, 4, 1>(p, pairs, s);
 }
 
 }  // namespace muon

@@ -139,6 +139,11 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// Waits until at most the most recent of this thread's bulk store groups
+// is still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // Waits until this thread's bulk stores are complete.
 __device__ __forceinline__ void bulk_wait_all0() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
