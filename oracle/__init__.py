@@ -10,5 +10,7 @@ from .muon_ref import (  # noqa: F401
     muon_step,
     muon_step_matrix,
     newton_schulz,
+    newton_schulz_distributed,
     shape_scale,
+    shard_ranges,
 )

@@ -290,3 +290,77 @@ def test_pins_reject_planted_scale_and_orientation_mistakes(monkeypatch):
                              beta=0.9, nesterov=False, ns_steps=5, a=A_,
                              b=B_, c=C_)
     assert not np.max(np.abs(out["W"] - expect)) <= 1e-3
+
+
+# --------------------------------------------------------------------------
+# Distributed mode: the iteration over P tensor-parallel slices of the
+# iterate's long side, with the partial first products summed.
+
+@pytest.mark.parametrize("rows,cols,P", [(8, 16, 2), (16, 8, 4), (12, 24, 3),
+                                         (40, 96, 8)])
+def test_distributed_closed_form(rows, cols, P):
+    """The slices' summed partials give the same iteration: the closed form
+    U p^5(s/||s||) V^T of an SVD-constructed input."""
+    s = np.geomspace(1.0, 0.05, min(rows, cols))
+    U, V, G = svd_matrix(rows, cols, s, seed=rows + 7 * cols + P)
+    out = run(np.zeros((rows, cols)), G, np.zeros((rows, cols)), nesterov=False,
+              beta=0.0, mode="distributed", nb=P)
+    assert np.max(np.abs(out["O"] - closed_form_O(U, V, s))) < 1e-9
+
+
+@pytest.mark.parametrize("m,n,P", [(6, 12, 3), (4, 8, 2), (5, 10, 5)])
+def test_distributed_products_against_triple_loops(m, n, P):
+    rng = np.random.default_rng(m * 31 + n)
+    X = rng.standard_normal((m, n))
+    X /= np.linalg.norm(X)
+    got = oracle.newton_schulz_distributed(X, 5, A_, B_, C_, P)
+    want = _loops_ns(X.tolist(), 5, A_, B_, C_)
+    assert np.max(np.abs(got - want)) < 1e-12
+
+
+def test_distributed_one_slice_is_full_and_slices_must_divide():
+    rng = np.random.default_rng(3)
+    W, G, M = (rng.standard_normal((24, 40)) for _ in range(3))
+    a = run(W, G, M, mode="distributed", nb=1)
+    b = run(W, G, M)
+    for k in ("W", "M", "O"):
+        assert np.array_equal(a[k], b[k])
+    with pytest.raises(ValueError):
+        run(W, G, M, mode="distributed", nb=3)      # 3 does not divide 40
+
+
+def _mutant_distributed(kind):
+    def ns(X, steps, a, b, c, shards):
+        X = np.array(X, dtype=np.float64, copy=True)
+        n = X.shape[1]
+        w = n // shards
+        for _ in range(steps):
+            if kind == "short_side":          # slices of the rows instead
+                h = X.shape[0] // shards
+                A = np.zeros((X.shape[0], X.shape[0]))
+                for p in range(shards):
+                    r = slice(p * h, (p + 1) * h)
+                    A[r, r] += X[r] @ X[r].T
+            else:
+                parts = range(shards - 1) if kind == "drop_slice" else range(shards)
+                if kind == "no_reduce":
+                    parts = range(1)
+                A = sum(X[:, p * w:(p + 1) * w] @ X[:, p * w:(p + 1) * w].T
+                        for p in parts)
+            B = b * A + c * (A @ A)
+            X = a * X + B @ X
+        return X
+    return ns
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
+@pytest.mark.parametrize("kind", ["drop_slice", "no_reduce", "short_side"])
+def test_pins_reject_planted_distributed_mistakes(kind, monkeypatch):
+    monkeypatch.setattr(muon_ref, "newton_schulz_distributed",
+                        _mutant_distributed(kind))
+    s = np.geomspace(1.0, 0.05, 8)
+    U, V, G = svd_matrix(8, 16, s, seed=11)
+    out = muon_ref.muon_step(np.zeros((8, 16)), G, np.zeros((8, 16)), lr=0.1,
+                             beta=0.0, nesterov=False, ns_steps=5, a=A_,
+                             b=B_, c=C_, mode="distributed", nb=4)
+    assert not np.max(np.abs(out["O"] - closed_form_O(U, V, s))) <= 1e-3
