@@ -242,7 +242,7 @@ def run_ours(args, wl, world, rank, local, pg):
     import torch
     import __graft_entry__
     __graft_entry__.build()
-    from newton_schulz_06_gb300 import MUON_BLOCKWISE, MUON_FULL, Muon, flops
+    from newton_schulz_06_gb300 import Muon, flops, mode_code
     from newton_schulz_06_gb300 import inputs as I
 
     torch.cuda.set_device(local)
@@ -251,7 +251,7 @@ def run_ours(args, wl, world, rank, local, pg):
     Ws, Gs, Ms = I.make_state(wl, dev)
     trips = list(zip(Ws, Gs, Ms))
     opt = Muon(trips)
-    mode = MUON_BLOCKWISE if wl.mode == "blockwise" else MUON_FULL
+    mode = mode_code(wl.mode)
     opt.ensure_workspace(mode, wl.nb, args.max_workspace)
     info = opt.plan_info(mode, wl.nb)
     useful = flops.useful_flops(wl.shapes, mode=wl.mode, nb=wl.nb)

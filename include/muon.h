@@ -72,6 +72,15 @@ extern "C" {
 /* orthogonalisation modes */
 #define MUON_FULL       0   /* each registered matrix as a whole            */
 #define MUON_BLOCKWISE  1   /* nb equal column blocks, each on its own      */
+/* Distributed mode ("Advancing Emerging Optimizers for Accelerated LLM
+ * Training", section "Distributed mode"): the iteration as a tensor-parallel
+ * group of nb ranks runs it, each rank holding an equal contiguous slice of
+ * the iterate's long side n.  The first product of every iteration is the
+ * sum of the slices' partial products (the all-reduce), added in fp32 in
+ * slice order 0, 1, ..., nb-1; the other two products are as in full mode.
+ * One GPU computes all slices.  nb must divide every n with n / nb a
+ * multiple of 64 (MUON_ERR_UNSUPPORTED otherwise); nb = 1 is full mode. */
+#define MUON_DISTRIBUTED 2
 
 typedef struct muon_ctx* muon_handle;
 
@@ -112,7 +121,8 @@ MUON_API int muon_register_params(muon_handle h, int n, const muon_param* params
  * (the largest single matrix or block plus the plan's tables);
  * *full_bytes: enough to run every matrix in a single group.  Any size in
  * between works; larger sizes give fewer, larger groups.  In blockwise mode
- * nb must divide every registered cols (MUON_ERR_UNSUPPORTED otherwise). */
+ * nb must divide every registered cols, in distributed mode every long side
+ * (see MUON_DISTRIBUTED); MUON_ERR_UNSUPPORTED otherwise. */
 MUON_API int muon_workspace_size(muon_handle h, int mode, int nb, size_t* min_bytes,
                         size_t* full_bytes);
 
@@ -126,8 +136,9 @@ MUON_API int muon_set_workspace(muon_handle h, void* dptr, size_t bytes);
  *   lr, beta, nesterov   learning rate, momentum factor, Nesterov on/off
  *   ns_steps             Newton-Schulz iterations (1..64; 5 is usual)
  *   a, b, c              coefficients of a X + (b A + c A A) X
- *   mode, nb             MUON_FULL (nb ignored) or MUON_BLOCKWISE with nb
- *                        column blocks (nb >= 1 dividing every cols)
+ *   mode, nb             MUON_FULL (nb ignored), MUON_BLOCKWISE with nb
+ *                        column blocks (nb >= 1 dividing every cols), or
+ *                        MUON_DISTRIBUTED with nb tensor-parallel slices
  * The first step after registering params, changing the workspace, the mode
  * or nb builds the plan and uploads its tables (host work plus one copy);
  * later steps only queue kernels.  Returns once the work is queued. */

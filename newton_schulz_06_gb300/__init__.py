@@ -6,7 +6,7 @@ The compute lives in the C-ABI shared library libmuon.so (include/muon.h);
 this package only binds it.  Build with ``python -m
 newton_schulz_06_gb300.build``.
 """
-from ._lib import (MUON_BF16, MUON_BLOCKWISE, MUON_F32, MUON_FULL,  # noqa
-                   MuonError)
+from ._lib import (MUON_BF16, MUON_BLOCKWISE, MUON_DISTRIBUTED,  # noqa
+                   MUON_F32, MUON_FULL, MuonError)
 from .flops import gemm_equiv_flops, useful_flops  # noqa: F401
-from .muon import DEFAULT_COEFFS, HostPlanner, Muon  # noqa: F401
+from .muon import DEFAULT_COEFFS, HostPlanner, Muon, mode_code  # noqa: F401

@@ -23,6 +23,7 @@ MUON_F32 = 0
 MUON_BF16 = 1
 MUON_FULL = 0
 MUON_BLOCKWISE = 1
+MUON_DISTRIBUTED = 2
 MUON_HOST_ONLY = -1
 MUON_N_STAGES = 7
 STAGE_NAMES = ("momentum", "norm", "normalise", "syrk1", "syrk2", "gemm",

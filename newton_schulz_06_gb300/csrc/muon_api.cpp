@@ -47,6 +47,7 @@ struct UnitDesc {
     bool transposed = false;
     float scale = 1.f;
     size_t x_bytes = 0, mm_bytes = 0, buf_bytes = 0;
+    int shards = 1;             // distributed mode: slices of the long side
     int64_t ew_tiles = 0;
     size_t need = 0;   // scratch bytes of this unit inside a group
 };
@@ -62,6 +63,7 @@ struct GroupDesc {
     size_t o_sx_off = 0, o_sa_off = 0, o_g_off = 0;
     int p_sx = 0, p_sa = 0, p_g = 0;
     int64_t ew_tiles = 0;
+    int shards = 1;                          // distributed mode: P
 };
 
 struct Plan {
@@ -177,10 +179,14 @@ void unit_tiles(const UnitDesc& u, bool pair, int64_t* syrk, int64_t* gemm,
 
 int build_units(muon_ctx* h, int mode, int nb, std::vector<UnitDesc>* out) {
     out->clear();
-    if (mode != MUON_FULL && mode != MUON_BLOCKWISE)
-        return fail(h, MUON_ERR_INVALID_ARG, "mode must be MUON_FULL or MUON_BLOCKWISE");
+    if (mode != MUON_FULL && mode != MUON_BLOCKWISE && mode != MUON_DISTRIBUTED)
+        return fail(h, MUON_ERR_INVALID_ARG,
+                    "mode must be MUON_FULL, MUON_BLOCKWISE or MUON_DISTRIBUTED");
     const int nblk = (mode == MUON_BLOCKWISE) ? nb : 1;
-    if (nblk < 1) return fail(h, MUON_ERR_INVALID_ARG, "nb must be >= 1");
+    const int shards = (mode == MUON_DISTRIBUTED) ? nb : 1;
+    if (nblk < 1 || shards < 1) return fail(h, MUON_ERR_INVALID_ARG, "nb must be >= 1");
+    if (shards > 1 && !h->pair)
+        return fail(h, MUON_ERR_UNSUPPORTED, "distributed mode needs the CTA-pair kernels");
     for (size_t i = 0; i < h->params.size(); ++i) {
         const muon_param& p = h->params[i];
         if (p.cols % nblk != 0)
@@ -208,6 +214,12 @@ int build_units(muon_ctx* h, int mode, int nb, std::vector<UnitDesc>* out) {
                 std::sqrt(std::max(1.0, double(p.rows) / double(bc))));
             u.x_bytes = align_up(size_t(u.m) * u.ld_x * 2, 1024);
             u.mm_bytes = align_up(size_t(u.m) * u.ld_mm * 2, 1024);
+            u.shards = shards;
+            if (shards > 1 && (u.n % shards != 0 || (u.n / shards) % BK != 0))
+                return fail(h, MUON_ERR_UNSUPPORTED,
+                            std::to_string(shards) + " slices of n=" + std::to_string(u.n) +
+                                " (parameter " + std::to_string(i) +
+                                ") are not equal multiples of 64");
             u.buf_bytes = 2 * u.x_bytes + 2 * u.mm_bytes;
             u.ew_tiles = ceil_div(u.m, EW_TILE) * ceil_div(u.n, EW_TILE);
             u.need = u.buf_bytes + size_t(u.ew_tiles) * 4 * EW_PARTIALS_PER_TILE + 4;
@@ -393,6 +405,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         off = align_up(off, 256);
         g.ns_off = off;
         off += sizeof(NsUnit) * nu;
+        g.shards = P.units[g.u0].shards;
         std::vector<TileItem> tsx, tsa, tg;
         int64_t tile_base = 0;
         for (int i = g.u0; i < g.u1; ++i) {
@@ -483,7 +496,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
                 const int64_t T2 = ceil_div(u.m, 256);
                 for (int64_t ti = 0; ti < T2; ++ti)
                     for (int64_t tj = ti; tj < T2; ++tj) {
-                        TileItem t;
+                        TileItem t{};
                         t.unit = li;
                         t.ti = static_cast<int16_t>(ti);
                         t.tj = static_cast<int16_t>(tj);
@@ -496,7 +509,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
                     }
                 for (int64_t ti = 0; ti < T2; ++ti)
                     for (int64_t tj = 0; tj < ceil_div(u.n, 256); ++tj) {
-                        TileItem t;
+                        TileItem t{};
                         t.unit = li;
                         t.ti = static_cast<int16_t>(ti);
                         t.tj = static_cast<int16_t>(tj);
@@ -513,7 +526,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
                         const bool lneed = bl < T && bl >= ti;
                         const bool rneed = br < T && br >= ti;
                         if (!lneed && !rneed) continue;
-                        TileItem t;
+                        TileItem t{};
                         t.unit = li;
                         t.ti = static_cast<int16_t>(ti);
                         t.tj = static_cast<int16_t>(tj);
@@ -526,7 +539,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
                     }
                 for (int64_t ti = 0; ti < T; ++ti)
                     for (int64_t tj = 0; tj < ceil_div(u.n, BN); ++tj) {
-                        TileItem t;
+                        TileItem t{};
                         t.unit = li;
                         t.ti = static_cast<int16_t>(ti);
                         t.tj = static_cast<int16_t>(tj);
@@ -584,7 +597,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
                                     cudaMemcpyHostToDevice, h->stream);
     if (e != cudaSuccess) return cuda_fail(h, e, "metadata upload");
     P.mode = mode;
-    P.nb = (mode == MUON_BLOCKWISE) ? nb : 1;
+    P.nb = (mode == MUON_FULL) ? 1 : nb;
     P.ws = h->ws;
     P.ws_bytes = h->ws_bytes;
     P.valid = true;
@@ -740,11 +753,12 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
     if (!std::isfinite(lr) || !std::isfinite(beta) || !std::isfinite(a) ||
         !std::isfinite(b) || !std::isfinite(c))
         return fail(h, MUON_ERR_INVALID_ARG, "non-finite hyper-parameter");
-    if (mode != MUON_FULL && mode != MUON_BLOCKWISE)
-        return fail(h, MUON_ERR_INVALID_ARG, "mode must be MUON_FULL or MUON_BLOCKWISE");
-    if (mode == MUON_BLOCKWISE && nb < 1) return fail(h, MUON_ERR_INVALID_ARG, "nb must be >= 1");
+    if (mode != MUON_FULL && mode != MUON_BLOCKWISE && mode != MUON_DISTRIBUTED)
+        return fail(h, MUON_ERR_INVALID_ARG,
+                    "mode must be MUON_FULL, MUON_BLOCKWISE or MUON_DISTRIBUTED");
+    if (mode != MUON_FULL && nb < 1) return fail(h, MUON_ERR_INVALID_ARG, "nb must be >= 1");
     DeviceGuard guard(h->device);
-    const int want_nb = (mode == MUON_BLOCKWISE) ? nb : 1;
+    const int want_nb = (mode == MUON_FULL) ? 1 : nb;
     Plan& P = h->plan;
     if (!P.valid || P.mode != mode || P.nb != want_nb || P.ws != h->ws ||
         P.ws_bytes != h->ws_bytes) {
@@ -835,6 +849,7 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
                 L.tiles = reinterpret_cast<const TileItem*>(ws + q.off);
                 L.num_tiles = q.n;
                 L.pair_off = h->pair ? reinterpret_cast<const int32_t*>(ws + q.oo) : nullptr;
+                L.shards = g.shards;
                 if (!begin(q.st)) return fail(h, MUON_ERR_CUDA, "event create");
                 if (h->pair && q.op == OP_GEMM_BX && L.last && upd_tma)
                     e = launch_ns_pair_update(L, q.np, h->stream);
@@ -843,7 +858,10 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
                 else
                     e = launch_ns(q.op, L, std::min(q.n, h->num_sms), h->stream);
                 end();
-                if (e != cudaSuccess) return cuda_fail(h, e, "tensor-core stage launch");
+                if (e != cudaSuccess) {
+                    P.valid = false;          // rebuilt (and re-uploaded) next step
+                    return cuda_fail(h, e, "tensor-core stage launch");
+                }
             }
             cur ^= 1;
         }
@@ -874,6 +892,7 @@ int muon_sync(muon_handle h) {
         if (word != 0) {
             const int zero = 0;
             cudaMemcpy(h->ws, &zero, sizeof(int), cudaMemcpyHostToDevice);
+            h->plan.valid = false;    // the next step rebuilds and re-uploads it
             if (word == DEV_ERR_TIMEOUT)
                 return fail(h, MUON_ERR_TIMEOUT, "a bounded wait on the GPU ran out");
             return fail(h, MUON_ERR_CUDA, "device error word " + std::to_string(word));

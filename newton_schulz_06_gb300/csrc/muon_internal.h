@@ -104,6 +104,12 @@ struct NsLaunch {
     // (a cost-balanced schedule built by the planner); nullptr = pair p takes
     // tiles p, p + pairs, ...
     const int32_t* pair_off;
+    // Distributed mode, first product (CTA-pair kernels): the K range of
+    // every tile is `shards` equal slices.  The pair runs them in turn, slice
+    // 0 into accumulator 0 and each later slice into accumulator 1, which
+    // the epilogue adds into accumulator 0 (slices 1 .. P-2) or to it (slice
+    // P-1, for the output): ((p_0 + p_1) + ...) + p_{P-1}, a fixed order.
+    int32_t shards;
 };
 
 struct EwLaunch {

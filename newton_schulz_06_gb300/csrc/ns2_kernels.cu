@@ -428,9 +428,11 @@ __device__ __forceinline__ TileRange tile_range(const NsLaunch& p, int pair, int
     return r;
 }
 
-template <int OP, int P_STAGES, int FW>
+// SL: distributed mode's first product (K in p.shards slices, OP_SYRK_X).
+template <int OP, int P_STAGES, int FW, int SL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     ns2_kernel(const __grid_constant__ NsLaunch p) {
+    static_assert(!SL || (OP == OP_SYRK_X && !FW), "slices: first product only");
     constexpr int P_EPI_OFF = p_epi_off<P_STAGES>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -513,7 +515,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 const int b0 = t.tj * 256 + t.n_off + static_cast<int>(rank) * hb;
                 const uint32_t tx_bytes = 2u * (P_A_BYTES + hb * BK * 2);
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag,
+                    if (!mbar_try_wait(smem_u32(&empty_bar[stage]), phase ^ 1) &&
+                        !wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag,
                                       p.err, limit)) {
                         ok = false;
                         break;
@@ -553,44 +556,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             int local = 0;
             bool ok = true;
             bool any = false;
+            // distributed mode's first product: slices of K in turn, slice 0
+            // into accumulator 0, later slices into accumulator 1 (u0, u1:
+            // uses of each so far)
+            constexpr bool sliced = SL != 0;
+            uint32_t u0 = 0, u1 = 0;
+            const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024);
+            const uint64_t b_desc0 = (OP == OP_GEMM_BX) ? smem_desc(smem_u32(sB), P_BOX, 1024)
+                                                        : smem_desc(smem_u32(sB), 16, 1024);
             const TileRange tr = tile_range(p, pair, npairs);
             for (int it = tr.begin; ok && it < tr.end; it += tr.step, ++local) {
                 const TileItem t = p.tiles[it];
                 const uint32_t idesc = instr_desc(256, t.n_len, OP == OP_GEMM_BX ? 1 : 0);
                 const NsUnit* U = p.units + t.unit;
                 const int kblocks = (k_extent<OP>(*U) + BK - 1) / BK;
-                const int acc = local & 1;
-                const uint32_t acc_phase = (local >> 1) & 1;
+                const int kslice = sliced ? kblocks / p.shards : kblocks;
+                const int acc = sliced ? 0 : (local & 1);
+                const uint32_t acc_phase = sliced ? (u0++ & 1) : ((local >> 1) & 1);
                 if (!wait_bounded(smem_u32(&tempty_bar[acc]), acc_phase ^ 1, abort_flag,
                                   p.err, limit)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * 256 + t.n_off;
+                uint32_t d_tmem = tmem_base + acc * 256 + t.n_off;
+                int kin = 0;                              // step within the slice
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag, p.err,
+                    if (sliced && kin == 0 && kb > 0) {
+                        // a new slice into accumulator 1, once the epilogue
+                        // has taken the previous one out
+                        if (!wait_bounded(smem_u32(&tempty_bar[1]), (u1++ & 1) ^ 1, abort_flag,
+                                          p.err, limit)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        d_tmem = tmem_base + 256 + t.n_off;
+                    }
+                    // this thread issues every MMA of the pair: the common
+                    // case (stage already full) stays inline, descriptors
+                    // are the stage-0 ones plus offsets (start address in
+                    // 16-byte units; shared memory stays below 256 KB, so
+                    // the 14-bit field never carries)
+                    if (!mbar_try_wait(smem_u32(&full_bar[stage]), phase) &&
+                        !wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag, p.err,
                                       limit)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(sA + stage * P_A_BYTES);
-                    const uint32_t b_base = smem_u32(sB + stage * P_B_BYTES);
+                    const uint64_t ad0 = a_desc0 + static_cast<uint64_t>(stage) * (P_A_BYTES >> 4);
+                    const uint64_t bd0 = b_desc0 + static_cast<uint64_t>(stage) * (P_B_BYTES >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = smem_desc(a_base + kk * 32, 16, 1024);
+                        const uint64_t ad = ad0 + static_cast<uint64_t>(kk * 2);
                         const uint64_t bd =
-                            (OP == OP_GEMM_BX) ? smem_desc(b_base + kk * 2048, P_BOX, 1024)
-                                               : smem_desc(b_base + kk * 32, 16, 1024);
-                        mma_pair(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                            bd0 + static_cast<uint64_t>(kk * ((OP == OP_GEMM_BX) ? 2048 : 32) >> 4);
+                        mma_pair(d_tmem, ad, bd, idesc,
+                             ((sliced ? kin : kb) > 0 || kk > 0) ? 1u : 0u);
                     }
                     any = true;
                     commit_pair_multicast(smem_u32(&empty_bar[stage]));
                     if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
+                    // a finished later slice is handed to the epilogue
+                    if (sliced && kb >= kslice && kin == kslice - 1)
+                        commit_pair_multicast(smem_u32(&tfull_bar[1]));
+                    if (sliced && ++kin == kslice) kin = 0;
                 }
                 if (!ok) break;
-                commit_pair_multicast(smem_u32(&tfull_bar[acc]));
+                if (!sliced) commit_pair_multicast(smem_u32(&tfull_bar[acc]));
             }
             if (!ok && any) {
                 commit_pair_local(smem_u32(drain_bar));
@@ -615,6 +649,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         uint32_t in_seq = 0;     // input loads issued by this warp
         uint32_t in_use = 0;     // input loads consumed
         uint32_t st_seq = 0;     // staging blocks used
+        constexpr bool sliced = SL != 0;
+        uint32_t f1 = 0;         // sliced: slices taken from accumulator 1
         uint32_t tempty_leader[2];
         tempty_leader[0] = map_to_rank(smem_u32(&tempty_bar[0]), 0);
         tempty_leader[1] = map_to_rank(smem_u32(&tempty_bar[1]), 0);
@@ -657,17 +693,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             };
             if (uses_in)
                 for (int k = 0; k < n_need && k < P_IN_SLOTS; ++k) issue(k);
-            ok = wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.err, limit);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) +
-                                   acc * 256 + half * 128;
+            // this warp's TMEM lanes and columns; sliced tiles keep the sum
+            // in accumulator 0 and the newest slice in accumulator 1
+            const uint32_t tlane = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + half * 128;
+            if (sliced) {
+                for (int sl = 1; ok && sl < p.shards; ++sl) {
+                    ok = wait_bounded(smem_u32(&tfull_bar[1]), f1++ & 1u, abort_flag, p.err,
+                                      limit);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc_fence_after();
+                    if (sl == p.shards - 1) break;       // the last slice: output below
+#pragma unroll 1
+                    for (int k = 0; k < n_need; ++k) {
+                        const int c = order[k];
+                        float s0[32], s1[32];
+                        tmem_ld32(tlane + 32 * c, s0);
+                        tmem_ld32(tlane + 256 + 32 * c, s1);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) s0[e] = s0[e] + s1[e];
+                        tmem_st32(tlane + 32 * c, s0);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader[1]);
+                }
+                if (!ok) break;
+            } else {
+                ok = wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.err, limit);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+            }
+            const uint32_t tbase = tlane + (sliced ? 0 : acc * 256);
 #pragma unroll 1
             for (int k = 0; k < n_need; ++k) {
                 const int c = order[k];
                 const int gc0 = col0 + 32 * c;
                 float v[32];
                 tmem_ld32(tbase + 32 * c, v);
+                if (sliced) {
+                    // ((p_0 + p_1) + ...) + p_{P-1}
+                    float last[32];
+                    tmem_ld32(tbase + 256 + 32 * c, last);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = v[e] + last[e];
+                }
                 if (uses_in) {
                     const uint32_t sl = in_use & 1u;
                     const uint8_t* slot = s_in + sl * p_in_blk<FW>();
@@ -728,7 +797,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader[acc]);
+            if (lane == 0) {
+                if (sliced) {
+                    mbar_arrive_cluster_relaxed(tempty_leader[0]);
+                    mbar_arrive_cluster_relaxed(tempty_leader[1]);
+                } else {
+                    mbar_arrive_cluster_relaxed(tempty_leader[acc]);
+                }
+            }
         }
         // after an abort: let input loads in flight land before leaving
         for (uint32_t q = in_use; q != in_seq; ++q)
@@ -746,24 +822,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     }
 }
 
-template <int OP, int ST, int FW>
+template <int OP, int ST, int FW, int SL = 0>
 cudaError_t launch_pair_st(const NsLaunch& p, int pairs, cudaStream_t s) {
     static int attr_done[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(ns2_kernel<OP, ST, FW>,
+        cudaError_t e = cudaFuncSetAttribute(ns2_kernel<OP, ST, FW, SL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              p_smem<ST, FW>());
         if (e != cudaSuccess) return e;
         attr_done[dev] = 1;
     }
-    return launch_kernel(ns2_kernel<OP, ST, FW>, dim3(2 * pairs), dim3(P_THREADS),
+    return launch_kernel(ns2_kernel<OP, ST, FW, SL>, dim3(2 * pairs), dim3(P_THREADS),
                          p_smem<ST, FW>(), s, p);
 }
 
 template <int OP>
 cudaError_t launch_pair_op(const NsLaunch& p, int pairs, int stages, cudaStream_t s) {
+    if (OP == OP_SYRK_X && p.shards > 1) return launch_pair_st<OP_SYRK_X, 5, 0, 1>(p, pairs, s);
     switch (stages) {
         case 4: return launch_pair_st<OP, 4, 0>(p, pairs, s);
         default: return launch_pair_st<OP, 5, 0>(p, pairs, s);
@@ -777,7 +854,7 @@ int ns_pair_max_clusters() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (cached[dev]) return cached[dev];
-    cudaError_t e = cudaFuncSetAttribute(ns2_kernel<OP_GEMM_BX, P_STAGES_MAX, 0>,
+    cudaError_t e = cudaFuncSetAttribute(ns2_kernel<OP_GEMM_BX, P_STAGES_MAX, 0, 0>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          p_smem<P_STAGES_MAX, 0>());
     if (e != cudaSuccess) return 0;
@@ -788,7 +865,7 @@ int ns_pair_max_clusters() {
     cfg.blockDim = dim3(P_THREADS, 1, 1);
     cfg.dynamicSmemBytes = p_smem<P_STAGES_MAX, 0>();
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, ns2_kernel<OP_GEMM_BX, P_STAGES_MAX, 0>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, ns2_kernel<OP_GEMM_BX, P_STAGES_MAX, 0, 0>, &cfg);
     if (e != cudaSuccess || n <= 0) {
         cudaGetLastError();
         n = sms / 2;

@@ -92,12 +92,20 @@ def workload(name: str) -> Workload:
         return Workload(name, kimi_k2_layer_shapes(), torch.bfloat16,
                         torch.bfloat16, grad="normal", grad_std=1e-2,
                         mode="blockwise", nb=4)
+    if name == "square_4096_bf16_distributed4":
+        return Workload(name, [(4096, 4096)], torch.bfloat16, torch.bfloat16,
+                        grad="log_scale_step", mode="distributed", nb=4)
+    if name == "qwen3_30b_a3b_block_distributed4":
+        return Workload(name, qwen3_30b_a3b_block_shapes(), torch.bfloat16,
+                        torch.bfloat16, grad="log_sigma", mode="distributed",
+                        nb=4)
     raise KeyError(name)
 
 
 WORKLOADS = ["single_256x512_f32", "square_4096_bf16", "qwen3_30b_a3b_block",
              "qwen3_30b_a3b_48_layers", "kimi_k2_layer_full",
-             "kimi_k2_layer_blockwise4"]
+             "kimi_k2_layer_blockwise4", "square_4096_bf16_distributed4",
+             "qwen3_30b_a3b_block_distributed4"]
 
 
 def seed_for(*parts) -> int:

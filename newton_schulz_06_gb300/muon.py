@@ -42,6 +42,12 @@ def _param(W: torch.Tensor, G: torch.Tensor, M: torch.Tensor) -> _lib.MuonParam:
     return p
 
 
+
+def mode_code(name: str) -> int:
+    """The C ABI's mode constant for "full", "blockwise" or "distributed"."""
+    return {"full": _lib.MUON_FULL, "blockwise": _lib.MUON_BLOCKWISE,
+            "distributed": _lib.MUON_DISTRIBUTED}[name]
+
 class Muon:
     """One libmuon handle over a fixed list of (W, G, M) device tensors."""
 

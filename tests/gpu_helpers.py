@@ -23,7 +23,7 @@ import numpy as np
 import torch
 
 import oracle
-from newton_schulz_06_gb300 import MUON_BLOCKWISE, MUON_FULL, Muon
+from newton_schulz_06_gb300 import Muon, mode_code
 
 COEFFS = tuple(float(np.float32(x)) for x in (3.4445, -4.7750, 2.0315))
 O_TOL = 3e-2
@@ -52,7 +52,7 @@ def gpu_step(triples, *, lr=0.02, beta=0.95, nesterov=True, ns_steps=5,
     (host copies of the inputs, fp32 W exports, bf16 O exports, opt)."""
     inputs = [(to_np(W), to_np(G), to_np(M)) for W, G, M in triples]
     opt = Muon(triples)
-    md = MUON_BLOCKWISE if mode == "blockwise" else MUON_FULL
+    md = mode_code(mode)
     opt.ensure_workspace(md, nb, max_workspace)
     wexp = oexp = None
     if exports:

@@ -156,3 +156,24 @@ def test_register_rejects_bad_params(L):
     assert lib.muon_step(h, 0.02, 0.95, 1, 5, 3.4445, -4.775, 2.0315, 0,
                          1) == L.MUON_ERR_STATE
     assert lib.muon_destroy(h) == 0
+
+
+def test_distributed_mode_plan_and_validation(L):
+    """Distributed mode keeps one unit per matrix, full mode's tiles and
+    full mode's workspace (the slices' sum stays in tensor memory); slices
+    must be equal multiples of 64 of every long side."""
+    shapes = [(4096, 4096), (768, 2048), (2048, 768)]
+    p = _planner(shapes)
+    full = p.plan_info(L.MUON_FULL, 1)
+    dist = p.plan_info(L.MUON_DISTRIBUTED, 4)
+    for k in ("units", "syrk_tiles", "gemm_tiles", "useful_flops", "executed_flops"):
+        assert dist[k] == full[k], k
+    assert p.workspace_size(L.MUON_DISTRIBUTED, 4) == p.workspace_size(L.MUON_FULL, 1)
+    assert p.plan_info(L.MUON_DISTRIBUTED, 1)["syrk_tiles"] == full["syrk_tiles"]
+    for bad in (3, 64):      # 2048 / 3 is not whole; 2048 / 64 = 32 < 64
+        with pytest.raises(L.MuonError) as e:
+            p.plan_info(L.MUON_DISTRIBUTED, bad)
+        assert e.value.code == L.MUON_ERR_UNSUPPORTED
+    with pytest.raises(L.MuonError) as e:
+        p.plan_info(L.MUON_DISTRIBUTED, 0)
+    assert e.value.code == L.MUON_ERR_INVALID_ARG

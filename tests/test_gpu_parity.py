@@ -177,3 +177,40 @@ def test_update_folded_into_gemm_matches_separate_pass_bitexact(monkeypatch):
     for i in range(len(shapes)):
         assert torch.equal(trips[i][0], clones[i][0]), shapes[i]
         assert torch.equal(w1[i], w2[i]) and torch.equal(o1[i], o2[i]), shapes[i]
+
+
+@pytest.mark.parametrize("rows,cols,P", [(256, 1024, 4), (1024, 512, 2),
+                                         (384, 1536, 8), (768, 2048, 4),
+                                         (200, 640, 2)])
+def test_distributed_mode_matches_oracle(rows, cols, P):
+    """Distributed mode (P slices of the long side; the partial first
+    products summed in slice order) against the oracle's distributed mode."""
+    trip = case(rows, cols, 600 + P)
+    inp, wexp, oexp, _ = gpu_step([trip], mode="distributed", nb=P)
+    ref = oracle_step(inp[0], mode="distributed", nb=P)
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref)
+
+
+def test_distributed_one_slice_is_full_mode_bitexact():
+    t1 = case(512, 1024, 610)
+    t2 = [t.clone() for t in t1]
+    _, w1, o1, _ = gpu_step([t1])
+    _, w2, o2, _ = gpu_step([t2], mode="distributed", nb=1)
+    assert torch.equal(o1[0], o2[0]) and torch.equal(t1[0], t2[0])
+
+
+def test_distributed_mode_reproducible_and_standalone_bitexact():
+    """The slice sum has a fixed order: repeated runs and a matrix stepped
+    alone or in a group give the same bits, over two steps (the slot
+    counters carry across launches and steps)."""
+    shapes = [(512, 2048), (2048, 512), (768, 1024)]
+    trips = [case(r, c, 620 + i) for i, (r, c) in enumerate(shapes)]
+    again = [[t.clone() for t in tr] for tr in trips]
+    alone = [t.clone() for t in trips[1]]
+    _, _, o1, _ = gpu_step(trips, mode="distributed", nb=4, steps=2)
+    _, _, o2, _ = gpu_step(again, mode="distributed", nb=4, steps=2)
+    _, _, o3, _ = gpu_step([alone], mode="distributed", nb=4, steps=2)
+    for i in range(len(shapes)):
+        assert torch.equal(o1[i], o2[i]), shapes[i]
+        assert torch.equal(trips[i][0], again[i][0]), shapes[i]
+    assert torch.equal(o1[1], o3[0]) and torch.equal(trips[1][0], alone[0])

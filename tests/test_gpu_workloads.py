@@ -19,7 +19,7 @@ import pytest
 import torch
 
 from gpu_helpers import check_against_oracle, oracle_step, to_np
-from newton_schulz_06_gb300 import MUON_BLOCKWISE, MUON_FULL, Muon
+from newton_schulz_06_gb300 import Muon, mode_code
 from newton_schulz_06_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -46,7 +46,7 @@ def run_workload(wl, sample, *, steps=1, exports_for=None, max_ws=None):
     Ws, Gs, Ms = I.make_state(wl, DEV)
     trips = list(zip(Ws, Gs, Ms))
     opt = Muon(trips)
-    md = MUON_BLOCKWISE if wl.mode == "blockwise" else MUON_FULL
+    md = mode_code(wl.mode)
     opt.ensure_workspace(md, wl.nb, max_ws)
     idx = range(len(trips)) if exports_for is None else exports_for
     wexp = [None] * len(trips)
@@ -89,7 +89,7 @@ def check_standalone(wl, trips_before, oexp, sample):
 
 def _alone(W, G, M, wl):
     opt = Muon([(W, G, M)])
-    md = MUON_BLOCKWISE if wl.mode == "blockwise" else MUON_FULL
+    md = mode_code(wl.mode)
     opt.ensure_workspace(md, wl.nb)
     o = torch.empty(W.shape, device=DEV, dtype=torch.bfloat16)
     opt.set_exports(None, [o])
@@ -103,6 +103,15 @@ def test_square_4096_three_steps_teacher_forced():
     trips, host, before, wexp, oexp, _ = run_workload(wl, [0], steps=3)
     errs = check_sample(wl, trips, host, wexp, oexp, [0])
     print("4096^2 step 3", errs)
+    check_standalone(wl, before, oexp, [0])
+
+
+def test_square_4096_distributed4_teacher_forced():
+    """Distributed mode over 4 slices at the benchmark's size, two steps."""
+    wl = I.workload("square_4096_bf16_distributed4")
+    trips, host, before, wexp, oexp, _ = run_workload(wl, [0], steps=2)
+    errs = check_sample(wl, trips, host, wexp, oexp, [0])
+    print("4096^2 distributed4 step 2", errs)
     check_standalone(wl, before, oexp, [0])
 
 
