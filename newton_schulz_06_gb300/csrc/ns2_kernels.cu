@@ -40,14 +40,16 @@ constexpr int P_TMEM_COLS = 512;
 constexpr int P_EPI_WARPS = 8;                     // 2 per TMEM lane group
 constexpr int P_THREADS = 64 + 32 * P_EPI_WARPS;
 constexpr int P_BLK = 32 * 32 * 2;                 // one 32x32 bf16 block
-// Per epilogue warp: two input slots (an X or A block, plus a W block when
-// the update is folded into the last GEMM), so inputs arrive two blocks
-// ahead, and two staging blocks, so a block is staged while the previous
-// one's TMA store still reads its own.
-constexpr int P_IN_SLOTS = 2;
+// Per epilogue warp: input slots (an X or A block, plus a W block when the
+// update is folded into the last GEMM) and two staging blocks, so a block is
+// staged while the previous one's TMA store still reads its own.  Inputs
+// arrive two blocks ahead; with the W blocks one ahead, which keeps five
+// pipeline stages in shared memory.
+constexpr int P_IN_SLOTS_MAX = 2;
+template <int FW> __host__ __device__ constexpr int p_in_slots() { return FW ? 1 : 2; }
 template <int FW> __host__ __device__ constexpr int p_in_blk() { return FW ? 2 * P_BLK : P_BLK; }
 template <int FW> __host__ __device__ constexpr int p_epi_warp_bytes() {
-    return P_IN_SLOTS * p_in_blk<FW>() + 2 * P_BLK;
+    return p_in_slots<FW>() * p_in_blk<FW>() + 2 * P_BLK;
 }
 template <int FW> __host__ __device__ constexpr int p_epi_bytes() {
     return P_EPI_WARPS * p_epi_warp_bytes<FW>();
@@ -445,10 +447,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     uint64_t* tfull_bar = bars + 2 * P_STAGES;
     uint64_t* tempty_bar = bars + 2 * P_STAGES + 2;
     uint64_t* drain_bar = bars + 2 * P_STAGES + 4;
-    uint64_t* in_bar = bars + 2 * P_STAGES + 5;    // P_IN_SLOTS per epilogue warp
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_bar + P_IN_SLOTS * P_EPI_WARPS);
+    constexpr int NS = p_in_slots<FW>();
+    uint64_t* in_bar = bars + 2 * P_STAGES + 5;    // NS per epilogue warp
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_bar + P_IN_SLOTS_MAX * P_EPI_WARPS);
     static_assert(p_smem<P_STAGES, FW>() <= 232448, "shared memory per CTA");
-    static_assert((2 * P_STAGES + 5 + P_IN_SLOTS * P_EPI_WARPS) * 8 + 8 <= 1024,
+    static_assert((2 * P_STAGES + 5 + P_IN_SLOTS_MAX * P_EPI_WARPS) * 8 + 8 <= 1024,
                   "barrier area");
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -468,7 +471,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             mbar_init(smem_u32(&tempty_bar[a]), 2 * P_EPI_WARPS);
         }
         mbar_init(smem_u32(drain_bar), 1);
-        for (int w = 0; w < P_IN_SLOTS * P_EPI_WARPS; ++w) mbar_init(smem_u32(&in_bar[w]), 1);
+        for (int w = 0; w < NS * P_EPI_WARPS; ++w) mbar_init(smem_u32(&in_bar[w]), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -644,8 +647,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         const int lg = warp & 3;
         const int half = ew >> 2;
         uint8_t* epi = smem + P_EPI_OFF + ew * p_epi_warp_bytes<FW>();
-        uint8_t* s_in = epi;                                   // P_IN_SLOTS slots
-        uint8_t* s_st = epi + P_IN_SLOTS * p_in_blk<FW>();     // two staging blocks
+        uint8_t* s_in = epi;                                   // NS slots
+        uint8_t* s_st = epi + NS * p_in_blk<FW>();             // two staging blocks
         uint32_t in_seq = 0;     // input loads issued by this warp
         uint32_t in_use = 0;     // input loads consumed
         uint32_t st_seq = 0;     // staging blocks used
@@ -684,15 +687,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             }
             const bool uses_in = (OP != OP_SYRK_X);
             auto issue = [&](int k) {       // input of the k-th needed block
-                const uint32_t sl = in_seq & 1u;
+                const uint32_t sl = in_seq % NS;
                 if (lane == 0)
                     issue_inputs<FW>(u, s_in + sl * p_in_blk<FW>(),
-                                     smem_u32(&in_bar[P_IN_SLOTS * ew + sl]),
+                                     smem_u32(&in_bar[NS * ew + sl]),
                                      col0 + 32 * order[k], r0w);
                 ++in_seq;
             };
             if (uses_in)
-                for (int k = 0; k < n_need && k < P_IN_SLOTS; ++k) issue(k);
+                for (int k = 0; k < n_need && k < NS; ++k) issue(k);
             // this warp's TMEM lanes and columns; sliced tiles keep the sum
             // in accumulator 0 and the newest slice in accumulator 1
             const uint32_t tlane = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + half * 128;
@@ -738,10 +741,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                     for (int e = 0; e < 32; ++e) v[e] = v[e] + last[e];
                 }
                 if (uses_in) {
-                    const uint32_t sl = in_use & 1u;
+                    const uint32_t sl = in_use % NS;
                     const uint8_t* slot = s_in + sl * p_in_blk<FW>();
-                    const bool got = wait_bounded(smem_u32(&in_bar[P_IN_SLOTS * ew + sl]),
-                                                  (in_use >> 1) & 1u, abort_flag, p.err, limit);
+                    const bool got = wait_bounded(smem_u32(&in_bar[NS * ew + sl]),
+                                                  (in_use / NS) & 1u, abort_flag, p.err, limit);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     ++in_use;
                     float x[32];
@@ -756,7 +759,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                                            next_stage(s_st, st_seq, lane));
                     }
                     __syncwarp();      // every lane's reads of the slot are done
-                    if (k + P_IN_SLOTS < n_need) issue(k + P_IN_SLOTS);
+                    if (k + NS < n_need) issue(k + NS);
                     if (FW) continue;
                 } else {
 #pragma unroll
@@ -808,7 +811,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         }
         // after an abort: let input loads in flight land before leaving
         for (uint32_t q = in_use; q != in_seq; ++q)
-            wait_quiet(smem_u32(&in_bar[P_IN_SLOTS * ew + (q & 1u)]), (q >> 1) & 1u, limit);
+            wait_quiet(smem_u32(&in_bar[NS * ew + q % NS]), (q / NS) & 1u, limit);
         if (lane == 0) bulk_wait_all0();
     }
 
@@ -884,10 +887,10 @@ cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, int stages,
     return cudaErrorInvalidValue;
 }
 
-// The last GEMM with the update folded in through TMA-loaded W blocks: four
-// pipeline stages leave room for the W blocks of both input slots.
+// The last GEMM with the update folded in through TMA-loaded W blocks (one
+// input slot of X and W blocks, five pipeline stages).
 cudaError_t launch_ns_pair_update(const NsLaunch& p, int pairs, cudaStream_t s) {
-    return launch_pair_st<OP_GEMM_BX, 4, 1>(p, pairs, s);
+    return launch_pair_st<OP_GEMM_BX, 5, 1>(p, pairs, s);
 }
 
 }  // namespace muon
