@@ -88,11 +88,6 @@ __device__ __forceinline__ void commit_pair_local(uint32_t bar) {
         : "memory");
 }
 
-template <int OP>
-__device__ __forceinline__ int k_extent(const NsUnit& U) {
-    return OP == OP_SYRK_X ? U.n : U.m;
-}
-
 // Tile-constant fields of a unit, copied into registers once per tile (the
 // kernels store through pointers the compiler cannot tell apart from the
 // tables, so fields read from the tables would be reloaded after every
@@ -503,15 +498,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             for (int s = 0; s < P_STAGES; ++s) issued[s] = 0;
             bool ok = true;
             const TileRange tr = tile_range(p, pair, npairs);
+            // the next tile's record is fetched while this tile streams
+            TileItem t_next = tr.begin < tr.end ? p.tiles[tr.begin] : TileItem{};
             for (int it = tr.begin; ok && it < tr.end; it += tr.step) {
-                const TileItem t = p.tiles[it];
+                const TileItem t = t_next;
+                if (it + tr.step < tr.end) t_next = p.tiles[it + tr.step];
                 const NsUnit* U = p.units + t.unit;
                 const void* tmA;
                 const void* tmB;
                 if (OP == OP_SYRK_X) { tmA = &U->tm_x[p.src]; tmB = tmA; }
                 else if (OP == OP_SYRK_A) { tmA = &U->tm_a; tmB = tmA; }
                 else { tmA = &U->tm_b; tmB = &U->tm_x[p.src]; }
-                const int kblocks = (k_extent<OP>(*U) + BK - 1) / BK;
+                const int kblocks = t.k_blocks;
                 const int r0 = t.ti * 256 + static_cast<int>(rank) * P_HALF;
                 // N = n_len columns split evenly over the pair (64 or 128 each)
                 const int hb = t.n_len >> 1;
@@ -568,11 +566,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             const uint64_t b_desc0 = (OP == OP_GEMM_BX) ? smem_desc(smem_u32(sB), P_BOX, 1024)
                                                         : smem_desc(smem_u32(sB), 16, 1024);
             const TileRange tr = tile_range(p, pair, npairs);
+            TileItem t_next = tr.begin < tr.end ? p.tiles[tr.begin] : TileItem{};
             for (int it = tr.begin; ok && it < tr.end; it += tr.step, ++local) {
-                const TileItem t = p.tiles[it];
+                const TileItem t = t_next;
+                if (it + tr.step < tr.end) t_next = p.tiles[it + tr.step];
                 const uint32_t idesc = instr_desc(256, t.n_len, OP == OP_GEMM_BX ? 1 : 0);
-                const NsUnit* U = p.units + t.unit;
-                const int kblocks = (k_extent<OP>(*U) + BK - 1) / BK;
+                const int kblocks = t.k_blocks;
                 const int kslice = sliced ? kblocks / p.shards : kblocks;
                 const int acc = sliced ? 0 : (local & 1);
                 const uint32_t acc_phase = sliced ? (u0++ & 1) : ((local >> 1) & 1);
@@ -660,8 +659,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         int local = 0;
         bool ok = true;
         const TileRange tr = tile_range(p, pair, npairs);
+        TileItem t_next = tr.begin < tr.end ? p.tiles[tr.begin] : TileItem{};
         for (int it = tr.begin; ok && it < tr.end; it += tr.step, ++local) {
-            const TileItem t = p.tiles[it];
+            const TileItem t = t_next;
+            if (it + tr.step < tr.end) t_next = p.tiles[it + tr.step];
             const EpiUnit u = load_epi_unit<OP>(p, t.unit);
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
