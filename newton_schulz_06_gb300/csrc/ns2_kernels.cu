@@ -46,18 +46,18 @@ constexpr int P_BLK = 32 * 32 * 2;                 // one 32x32 bf16 block
 // arrive two blocks ahead; with the W blocks one ahead, which keeps five
 // pipeline stages in shared memory.
 constexpr int P_IN_SLOTS_MAX = 2;
-template <int FW> __host__ __device__ constexpr int p_in_slots() { return FW ? 1 : 2; }
+template <int ST, int FW> __host__ __device__ constexpr int p_in_slots() { return FW ? 1 : 2; }
 template <int FW> __host__ __device__ constexpr int p_in_blk() { return FW ? 2 * P_BLK : P_BLK; }
-template <int FW> __host__ __device__ constexpr int p_epi_warp_bytes() {
-    return p_in_slots<FW>() * p_in_blk<FW>() + 2 * P_BLK;
+template <int ST, int FW> __host__ __device__ constexpr int p_epi_warp_bytes() {
+    return p_in_slots<ST, FW>() * p_in_blk<FW>() + 2 * P_BLK;
 }
-template <int FW> __host__ __device__ constexpr int p_epi_bytes() {
-    return P_EPI_WARPS * p_epi_warp_bytes<FW>();
+template <int ST, int FW> __host__ __device__ constexpr int p_epi_bytes() {
+    return P_EPI_WARPS * p_epi_warp_bytes<ST, FW>();
 }
 // Shared memory of a kernel with ST pipeline stages.
 template <int ST> __host__ __device__ constexpr int p_epi_off() { return ST * (P_A_BYTES + P_B_BYTES) + 1024; }
 template <int ST, int FW> __host__ __device__ constexpr int p_smem() {
-    return p_epi_off<ST>() + p_epi_bytes<FW>() + 1024;
+    return p_epi_off<ST>() + p_epi_bytes<ST, FW>() + 1024;
 }
 
 __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -347,19 +347,61 @@ __device__ __forceinline__ uint8_t* next_stage(uint8_t* st0, uint32_t& st_seq, i
     return st0 + (st_seq++ & 1u) * P_BLK;
 }
 
-// Lane 0: TMA loads of the epilogue input block at (x, y) into input slot
-// `slot` and, when the update is folded in (FW), of the matching W block (at
-// (x, y) in the weight's orientation, or (y, x) for a transposed unit),
-// both on the slot's barrier.
+// The 32 x 32 blocks one epilogue warp handles in one tile: which of its
+// four column blocks are needed, in order, where they are, and where their
+// input blocks come from.  Built for the next tile while the current one is
+// drained, so its first inputs can be requested early.
+struct InPlan {
+    const CUtensorMap* te_in;    // GEMM: X, SYRK-2: A
+    const CUtensorMap* te_w;     // folded update: W
+    int transposed;              // folded update: W is the iterate's transpose
+    int r0w, col0;               // first row, first column of the warp's part
+    int n;                       // needed blocks
+    uint32_t order;              // their column-block indices, 2 bits each
+    __device__ __forceinline__ int block(int k) const {
+        return static_cast<int>((order >> (2 * k)) & 3u);
+    }
+};
+
+template <int OP>
+__device__ __forceinline__ InPlan plan_blocks(const NsLaunch& p, const TileItem& t,
+                                              uint32_t rank, int lg, int half) {
+    const NsUnit* U = p.units + t.unit;
+    InPlan q;
+    q.te_in = (OP == OP_GEMM_BX) ? &U->te_x[p.src] : &U->te_a;
+    q.te_w = &U->te_w;
+    q.transposed = (OP == OP_GEMM_BX && p.last) ? p.ew[t.unit].transposed : 0;
+    q.r0w = t.ti * 256 + static_cast<int>(rank) * P_HALF + lg * 32;
+    q.col0 = t.tj * 256 + half * 128;
+    const int m = U->m;
+    const int lim_c = (OP == OP_GEMM_BX) ? U->n : m;
+    q.n = 0;
+    q.order = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int gc0 = q.col0 + 32 * c;
+        const int rel = half * 128 + 32 * c;          // column within the tile
+        bool nd = q.r0w < m && gc0 < lim_c && rel >= t.n_off && rel < t.n_off + t.n_len;
+        if (OP != OP_GEMM_BX) nd = nd && gc0 >= q.r0w;    // upper blocks only
+        if (nd) q.order |= static_cast<uint32_t>(c) << (2 * q.n++);
+    }
+    return q;
+}
+
+// Lane 0: TMA loads of the input block of needed block k of plan q into
+// input slot `slot` and, when the update is folded in (FW), of the matching
+// W block (at (x, y) in the weight's orientation, or (y, x) for a
+// transposed unit), both on the slot's barrier.
 template <int FW>
-__device__ __forceinline__ void issue_inputs(const EpiUnit& u, uint8_t* slot, uint32_t bar,
-                                             int x, int y) {
+__device__ __forceinline__ void issue_inputs(const InPlan& q, int k, uint8_t* slot,
+                                             uint32_t bar) {
+    const int x = q.col0 + 32 * q.block(k), y = q.r0w;
     fence_proxy_async_smem();
     mbar_expect_tx(bar, p_in_blk<FW>());
-    tma_load_2d(smem_u32(slot), u.te_in, bar, x, y);
+    tma_load_2d(smem_u32(slot), q.te_in, bar, x, y);
     if (FW) {
-        if (u.transposed) tma_load_2d(smem_u32(slot + P_BLK), u.te_w, bar, y, x);
-        else tma_load_2d(smem_u32(slot + P_BLK), u.te_w, bar, x, y);
+        if (q.transposed) tma_load_2d(smem_u32(slot + P_BLK), q.te_w, bar, y, x);
+        else tma_load_2d(smem_u32(slot + P_BLK), q.te_w, bar, x, y);
     }
 }
 
@@ -442,7 +484,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     uint64_t* tfull_bar = bars + 2 * P_STAGES;
     uint64_t* tempty_bar = bars + 2 * P_STAGES + 2;
     uint64_t* drain_bar = bars + 2 * P_STAGES + 4;
-    constexpr int NS = p_in_slots<FW>();
+    constexpr int NS = p_in_slots<P_STAGES, FW>();
     uint64_t* in_bar = bars + 2 * P_STAGES + 5;    // NS per epilogue warp
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_bar + P_IN_SLOTS_MAX * P_EPI_WARPS);
     static_assert(p_smem<P_STAGES, FW>() <= 232448, "shared memory per CTA");
@@ -645,7 +687,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         const int ew = warp - 2;
         const int lg = warp & 3;
         const int half = ew >> 2;
-        uint8_t* epi = smem + P_EPI_OFF + ew * p_epi_warp_bytes<FW>();
+        uint8_t* epi = smem + P_EPI_OFF + ew * p_epi_warp_bytes<P_STAGES, FW>();
         uint8_t* s_in = epi;                                   // NS slots
         uint8_t* s_st = epi + NS * p_in_blk<FW>();             // two staging blocks
         uint32_t in_seq = 0;     // input loads issued by this warp
@@ -658,45 +700,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         tempty_leader[1] = map_to_rank(smem_u32(&tempty_bar[1]), 0);
         int local = 0;
         bool ok = true;
+        const bool uses_in = (OP != OP_SYRK_X);
         const TileRange tr = tile_range(p, pair, npairs);
         TileItem t_next = tr.begin < tr.end ? p.tiles[tr.begin] : TileItem{};
+        // input blocks stream through the slots in tile order, across tile
+        // boundaries: cur is this tile's plan, nxt the next tile's
+        InPlan cur{}, nxt{};
+        if (tr.begin < tr.end) cur = plan_blocks<OP>(p, t_next, rank, lg, half);
+        int cur_issued = 0, nxt_issued = 0;
+        auto issue_from = [&](const InPlan& q, int k) {
+            const uint32_t sl = in_seq % NS;
+            if (lane == 0)
+                issue_inputs<FW>(q, k, s_in + sl * p_in_blk<FW>(), smem_u32(&in_bar[NS * ew + sl]));
+            ++in_seq;
+        };
         for (int it = tr.begin; ok && it < tr.end; it += tr.step, ++local) {
             const TileItem t = t_next;
-            if (it + tr.step < tr.end) t_next = p.tiles[it + tr.step];
+            const bool has_next = it + tr.step < tr.end;
+            if (has_next) t_next = p.tiles[it + tr.step];
+            if (uses_in)
+                while (cur_issued < cur.n && in_seq - in_use < static_cast<uint32_t>(NS))
+                    issue_from(cur, cur_issued++);
+            nxt.n = 0;
+            nxt_issued = 0;
+            if (has_next) nxt = plan_blocks<OP>(p, t_next, rank, lg, half);
             const EpiUnit u = load_epi_unit<OP>(p, t.unit);
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
-            const int r0w = t.ti * 256 + static_cast<int>(rank) * P_HALF + lg * 32;
-            const int col0 = t.tj * 256 + half * 128;
-            const int lim_c = (OP == OP_GEMM_BX) ? u.n : u.m;
+            const int r0w = cur.r0w;
+            const int col0 = cur.col0;
             float scale = 1.f;
             if (p.first && OP != OP_SYRK_A) {
                 const float inv = p.inv_norm[t.unit];
                 scale = (OP == OP_SYRK_X) ? inv * inv : inv;
             }
-            // which of the 4 blocks this warp stores (warp-uniform), in order
-            int order[4];
-            int n_need = 0;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int gc0 = col0 + 32 * c;
-                const int rel = half * 128 + 32 * c;          // column within the tile
-                bool nd = r0w < u.m && gc0 < lim_c && rel >= t.n_off &&
-                          rel < t.n_off + t.n_len;
-                if (OP != OP_GEMM_BX) nd = nd && gc0 >= r0w;      // upper blocks only
-                if (nd) order[n_need++] = c;
-            }
-            const bool uses_in = (OP != OP_SYRK_X);
-            auto issue = [&](int k) {       // input of the k-th needed block
-                const uint32_t sl = in_seq % NS;
-                if (lane == 0)
-                    issue_inputs<FW>(u, s_in + sl * p_in_blk<FW>(),
-                                     smem_u32(&in_bar[NS * ew + sl]),
-                                     col0 + 32 * order[k], r0w);
-                ++in_seq;
-            };
-            if (uses_in)
-                for (int k = 0; k < n_need && k < NS; ++k) issue(k);
+            // the blocks this warp stores (warp-uniform), in order
+            const int n_need = cur.n;
             // this warp's TMEM lanes and columns; sliced tiles keep the sum
             // in accumulator 0 and the newest slice in accumulator 1
             const uint32_t tlane = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + half * 128;
@@ -709,7 +748,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                     if (sl == p.shards - 1) break;       // the last slice: output below
 #pragma unroll 1
                     for (int k = 0; k < n_need; ++k) {
-                        const int c = order[k];
+                        const int c = cur.block(k);
                         float s0[32], s1[32];
                         tmem_ld32(tlane + 32 * c, s0);
                         tmem_ld32(tlane + 256 + 32 * c, s1);
@@ -730,7 +769,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             const uint32_t tbase = tlane + (sliced ? 0 : acc * 256);
 #pragma unroll 1
             for (int k = 0; k < n_need; ++k) {
-                const int c = order[k];
+                const int c = cur.block(k);
                 const int gc0 = col0 + 32 * c;
                 float v[32];
                 tmem_ld32(tbase + 32 * c, v);
@@ -760,7 +799,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                                            next_stage(s_st, st_seq, lane));
                     }
                     __syncwarp();      // every lane's reads of the slot are done
-                    if (k + NS < n_need) issue(k + NS);
+                    // refill the slot: this tile's next block, else the next
+                    // tile's first
+                    if (cur_issued < cur.n) issue_from(cur, cur_issued++);
+                    else if (nxt_issued < nxt.n) issue_from(nxt, nxt_issued++);
                     if (FW) continue;
                 } else {
 #pragma unroll
@@ -799,6 +841,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 }
             }
             if (!__all_sync(0xffffffffu, ok)) break;
+            cur = nxt;
+            cur_issued = nxt_issued;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
