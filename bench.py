@@ -319,8 +319,8 @@ def run_ours(args, wl, world, rank, local, pg):
             stage_tot[name] = (t + tms, c + n)
     opt.set_profiling(False)
 
-    # end to end through the public API with host buffers: H2D of the
-    # step's gradients from pinned memory, the step, D2H of the weights
+    # end to end through the C ABI with host buffers (muon_step_host): the
+    # step's gradients in from pinned memory, the step, the weights back out
     pinned_g = [torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
                 for G in Gs]
     for i, G in enumerate(Gs):
@@ -334,12 +334,8 @@ def run_ours(args, wl, world, rank, local, pg):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for G, P in zip(Gs, pinned_g):
-            G.copy_(P, non_blocking=True)
-        opt.step(**kw)
-        for W, P in zip(Ws, pinned_w):
-            P.copy_(W, non_blocking=True)
-        torch.cuda.synchronize()
+        opt.step_host(pinned_g, pinned_w, **kw)
+        opt.sync()
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
     e2e = statistics.mean(e2e_ms)
     e2e = max_over_ranks(pg, e2e)
@@ -394,7 +390,8 @@ def run_ours(args, wl, world, rank, local, pg):
         "clocks": clocks,
         "e2e": {"value": world * useful / (e2e / 1e3) / 1e12,
                 "unit": "TFLOP/s", "ms_per_step": e2e,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "muon_step_host: G from pinned host memory, the step, W back"},
         "gpu_launches": launches,
         "roofline": roofline,
     }

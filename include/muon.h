@@ -145,6 +145,21 @@ MUON_API int muon_set_workspace(muon_handle h, void* dptr, size_t bytes);
 MUON_API int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
               float a, float b, float c, int mode, int nb);
 
+/* The same step with the gradients taken from, and the updated weights
+ * returned to, host memory.  n must equal the number of registered
+ * parameters.  g_host[i] holds parameter i's gradient (rows x cols, row-major,
+ * leading dimension cols, element type g_dtype); it is copied into the
+ * registered device g before the step.  After the step the updated weight
+ * (element type w_dtype) is copied to w_host[i] (rows x cols, leading
+ * dimension cols); a NULL w_host[i] skips that copy.  Everything is queued on
+ * the handle's stream and the call returns once it is queued: host buffers
+ * must stay valid, and unchanged, until muon_sync returns, and should be
+ * pinned (page-locked) for the copies to run asynchronously.  The caller
+ * owns them.  Errors as muon_step; a failed copy is MUON_ERR_CUDA. */
+MUON_API int muon_step_host(muon_handle h, int n, const void* const* g_host,
+                            void* const* w_host, float lr, float beta, int nesterov,
+                            int ns_steps, float a, float b, float c, int mode, int nb);
+
 /* Waits for the handle's stream and reports any error raised on the GPU
  * (MUON_ERR_TIMEOUT when a bounded wait ran out, MUON_ERR_CUDA otherwise). */
 MUON_API int muon_sync(muon_handle h);

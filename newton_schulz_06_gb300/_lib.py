@@ -35,7 +35,7 @@ EXPORTS = ("muon_create", "muon_set_stream", "muon_register_params",
            "muon_sync", "muon_destroy", "muon_last_error",
            "muon_set_profiling", "muon_stage_times", "muon_last_launch_count",
            "muon_debug_set_exports", "muon_get_plan_info",
-           "muon_step_noalloc", "muon_debug_wait_timeout")
+           "muon_step_noalloc", "muon_debug_wait_timeout", "muon_step_host")
 
 
 class MuonParam(ctypes.Structure):
@@ -100,6 +100,8 @@ def lib() -> ctypes.CDLL:
         "muon_step_noalloc": [ctypes.POINTER(MuonParam), f32, f32, i32, i32,
                               f32, f32, f32, vp, ctypes.c_char_p, sz],
         "muon_debug_wait_timeout": [H, vp, i32],
+        "muon_step_host": [H, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), f32,
+                           f32, i32, i32, f32, f32, f32, i32, i32],
     }
     for name, args in sig.items():
         fn = getattr(L, name)

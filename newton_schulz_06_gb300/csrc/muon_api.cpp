@@ -879,6 +879,43 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
     return MUON_OK;
 }
 
+int muon_step_host(muon_handle h, int n, const void* const* g_host, void* const* w_host,
+                   float lr, float beta, int nesterov, int ns_steps, float a, float b, float c,
+                   int mode, int nb) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (h->device == MUON_HOST_ONLY) return fail(h, MUON_ERR_STATE, "host-only handle");
+    if (n != static_cast<int>(h->params.size()))
+        return fail(h, MUON_ERR_INVALID_ARG,
+                    "n=" + std::to_string(n) + " but " + std::to_string(h->params.size()) +
+                        " parameters are registered");
+    if (!g_host || !w_host) return fail(h, MUON_ERR_INVALID_ARG, "NULL host pointer array");
+    for (int i = 0; i < n; ++i)
+        if (!g_host[i])
+            return fail(h, MUON_ERR_INVALID_ARG, "g_host[" + std::to_string(i) + "] is NULL");
+    DeviceGuard guard(h->device);
+    for (int i = 0; i < n; ++i) {
+        const muon_param& p = h->params[i];
+        const size_t es = elem_size(p.g_dtype);
+        const cudaError_t e = cudaMemcpy2DAsync(
+            const_cast<void*>(p.g), size_t(p.ld_g) * es, g_host[i], size_t(p.cols) * es,
+            size_t(p.cols) * es, size_t(p.rows), cudaMemcpyHostToDevice, h->stream);
+        if (e != cudaSuccess) return cuda_fail(h, e, "gradient copy to the device");
+    }
+    const int rc = muon_step(h, lr, beta, nesterov, ns_steps, a, b, c, mode, nb);
+    if (rc) return rc;
+    for (int i = 0; i < n; ++i) {
+        if (!w_host[i]) continue;
+        const muon_param& p = h->params[i];
+        const size_t es = elem_size(p.w_dtype);
+        const cudaError_t e = cudaMemcpy2DAsync(w_host[i], size_t(p.cols) * es, p.w,
+                                                size_t(p.ld_w) * es, size_t(p.cols) * es,
+                                                size_t(p.rows), cudaMemcpyDeviceToHost,
+                                                h->stream);
+        if (e != cudaSuccess) return cuda_fail(h, e, "weight copy to the host");
+    }
+    return MUON_OK;
+}
+
 int muon_sync(muon_handle h) {
     if (!h) return MUON_ERR_INVALID_ARG;
     if (h->device == MUON_HOST_ONLY) return fail(h, MUON_ERR_STATE, "host-only handle");

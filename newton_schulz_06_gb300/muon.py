@@ -111,6 +111,24 @@ class Muon:
         check(lib().muon_step(self._h, lr, beta, int(bool(nesterov)),
                               ns_steps, a, b, c, mode, nb), self._h)
 
+    def step_host(self, g_host, w_host, lr: float = 0.02, beta: float = 0.95,
+                  nesterov: bool = True, ns_steps: int = 5, coeffs=DEFAULT_COEFFS,
+                  mode: int = _lib.MUON_FULL, nb: int = 1,
+                  max_workspace: Optional[int] = None):
+        """One step with gradients from, and weights back to, host memory
+        (contiguous CPU tensors, ideally pinned; w_host entries may be None).
+        The tensors must stay alive and unchanged until sync()."""
+        if self._ws is None:
+            self.ensure_workspace(mode, nb, max_workspace)
+        n = len(self._tensors)
+        if len(g_host) != n or len(w_host) != n:
+            raise ValueError(f"need {n} gradient and weight host tensors")
+        gp = (ctypes.c_void_p * n)(*[g.data_ptr() for g in g_host])
+        wp = (ctypes.c_void_p * n)(*[None if w is None else w.data_ptr() for w in w_host])
+        a, b, c = coeffs
+        check(lib().muon_step_host(self._h, n, gp, wp, lr, beta, int(bool(nesterov)),
+                                   ns_steps, a, b, c, mode, nb), self._h)
+
     def sync(self):
         check(lib().muon_sync(self._h), self._h)
 

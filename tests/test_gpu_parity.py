@@ -9,6 +9,7 @@ import torch
 
 from gpu_helpers import (check_against_oracle, gpu_step, oracle_step, relF,
                          to_np)
+from newton_schulz_06_gb300 import Muon
 from newton_schulz_06_gb300.inputs import random_case, workload, make_state
 
 pytestmark = pytest.mark.gpu
@@ -214,3 +215,26 @@ def test_distributed_mode_reproducible_and_standalone_bitexact():
         assert torch.equal(o1[i], o2[i]), shapes[i]
         assert torch.equal(trips[i][0], again[i][0]), shapes[i]
     assert torch.equal(o1[1], o3[0]) and torch.equal(trips[1][0], alone[0])
+
+
+def test_step_with_host_buffers_matches_device_step_bitexact():
+    """muon_step_host: gradients in from pinned host memory, weights back out,
+    gives the same bits as copying G in and W out around muon_step."""
+    shapes = [(256, 640), (640, 256), (300, 300)]
+    trips = [case(r, c, 700 + i) for i, (r, c) in enumerate(shapes)]
+    clones = [[t.clone() for t in tr] for tr in trips]
+    g_host = [torch.randn(r, c, generator=torch.Generator().manual_seed(710 + i)
+                          ).to(torch.bfloat16).pin_memory() for i, (r, c) in enumerate(shapes)]
+    w_host = [torch.empty(r, c, dtype=torch.bfloat16).pin_memory() for r, c in shapes]
+    opt = Muon(trips)
+    opt.step_host(g_host, w_host)
+    opt.sync()
+    ref = Muon(clones)
+    for (W, G, M), g in zip(clones, g_host):
+        G.copy_(g)
+    ref.step()
+    ref.sync()
+    torch.cuda.synchronize()
+    for i in range(len(shapes)):
+        assert torch.equal(w_host[i], clones[i][0].cpu()), shapes[i]
+        assert torch.equal(trips[i][0], clones[i][0]) and torch.equal(trips[i][2], clones[i][2])
