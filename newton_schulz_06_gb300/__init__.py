@@ -10,3 +10,4 @@ from ._lib import (MUON_BF16, MUON_BLOCKWISE, MUON_DISTRIBUTED,  # noqa
                    MUON_F32, MUON_FULL, MuonError)
 from .flops import gemm_equiv_flops, useful_flops  # noqa: F401
 from .muon import DEFAULT_COEFFS, HostPlanner, Muon, mode_code  # noqa: F401
+from .layerwise import LayerwiseMuon, lpt_partition  # noqa: F401

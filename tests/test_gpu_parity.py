@@ -238,3 +238,25 @@ def test_step_with_host_buffers_matches_device_step_bitexact():
     for i in range(len(shapes)):
         assert torch.equal(w_host[i], clones[i][0].cpu()), shapes[i]
         assert torch.equal(trips[i][0], clones[i][0]) and torch.equal(trips[i][2], clones[i][2])
+
+
+def test_layerwise_single_rank_is_the_grouped_step_bitexact():
+    """With one rank the layer-wise optimizer owns every matrix: its step is
+    libmuon's grouped step (same bits, momentum kept by the optimizer)."""
+    from newton_schulz_06_gb300.layerwise import LayerwiseMuon
+    shapes = [(256, 640), (640, 256), (300, 300), (96, 1000)]
+    trips = [case(r, c, 800 + i, momentum="zero") for i, (r, c) in enumerate(shapes)]
+    W2 = [t[0].clone() for t in trips]
+    G2 = [t[1].clone() for t in trips]
+    opt = Muon(trips)
+    lw = LayerwiseMuon(W2, G2)
+    assert lw.world == 1 and lw.owned == list(range(len(shapes)))
+    for _ in range(2):
+        opt.step()
+        lw.step()
+    opt.sync()
+    lw.sync()
+    torch.cuda.synchronize()
+    for i in range(len(shapes)):
+        assert torch.equal(trips[i][0], W2[i]), shapes[i]
+        assert torch.equal(trips[i][2], lw.momentum[i]), shapes[i]
