@@ -238,7 +238,8 @@ size_t meta_bound(const std::vector<UnitDesc>& units) {
         unit_tiles(u, true, &s2, &g2, &x, &y);
         s = std::max(s, s2);
         g = std::max(g, g2);
-        // tile lists (twice: tiles may be split in halves) and pair offsets
+        // tile lists (room for twice the tiles, as if every tile were split in
+        // halves) and pair offsets
         b += sizeof(EwUnit) + sizeof(NsUnit) + 8 * 256 +
              2 * size_t(2 * s + g) * sizeof(TileItem) + 3 * 4 * 1024;
     }

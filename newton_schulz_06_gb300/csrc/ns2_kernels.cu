@@ -6,9 +6,9 @@
 // Why pairs: at full tensor rate a single CTA with 128 x 256 tiles consumes
 // 48 KB of operands per 512 cycles, and four 48 KB stages do not cover the
 // TMA round trip under load.  In a pair each CTA stages only its 128 rows of
-// A and its half (128 rows or columns) of B, 32 KB per k-block, so six
-// stages fit in shared memory and the L2-to-SM traffic per FLOP drops by a
-// third.  The even CTA of the pair (the leader) issues
+// A and its half (128 rows or columns) of B, 32 KB per k-block, so five
+// stages fit in shared memory beside the epilogue's buffers and the L2-to-SM
+// traffic per FLOP drops by a third.  The even CTA of the pair (the leader) issues
 // tcgen05.mma.cta_group::2 with M = 256, N = 256: rows 0-127 of A and the
 // first half of B come from its shared memory, rows 128-255 and the second
 // half of B from the peer's, and each CTA's TMEM receives its own 128 rows of
@@ -16,6 +16,15 @@
 // the leader's barrier.  The leader's commits multicast to both CTAs.  Both
 // CTAs' epilogues drain their TMEM rows and release the accumulator on the
 // leader's barrier.
+//
+// The producer and MMA threads' per-k-block loops are on the critical path
+// (a few added instructions there cost several percent): both test their
+// barrier inline and call the bounded wait only when the stage is not ready,
+// and the MMA thread adds offsets to precomputed descriptors.
+//
+// Distributed mode's first product (SL = 1) runs each tile's K slices in
+// turn on the same pair and sums them in tensor memory (accumulator 0 holds
+// the running sum, accumulator 1 the newest slice).
 //
 // Symmetric stages compute tiles (ti, tj) with ti <= tj on the 256 grid
 // ("Advancing Emerging Optimizers for Accelerated LLM Training", section
