@@ -176,10 +176,11 @@ MUON_API const char* muon_last_error(muon_handle h);
 /* Stage timing.  When on, muon_step records CUDA events around each kind of
  * launch on the handle's stream; muon_stage_times() (after muon_sync) fills
  * up to `n` totals in milliseconds for the last step, in the order
- * momentum, norm, normalise, syrk1, syrk2, gemm, update, and the number of
- * launches of each kind into `launches` (may be NULL).  Returns the number
- * of stages written. */
-#define MUON_N_STAGES 7
+ * momentum, norm, normalise, syrk1, syrk2, gemm, update, fused (a GEMM
+ * launch that also runs the next iteration's first product), and the number
+ * of launches of each kind into `launches` (may be NULL).  Returns the
+ * number of stages written. */
+#define MUON_N_STAGES 8
 MUON_API int muon_set_profiling(muon_handle h, int on);
 MUON_API int muon_stage_times(muon_handle h, float* ms, int* launches, int n);
 

@@ -25,9 +25,9 @@ MUON_FULL = 0
 MUON_BLOCKWISE = 1
 MUON_DISTRIBUTED = 2
 MUON_HOST_ONLY = -1
-MUON_N_STAGES = 7
+MUON_N_STAGES = 8
 STAGE_NAMES = ("momentum", "norm", "normalise", "syrk1", "syrk2", "gemm",
-               "update")
+               "update", "fused")
 
 # Every entry point include/muon.h declares.
 EXPORTS = ("muon_create", "muon_set_stream", "muon_register_params",

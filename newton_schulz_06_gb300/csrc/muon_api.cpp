@@ -13,6 +13,7 @@
 // every unit's intermediates at once; they run one after another.
 #include <algorithm>
 #include <cmath>
+#include <map>
 #include <queue>
 #include <cstdio>
 #include <cstdlib>
@@ -38,7 +39,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 enum Stage { ST_MOMENTUM, ST_NORM, ST_NORMALISE, ST_SYRK1, ST_SYRK2,
-             ST_GEMM, ST_UPDATE };
+             ST_GEMM, ST_UPDATE, ST_FUSED };
 
 struct UnitDesc {
     int param = 0, block = 0;
@@ -47,6 +48,7 @@ struct UnitDesc {
     bool transposed = false;
     float scale = 1.f;
     size_t x_bytes = 0, mm_bytes = 0, buf_bytes = 0;
+    size_t row_bytes = 0;       // fused launches: one counter per 256-row block
     int shards = 1;             // distributed mode: slices of the long side
     int64_t ew_tiles = 0;
     size_t need = 0;   // scratch bytes of this unit inside a group
@@ -62,6 +64,16 @@ struct GroupDesc {
     // CTA-pair schedules: per-pair offsets into the tile lists
     size_t o_sx_off = 0, o_sa_off = 0, o_g_off = 0;
     int p_sx = 0, p_sa = 0, p_g = 0;
+    // fused launches (GEMM of iteration s + first product of s + 1)
+    size_t t_f_off = 0, o_f_off = 0;
+    int n_f = 0, p_f = 0;
+    bool fused_ok = false;
+    // fused launches since the counters were last zeroed; the counters sit
+    // in the metadata region (never aliased by a group's scratch) and only
+    // grow, so a launch waits for PAIR_EPI_WARPS * row tiles * its epoch
+    int64_t fuse_epoch = 0;
+    size_t rc_off = 0, rc_bytes = 0;         // this group's counter block
+    int64_t rc_step = 0;                     // largest per-launch increment
     int64_t ew_tiles = 0;
     int shards = 1;                          // distributed mode: P
 };
@@ -109,6 +121,8 @@ struct muon_ctx {
     // (groups whose weights are all bf16 and 16-byte aligned; else pass 0)
     int fuse_update = 2;
     int stages = 5;            // pair mode: TMA pipeline depth (4 or 5)
+    bool fuse_stages = true;   // pair mode: GEMM(s) and first product of s+1 in one launch
+    int64_t rc_limit = int64_t(1) << 30;   // row-counter target at which they are zeroed
     int max_pairs = 0;
 };
 
@@ -220,6 +234,7 @@ int build_units(muon_ctx* h, int mode, int nb, std::vector<UnitDesc>* out) {
                             std::to_string(shards) + " slices of n=" + std::to_string(u.n) +
                                 " (parameter " + std::to_string(i) +
                                 ") are not equal multiples of 64");
+            u.row_bytes = align_up(size_t(ceil_div(u.m, 256)) * 4, 256);
             u.buf_bytes = 2 * u.x_bytes + 2 * u.mm_bytes;
             u.ew_tiles = ceil_div(u.m, EW_TILE) * ceil_div(u.n, EW_TILE);
             u.need = u.buf_bytes + size_t(u.ew_tiles) * 4 * EW_PARTIALS_PER_TILE + 4;
@@ -240,7 +255,7 @@ size_t meta_bound(const std::vector<UnitDesc>& units) {
         g = std::max(g, g2);
         // tile lists (room for twice the tiles, as if every tile were split in
         // halves) and pair offsets
-        b += sizeof(EwUnit) + sizeof(NsUnit) + 8 * 256 +
+        b += sizeof(EwUnit) + sizeof(NsUnit) + 8 * 256 + u.row_bytes +
              2 * size_t(2 * s + g) * sizeof(TileItem) + 3 * 4 * 1024;
     }
     return align_up(b, 1024);
@@ -365,6 +380,61 @@ void lpt_schedule(std::vector<TileItem>* v, int P, bool allow_split,
     (*off)[P] = static_cast<int32_t>(v->size());
 }
 
+// Groups with at most this many GEMM tiles per CTA pair fuse GEMM(s) with
+// the first product of s + 1.
+constexpr int FUSE_MAX_TILES_PER_PAIR = 8;
+
+// Schedule of a fused launch over P CTA pairs: the GEMM tiles by the LPT
+// rule above, then the first-product tiles of the next iteration in the
+// order their two row blocks of X' complete under that schedule (a row block
+// is complete when its last GEMM tile ends), each to the pair that is free
+// first.  Every pair's list has its GEMM tiles before its first-product
+// tiles, so a waiting tile only ever waits on tiles that never wait.
+void lpt_schedule_fused(std::vector<TileItem> gemm, const std::vector<TileItem>& syrk, int P,
+                        std::vector<TileItem>* v, std::vector<int32_t>* off) {
+    std::vector<int32_t> goff;
+    lpt_schedule(&gemm, P, false, &goff);
+    // finish time of every (unit, row block) under the GEMM schedule
+    std::vector<int64_t> load(P, 0);
+    std::map<std::pair<int32_t, int>, int64_t> row_end;
+    for (int p = 0; p < P; ++p)
+        for (int k = goff[p]; k < goff[p + 1]; ++k) {
+            const TileItem& t = gemm[k];
+            load[p] += int64_t(t.k_blocks) * t.n_len;
+            int64_t& e = row_end[{t.unit, t.ti}];
+            e = std::max(e, load[p]);
+        }
+    auto ready = [&](const TileItem& t) {
+        return std::max(row_end[{t.unit, t.ti}], row_end[{t.unit, t.tj}]);
+    };
+    std::vector<size_t> order(syrk.size());
+    for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) {
+        return ready(syrk[a]) < ready(syrk[b]);
+    });
+    using Load = std::pair<int64_t, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> free_at;
+    for (int p = 0; p < P; ++p) free_at.push({load[p], p});
+    std::vector<std::vector<TileItem>> extra(P);
+    for (size_t i : order) {
+        const Load l = free_at.top();
+        free_at.pop();
+        TileItem t = syrk[i];
+        t.flags |= TILE_NEXT_SYRK;
+        extra[l.second].push_back(t);
+        free_at.push({std::max(l.first, ready(syrk[i])) + int64_t(t.k_blocks) * t.n_len,
+                      l.second});
+    }
+    v->clear();
+    off->assign(P + 1, 0);
+    for (int p = 0; p < P; ++p) {
+        (*off)[p] = static_cast<int32_t>(v->size());
+        v->insert(v->end(), gemm.begin() + goff[p], gemm.begin() + goff[p + 1]);
+        v->insert(v->end(), extra[p].begin(), extra[p].end());
+    }
+    (*off)[P] = static_cast<int32_t>(v->size());
+}
+
 int build_plan(muon_ctx* h, int mode, int nb) {
     Plan& P = h->plan;
     P = Plan();
@@ -407,6 +477,17 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         g.ns_off = off;
         off += sizeof(NsUnit) * nu;
         g.shards = P.units[g.u0].shards;
+        // row-block counters of fused launches, zero in the uploaded image
+        off = align_up(off, 256);
+        g.rc_off = off;
+        g.rc_step = 0;
+        for (int i = g.u0; i < g.u1; ++i) {
+            off += P.units[i].row_bytes;
+            g.rc_step = std::max<int64_t>(g.rc_step,
+                                          int64_t(PAIR_EPI_WARPS) * ceil_div(P.units[i].n, 256));
+        }
+        g.rc_bytes = off - g.rc_off;
+        size_t rc_next = g.rc_off;
         std::vector<TileItem> tsx, tsa, tg;
         int64_t tile_base = 0;
         for (int i = g.u0; i < g.u1; ++i) {
@@ -483,6 +564,8 @@ int build_plan(muon_ctx* h, int mode, int nb) {
             ns.x[1] = e.x[1];
             ns.a = reinterpret_cast<__nv_bfloat16*>(ab);
             ns.b = reinterpret_cast<__nv_bfloat16*>(bb);
+            ns.row_done = reinterpret_cast<int32_t*>(ws + rc_next);
+            rc_next += u.row_bytes;
             ns.m = u.m;
             ns.n = u.n;
             ns.ld_x = u.ld_x;
@@ -559,6 +642,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         sort_tiles(&tsx);
         sort_tiles(&tsa);
         sort_tiles(&tg);
+        const std::vector<TileItem> tsx0 = tsx, tg0 = tg;     // before put() reorders
         const int64_t base_sx = static_cast<int64_t>(tsx.size());
         const int64_t base_g = static_cast<int64_t>(tg.size());
         auto put = [&](std::vector<TileItem>& v, size_t* o, int* n, size_t* oo, int* np) {
@@ -584,6 +668,32 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         put(tsx, &g.t_sx_off, &g.n_sx, &g.o_sx_off, &g.p_sx);
         put(tsa, &g.t_sa_off, &g.n_sa, &g.o_sa_off, &g.p_sa);
         put(tg, &g.t_g_off, &g.n_g, &g.o_g_off, &g.p_g);
+        g.fuse_epoch = 0;
+        // Fusing pays where the GEMM's last wave is a large share of the
+        // launch (few tiles per pair, as for one large matrix); with many
+        // short tiles per pair the extra store completion per GEMM tile in
+        // the epilogue costs more (measured: 4096^2 -1.8%, a 388-matrix
+        // group +3.6%)
+        g.fused_ok = h->pair && h->fuse_stages && g.shards == 1 && !tg0.empty() &&
+                     tg0.size() <= size_t(FUSE_MAX_TILES_PER_PAIR) *
+                                       size_t(std::max(1, h->max_pairs));
+        if (g.fused_ok) {
+            const int pairs = std::max(
+                1, std::min(h->max_pairs, static_cast<int>(tg0.size() + tsx0.size())));
+            std::vector<TileItem> vf;
+            std::vector<int32_t> offs;
+            lpt_schedule_fused(tg0, tsx0, pairs, &vf, &offs);
+            off = align_up(off, 256);
+            g.o_f_off = off;
+            g.p_f = pairs;
+            std::memcpy(meta.data() + off, offs.data(), offs.size() * sizeof(int32_t));
+            off += offs.size() * sizeof(int32_t);
+            off = align_up(off, 256);
+            g.t_f_off = off;
+            g.n_f = static_cast<int>(vf.size());
+            std::memcpy(meta.data() + off, vf.data(), vf.size() * sizeof(TileItem));
+            off += vf.size() * sizeof(TileItem);
+        }
         P.syrk_tiles += base_sx;
         P.gemm_tiles += base_g;
         P.ew_tiles += g.ew_tiles;
@@ -671,6 +781,11 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     h->fuse = fuse;
     h->fuse_update = fuse_update;
     if (const char* pd = std::getenv("MUON_PDL")) set_programmatic_launch(std::string(pd) != "0");
+    if (const char* fs = std::getenv("MUON_FUSE_STAGES")) h->fuse_stages = std::string(fs) != "0";
+    if (const char* rl = std::getenv("MUON_FUSE_COUNTER_LIMIT")) {
+        const long long v = std::atoll(rl);
+        if (v > 0 && v <= (1ll << 30)) h->rc_limit = v;
+    }
     if (const char* st = std::getenv("MUON_STAGES")) {
         const int v = std::atoi(st);
         if (v >= 4 && v <= 5) h->stages = v;
@@ -790,7 +905,7 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         if (h->profiling) cudaEventRecord(h->launches.back().stop, h->stream);
     };
     const int ew_grid_cap = h->num_sms * 8;
-    for (const GroupDesc& g : P.groups) {
+    for (GroupDesc& g : P.groups) {
         const int nu = g.u1 - g.u0;
         const size_t inv_off = P.scratch_off;
         const size_t part_off = align_up(inv_off + size_t(nu) * 4, 256);
@@ -808,6 +923,13 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         ew.eps = NORM_EPS;
         const int ew_grid = static_cast<int>(std::min<int64_t>(g.ew_tiles, ew_grid_cap));
         const bool fused = h->pair && h->fuse;
+        if (g.fused_ok && ns_steps > 1 &&
+            g.rc_step * (g.fuse_epoch + ns_steps) > h->rc_limit) {
+            // the targets would near int32 overflow: start the counters over
+            const cudaError_t ce = cudaMemsetAsync(ws + g.rc_off, 0, g.rc_bytes, h->stream);
+            if (ce != cudaSuccess) return cuda_fail(h, ce, "row counter reset");
+            g.fuse_epoch = 0;
+        }
         ew.write_x = fused ? 1 : 0;
         cudaError_t e;
         if (!begin(ST_MOMENTUM)) return fail(h, MUON_ERR_CUDA, "event create");
@@ -835,6 +957,9 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         L.ew = ew.units;
         L.lr = lr;
         int cur = 0;
+        // GEMM(s) and the first product of s + 1 share a launch (all but the
+        // last iteration); that first product then does not run on its own
+        const bool fuse_it = g.fused_ok && ns_steps > 1;
         for (int s = 0; s < ns_steps; ++s) {
             L.src = cur;
             L.first = (fused && s == 0) ? 1 : 0;
@@ -842,15 +967,23 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
             const bool upd_regs = fused && h->fuse_update == 1;
             const bool upd_tma = fused && h->fuse_update == 2 && g.w_tma;
             L.last = (last && (upd_regs || upd_tma)) ? 1 : 0;
-            const struct { NsOp op; size_t off; int n; int st; size_t oo; int np; } seq[3] = {
-                {OP_SYRK_X, g.t_sx_off, g.n_sx, ST_SYRK1, g.o_sx_off, g.p_sx},
-                {OP_SYRK_A, g.t_sa_off, g.n_sa, ST_SYRK2, g.o_sa_off, g.p_sa},
-                {OP_GEMM_BX, g.t_g_off, g.n_g, ST_GEMM, g.o_g_off, g.p_g}};
-            for (const auto& q : seq) {
+            struct Q { NsOp op; size_t off; int n; int st; size_t oo; int np; };
+            Q seq[3];
+            int nq = 0;
+            if (!(fuse_it && s > 0))
+                seq[nq++] = {OP_SYRK_X, g.t_sx_off, g.n_sx, ST_SYRK1, g.o_sx_off, g.p_sx};
+            seq[nq++] = {OP_SYRK_A, g.t_sa_off, g.n_sa, ST_SYRK2, g.o_sa_off, g.p_sa};
+            if (fuse_it && !last)
+                seq[nq++] = {OP_FUSED, g.t_f_off, g.n_f, ST_FUSED, g.o_f_off, g.p_f};
+            else
+                seq[nq++] = {OP_GEMM_BX, g.t_g_off, g.n_g, ST_GEMM, g.o_g_off, g.p_g};
+            for (int qi = 0; qi < nq; ++qi) {
+                const Q& q = seq[qi];
                 L.tiles = reinterpret_cast<const TileItem*>(ws + q.off);
                 L.num_tiles = q.n;
                 L.pair_off = h->pair ? reinterpret_cast<const int32_t*>(ws + q.oo) : nullptr;
                 L.shards = g.shards;
+                L.fuse_epoch = (q.op == OP_FUSED) ? static_cast<int32_t>(++g.fuse_epoch) : 0;
                 if (!begin(q.st)) return fail(h, MUON_ERR_CUDA, "event create");
                 if (h->pair && q.op == OP_GEMM_BX && L.last && upd_tma)
                     e = launch_ns_pair_update(L, q.np, h->stream);

@@ -68,6 +68,10 @@ struct alignas(128) NsUnit {
     __nv_bfloat16* x[2];
     __nv_bfloat16* a;
     __nv_bfloat16* b;
+    // GEMM tiles of a launch that also holds the next iteration's first
+    // product: per 256-row block of X', the epilogue warps that finished
+    // storing their part (PAIR_EPI_WARPS per tile)
+    int32_t* row_done;
     int32_t m, n, ld_x, ld_mm;
 };
 
@@ -79,9 +83,20 @@ struct TileItem {
     int16_t ti, tj;
     int16_t n_off, n_len;
     int32_t k_blocks;        // number of BK steps (cost, also used by LPT)
+    int32_t flags;           // TILE_*
 };
 
-enum NsOp { OP_SYRK_X = 0, OP_SYRK_A = 1, OP_GEMM_BX = 2 };
+// In a launch of OP_FUSED, a tile of the next iteration's first product
+// (A' = X' X'^T); the other tiles are this iteration's GEMM (X' = a X + B X).
+constexpr int TILE_NEXT_SYRK = 1;
+// epilogue warps of a CTA pair (each counts once per finished GEMM tile)
+constexpr int PAIR_EPI_WARPS = 16;
+
+// OP_FUSED: one launch with iteration s's GEMM and iteration s+1's first
+// product.  A first-product tile starts once the two 256-row blocks of X' it
+// reads are complete (row counters of the GEMM tiles); every CTA pair runs
+// all its GEMM tiles first, so no wait depends on a tile that waits.
+enum NsOp { OP_SYRK_X = 0, OP_SYRK_A = 1, OP_GEMM_BX = 2, OP_FUSED = 3 };
 
 struct NsLaunch {
     const NsUnit* units;
@@ -104,6 +119,10 @@ struct NsLaunch {
     // (a cost-balanced schedule built by the planner); nullptr = pair p takes
     // tiles p, p + pairs, ...
     const int32_t* pair_off;
+    // OP_FUSED: the launch's number since the plan was built (from 1); a row
+    // block of X' is complete when its counter reaches
+    // PAIR_EPI_WARPS * (GEMM tiles per row) * fuse_epoch
+    int32_t fuse_epoch;
     // Distributed mode, first product (CTA-pair kernels): the K range of
     // every tile is `shards` equal slices.  The pair runs them in turn, slice
     // 0 into accumulator 0 and each later slice into accumulator 1, which

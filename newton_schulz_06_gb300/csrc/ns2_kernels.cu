@@ -97,6 +97,16 @@ __device__ __forceinline__ void commit_pair_local(uint32_t bar) {
         : "memory");
 }
 
+// The operation of tile t in a launch of OP (per tile only for OP_FUSED).
+template <int OP>
+__device__ __forceinline__ int tile_op(const TileItem& t) {
+    if (OP != OP_FUSED) return OP;
+    return (t.flags & TILE_NEXT_SYRK) ? OP_SYRK_X : OP_GEMM_BX;
+}
+
+// GEMM tiles per 256-row block of X' (= column tiles of the unit).
+__device__ __forceinline__ int row_tiles(const NsUnit& U) { return (U.n + 255) / 256; }
+
 // Tile-constant fields of a unit, copied into registers once per tile (the
 // kernels store through pointers the compiler cannot tell apart from the
 // tables, so fields read from the tables would be reloaded after every
@@ -120,12 +130,13 @@ struct EpiUnit {
     float step;
 };
 
+// op: the tile's operation (OP itself unless OP == OP_FUSED).
 template <int OP>
-__device__ __forceinline__ EpiUnit load_epi_unit(const NsLaunch& p, int unit) {
+__device__ __forceinline__ EpiUnit load_epi_unit(const NsLaunch& p, int unit, int op) {
     const NsUnit* U = p.units + unit;
     EpiUnit e;
-    e.te_in = (OP == OP_GEMM_BX) ? &U->te_x[p.src] : &U->te_a;
-    e.te_out = (OP == OP_SYRK_X) ? &U->te_a : (OP == OP_SYRK_A) ? &U->te_b : &U->te_x[p.src ^ 1];
+    e.te_in = (op == OP_GEMM_BX) ? &U->te_x[p.src] : &U->te_a;
+    e.te_out = (op == OP_SYRK_X) ? &U->te_a : (op == OP_SYRK_A) ? &U->te_b : &U->te_x[p.src ^ 1];
     e.te_w = &U->te_w;
     e.m = U->m;
     e.n = U->n;
@@ -134,14 +145,14 @@ __device__ __forceinline__ EpiUnit load_epi_unit(const NsLaunch& p, int unit) {
     e.xin = U->x[p.src];
     e.xout = U->x[p.src ^ 1];
     e.ain = U->a;
-    e.out = (OP == OP_SYRK_X) ? U->a : U->b;
+    e.out = (op == OP_SYRK_X) ? U->a : U->b;
     e.w = nullptr;
     e.w_dbg = nullptr;
     e.o_dbg = nullptr;
     e.ld_w = e.ld_dbg = 0;
     e.w_f32 = e.vec16 = e.transposed = 0;
     e.step = 0.f;
-    if (OP == OP_GEMM_BX && p.last) {
+    if (op == OP_GEMM_BX && p.last) {
         const EwUnit* E = p.ew + unit;
         e.w = E->w;
         e.w_dbg = E->w_dbg;
@@ -366,6 +377,7 @@ struct InPlan {
     int transposed;              // folded update: W is the iterate's transpose
     int r0w, col0;               // first row, first column of the warp's part
     int n;                       // needed blocks
+    int uses_in;                 // the tile reads input blocks
     uint32_t order;              // their column-block indices, 2 bits each
     __device__ __forceinline__ int block(int k) const {
         return static_cast<int>((order >> (2 * k)) & 3u);
@@ -376,14 +388,16 @@ template <int OP>
 __device__ __forceinline__ InPlan plan_blocks(const NsLaunch& p, const TileItem& t,
                                               uint32_t rank, int lg, int half) {
     const NsUnit* U = p.units + t.unit;
+    const int op = tile_op<OP>(t);
     InPlan q;
-    q.te_in = (OP == OP_GEMM_BX) ? &U->te_x[p.src] : &U->te_a;
+    q.te_in = (op == OP_GEMM_BX) ? &U->te_x[p.src] : &U->te_a;
     q.te_w = &U->te_w;
-    q.transposed = (OP == OP_GEMM_BX && p.last) ? p.ew[t.unit].transposed : 0;
+    q.transposed = (op == OP_GEMM_BX && p.last) ? p.ew[t.unit].transposed : 0;
+    q.uses_in = op != OP_SYRK_X;
     q.r0w = t.ti * 256 + static_cast<int>(rank) * P_HALF + lg * 32;
     q.col0 = t.tj * 256 + half * 128;
     const int m = U->m;
-    const int lim_c = (OP == OP_GEMM_BX) ? U->n : m;
+    const int lim_c = (op == OP_GEMM_BX) ? U->n : m;
     q.n = 0;
     q.order = 0;
 #pragma unroll
@@ -391,7 +405,7 @@ __device__ __forceinline__ InPlan plan_blocks(const NsLaunch& p, const TileItem&
         const int gc0 = q.col0 + 32 * c;
         const int rel = half * 128 + 32 * c;          // column within the tile
         bool nd = q.r0w < m && gc0 < lim_c && rel >= t.n_off && rel < t.n_off + t.n_len;
-        if (OP != OP_GEMM_BX) nd = nd && gc0 >= q.r0w;    // upper blocks only
+        if (op != OP_GEMM_BX) nd = nd && gc0 >= q.r0w;    // upper blocks only
         if (nd) q.order |= static_cast<uint32_t>(c) << (2 * q.n++);
     }
     return q;
@@ -555,11 +569,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 const TileItem t = t_next;
                 if (it + tr.step < tr.end) t_next = p.tiles[it + tr.step];
                 const NsUnit* U = p.units + t.unit;
+                const int op = tile_op<OP>(t);
+                // in a fused launch the first-product tiles read X' (the
+                // other buffer), once the GEMM tiles wrote both row blocks
+                const bool next_syrk = (OP == OP_FUSED) && op == OP_SYRK_X;
                 const void* tmA;
                 const void* tmB;
-                if (OP == OP_SYRK_X) { tmA = &U->tm_x[p.src]; tmB = tmA; }
-                else if (OP == OP_SYRK_A) { tmA = &U->tm_a; tmB = tmA; }
+                if (op == OP_SYRK_X) { tmA = &U->tm_x[next_syrk ? p.src ^ 1 : p.src]; tmB = tmA; }
+                else if (op == OP_SYRK_A) { tmA = &U->tm_a; tmB = tmA; }
                 else { tmA = &U->tm_b; tmB = &U->tm_x[p.src]; }
+                if (next_syrk) {
+                    const int32_t target = PAIR_EPI_WARPS * row_tiles(*U) * p.fuse_epoch;
+                    if (!wait_count(U->row_done + t.ti, target, abort_flag, p.err, limit) ||
+                        !wait_count(U->row_done + t.tj, target, abort_flag, p.err, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_global();      // TMA reads after the acquire
+                }
                 const int kblocks = t.k_blocks;
                 const int r0 = t.ti * 256 + static_cast<int>(rank) * P_HALF;
                 // N = n_len columns split evenly over the pair (64 or 128 each)
@@ -581,7 +608,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                     const int k0 = kb * BK;
                     tma_load_2d_pair(a_dst, tmA, fb, k0, r0);
                     tma_load_2d_pair(a_dst + P_BOX, tmA, fb, k0, r0 + 64);
-                    if (OP == OP_GEMM_BX) {
+                    if (op == OP_GEMM_BX) {
                         tma_load_2d_pair(b_dst, tmB, fb, b0, k0);
                         if (hb > 64) tma_load_2d_pair(b_dst + P_BOX, tmB, fb, b0 + 64, k0);
                     } else {
@@ -614,14 +641,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             constexpr bool sliced = SL != 0;
             uint32_t u0 = 0, u1 = 0;
             const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024);
-            const uint64_t b_desc0 = (OP == OP_GEMM_BX) ? smem_desc(smem_u32(sB), P_BOX, 1024)
-                                                        : smem_desc(smem_u32(sB), 16, 1024);
+            // B operand: MN-major for the GEMM (X), K-major otherwise
+            const uint64_t b_desc_mn = smem_desc(smem_u32(sB), P_BOX, 1024);
+            const uint64_t b_desc_k = smem_desc(smem_u32(sB), 16, 1024);
             const TileRange tr = tile_range(p, pair, npairs);
             TileItem t_next = tr.begin < tr.end ? p.tiles[tr.begin] : TileItem{};
             for (int it = tr.begin; ok && it < tr.end; it += tr.step, ++local) {
                 const TileItem t = t_next;
                 if (it + tr.step < tr.end) t_next = p.tiles[it + tr.step];
-                const uint32_t idesc = instr_desc(256, t.n_len, OP == OP_GEMM_BX ? 1 : 0);
+                const int op = tile_op<OP>(t);
+                const uint32_t idesc = instr_desc(256, t.n_len, op == OP_GEMM_BX ? 1 : 0);
+                const uint64_t b_desc0 = (op == OP_GEMM_BX) ? b_desc_mn : b_desc_k;
+                const uint32_t b_kstep = (op == OP_GEMM_BX) ? (2048 >> 4) : (32 >> 4);
                 const int kblocks = t.k_blocks;
                 const int kslice = sliced ? kblocks / p.shards : kblocks;
                 const int acc = sliced ? 0 : (local & 1);
@@ -663,8 +694,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         const uint64_t ad = ad0 + static_cast<uint64_t>(kk * 2);
-                        const uint64_t bd =
-                            bd0 + static_cast<uint64_t>(kk * ((OP == OP_GEMM_BX) ? 2048 : 32) >> 4);
+                        const uint64_t bd = bd0 + static_cast<uint64_t>(kk * b_kstep);
                         mma_pair(d_tmem, ad, bd, idesc,
                              ((sliced ? kin : kb) > 0 || kk > 0) ? 1u : 0u);
                     }
@@ -709,7 +739,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         tempty_leader[1] = map_to_rank(smem_u32(&tempty_bar[1]), 0);
         int local = 0;
         bool ok = true;
-        const bool uses_in = (OP != OP_SYRK_X);
         const TileRange tr = tile_range(p, pair, npairs);
         TileItem t_next = tr.begin < tr.end ? p.tiles[tr.begin] : TileItem{};
         // input blocks stream through the slots in tile order, across tile
@@ -727,21 +756,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             const TileItem t = t_next;
             const bool has_next = it + tr.step < tr.end;
             if (has_next) t_next = p.tiles[it + tr.step];
-            if (uses_in)
+            if (cur.uses_in)
                 while (cur_issued < cur.n && in_seq - in_use < static_cast<uint32_t>(NS))
                     issue_from(cur, cur_issued++);
             nxt.n = 0;
             nxt_issued = 0;
             if (has_next) nxt = plan_blocks<OP>(p, t_next, rank, lg, half);
-            const EpiUnit u = load_epi_unit<OP>(p, t.unit);
+            const int op = tile_op<OP>(t);
+            const bool uses_in = cur.uses_in;
+            const EpiUnit u = load_epi_unit<OP>(p, t.unit, op);
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             const int r0w = cur.r0w;
             const int col0 = cur.col0;
             float scale = 1.f;
-            if (p.first && OP != OP_SYRK_A) {
+            // iteration 1 scales by the norm; a fused launch's first-product
+            // tiles belong to the next iteration
+            if (p.first && op != OP_SYRK_A && !(OP == OP_FUSED && op == OP_SYRK_X)) {
                 const float inv = p.inv_norm[t.unit];
-                scale = (OP == OP_SYRK_X) ? inv * inv : inv;
+                scale = (op == OP_SYRK_X) ? inv * inv : inv;
             }
             // the blocks this warp stores (warp-uniform), in order
             const int n_need = cur.n;
@@ -800,7 +833,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                     ld_row_bf16(slot, lane, x);
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        v[e] = (OP == OP_SYRK_A) ? fmaf(p.b, x[e], p.c * v[e])
+                        v[e] = (op == OP_SYRK_A) ? fmaf(p.b, x[e], p.c * v[e])
                                                  : scale * fmaf(p.a, x[e], v[e]);
                     if (FW) {
                         // W <- W - lr*scale*O, O = bf16(v); no X' output
@@ -811,13 +844,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                     // refill the slot: this tile's next block, else the next
                     // tile's first
                     if (cur_issued < cur.n) issue_from(cur, cur_issued++);
-                    else if (nxt_issued < nxt.n) issue_from(nxt, nxt_issued++);
+                    else if (nxt.uses_in && nxt_issued < nxt.n) issue_from(nxt, nxt_issued++);
                     if (FW) continue;
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] *= scale;
                 }
-                if (OP == OP_GEMM_BX) {
+                if (op == OP_GEMM_BX) {
                     if (p.last) {
                         stage_free(lane);
                         gemm_update_block(u, r0w, gc0, lane, v, s_st + (st_seq & 1u) * P_BLK);
@@ -850,6 +883,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 }
             }
             if (!__all_sync(0xffffffffu, ok)) break;
+            if (OP == OP_FUSED && op == OP_GEMM_BX) {
+                // this warp's part of row block ti of X' is in memory: count
+                // it for the first-product tiles waiting on the row
+                if (lane == 0) {
+                    bulk_wait_all0();
+                    fence_proxy_async_global();
+                    count_release(p.units[t.unit].row_done + t.ti);
+                }
+                __syncwarp();
+            }
             cur = nxt;
             cur_issued = nxt_issued;
             tc_fence_before();
@@ -937,6 +980,7 @@ cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, int stages,
         case OP_SYRK_X: return launch_pair_op<OP_SYRK_X>(p, pairs, stages, s);
         case OP_SYRK_A: return launch_pair_op<OP_SYRK_A>(p, pairs, stages, s);
         case OP_GEMM_BX: return launch_pair_op<OP_GEMM_BX>(p, pairs, stages, s);
+        case OP_FUSED: return launch_pair_op<OP_FUSED>(p, pairs, stages, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -95,6 +95,40 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Bounded wait until a global counter that other CTAs of the grid raise
+// reaches `target`, with acquire semantics (the caller's later accesses see
+// what the raisers wrote before their release).  Same failure behaviour as
+// wait_bounded.
+__device__ __noinline__ bool wait_count(const int32_t* cnt, int32_t target,
+                                        volatile int* abort_flag, int* err,
+                                        uint64_t limit_ns) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+        if (v >= target) return true;
+        if ((i & 15) == 15) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > limit_ns) {
+                *abort_flag = 1;
+                atomicCAS(err, 0, DEV_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Adds 1 to a global counter with release semantics.
+__device__ __forceinline__ void count_release(int32_t* cnt) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(cnt) : "memory");
+}
+
+// Orders this thread's generic-proxy and async-proxy (TMA) accesses to
+// global memory with each other.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Same, without recording anything: used while draining after an abort.
 __device__ __forceinline__ void wait_quiet(uint32_t bar, uint32_t parity,
                                            uint64_t limit_ns) {

@@ -71,9 +71,9 @@ def test_groups_from_a_small_workspace_bitexact():
     shapes = [(256, 512), (512, 256), (384, 384), (128, 640)]
     trips = [case(r, c, 30 + i) for i, (r, c) in enumerate(shapes)]
     clones = [[t.clone() for t in tr] for tr in trips]
-    _, _, o_big, opt = gpu_step(trips)
+    _, _, o_big, opt = gpu_step(trips, steps=2)
     mn, full = opt.workspace_size()
-    _, _, o_small, opt2 = gpu_step(clones, max_workspace=mn)
+    _, _, o_small, opt2 = gpu_step(clones, max_workspace=mn, steps=2)
     assert opt2.plan_info()["groups"] > 1
     for a, b in zip(o_big, o_small):
         assert torch.equal(a, b)
@@ -151,6 +151,7 @@ def test_output_singular_values_in_band():
 @pytest.mark.parametrize("fuse_env", [{"MUON_FUSE": "0"},
                                       {"MUON_FUSE_UPDATE": "0"},
                                       {"MUON_FUSE_UPDATE": "1"},
+                                      {"MUON_FUSE_STAGES": "0"},
                                       {"MUON_CTA_GROUP": "1"}])
 def test_alternative_pipelines_match_oracle(fuse_env, monkeypatch):
     """The unfused pipeline, the update fused into the last GEMM, and the
@@ -260,3 +261,36 @@ def test_layerwise_single_rank_is_the_grouped_step_bitexact():
     for i in range(len(shapes)):
         assert torch.equal(trips[i][0], W2[i]), shapes[i]
         assert torch.equal(trips[i][2], lw.momentum[i]), shapes[i]
+
+
+@pytest.mark.parametrize("ns_steps", [1, 2, 5])
+def test_fused_gemm_and_next_first_product_bitexact(ns_steps, monkeypatch):
+    """One launch holding iteration s's GEMM and iteration s+1's first
+    product (the latter waiting on row-block counters) computes every tile as
+    the separate launches do: identical bits, over two steps (the counters
+    carry across launches and steps)."""
+    shapes = [(512, 768), (768, 2048), (300, 300), (2048, 640), (96, 1000)]
+    trips = [case(r, c, 900 + i) for i, (r, c) in enumerate(shapes)]
+    clones = [[t.clone() for t in tr] for tr in trips]
+    _, w1, o1, _ = gpu_step(trips, ns_steps=ns_steps, steps=2)
+    monkeypatch.setenv("MUON_FUSE_STAGES", "0")
+    _, w2, o2, _ = gpu_step(clones, ns_steps=ns_steps, steps=2)
+    for i in range(len(shapes)):
+        assert torch.equal(o1[i], o2[i]), shapes[i]
+        assert torch.equal(trips[i][0], clones[i][0]), shapes[i]
+
+
+def test_fused_counters_zeroed_and_restarted_bitexact(monkeypatch):
+    """The fused launches' row counters only grow across steps; when a
+    step's targets would pass the limit the group's counters are zeroed and
+    the epochs start over.  With a limit of 1 that happens before every
+    step: three steps give the same bits as counters that never restart."""
+    shapes = [(1024, 1536), (640, 640)]
+    trips = [case(r, c, 950 + i) for i, (r, c) in enumerate(shapes)]
+    clones = [[t.clone() for t in tr] for tr in trips]
+    _, _, o1, _ = gpu_step(trips, steps=3)
+    monkeypatch.setenv("MUON_FUSE_COUNTER_LIMIT", "1")
+    _, _, o2, _ = gpu_step(clones, steps=3)
+    for i in range(len(shapes)):
+        assert torch.equal(o1[i], o2[i]), shapes[i]
+        assert torch.equal(trips[i][0], clones[i][0]), shapes[i]
