@@ -350,15 +350,17 @@ def run_ours(args, wl, world, rank, local, pg):
         "syrk1": sum(m * (m + 1) * n for m, n in units),
         "syrk2": sum(m * (m + 1) * m for m, n in units),
     }
-    # a fused launch runs one iteration's GEMM and the next one's first product
-    per_launch["fused"] = per_launch["gemm"] + per_launch["syrk1"]
+    # a chained launch runs every product of the step but the last X update
+    ns = kw.get("ns_steps", 5)
+    per_launch["chain"] = (ns * (per_launch["syrk1"] + per_launch["syrk2"])
+                           + (ns - 1) * per_launch["gemm"])
     dom = max((k for k in per_launch if stage_tot.get(k, (0, 0))[1]),
               key=lambda k: stage_tot[k][0])
     t_dom, n_dom = stage_tot[dom]
     avg_launch_s = t_dom / n_dom / 1e3
     achieved = per_launch[dom] / avg_launch_s / 1e12
     peak = peaks["bf16_tflops"]
-    op = {"gemm": 2, "syrk1": 0, "syrk2": 1, "fused": 3}[dom]
+    op = {"gemm": 2, "syrk1": 0, "syrk2": 1, "chain": 3}[dom]
     pair = os.environ.get("MUON_CTA_GROUP", "2") != "1"
     kname = f"ns2_kernel<{op}>" if pair else f"ns_kernel<{op}>"
     roofline = {"bound": "tensor", "kernel": kname, "stage": dom,

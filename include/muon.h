@@ -176,8 +176,8 @@ MUON_API const char* muon_last_error(muon_handle h);
 /* Stage timing.  When on, muon_step records CUDA events around each kind of
  * launch on the handle's stream; muon_stage_times() (after muon_sync) fills
  * up to `n` totals in milliseconds for the last step, in the order
- * momentum, norm, normalise, syrk1, syrk2, gemm, update, fused (a GEMM
- * launch that also runs the next iteration's first product), and the number
+ * momentum, norm, normalise, syrk1, syrk2, gemm, update, chain (one launch
+ * with every product of the step but the last X update), and the number
  * of launches of each kind into `launches` (may be NULL).  Returns the
  * number of stages written. */
 #define MUON_N_STAGES 8
@@ -211,6 +211,9 @@ typedef struct {
     /* per Newton-Schulz iteration, all units: useful = upper-triangle
      * symmetric products + the GEMM; executed = what the tiles compute */
     int64_t useful_flops, executed_flops;
+    /* groups whose products run as one chained launch per step (every
+     * product but the last X update; groups of few large matrices) */
+    int64_t chained_groups;
 } muon_plan_info;
 MUON_API int muon_get_plan_info(muon_handle h, int mode, int nb, muon_plan_info* out);
 

@@ -27,7 +27,7 @@ MUON_DISTRIBUTED = 2
 MUON_HOST_ONLY = -1
 MUON_N_STAGES = 8
 STAGE_NAMES = ("momentum", "norm", "normalise", "syrk1", "syrk2", "gemm",
-               "update", "fused")
+               "update", "chain")
 
 # Every entry point include/muon.h declares.
 EXPORTS = ("muon_create", "muon_set_stream", "muon_register_params",
@@ -51,7 +51,8 @@ class MuonPlanInfo(ctypes.Structure):
                 ("syrk_tiles", ctypes.c_int64), ("gemm_tiles", ctypes.c_int64),
                 ("ew_tiles", ctypes.c_int64),
                 ("useful_flops", ctypes.c_int64),
-                ("executed_flops", ctypes.c_int64)]
+                ("executed_flops", ctypes.c_int64),
+                ("chained_groups", ctypes.c_int64)]
 
 
 class MuonError(RuntimeError):

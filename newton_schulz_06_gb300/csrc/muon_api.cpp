@@ -39,7 +39,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 enum Stage { ST_MOMENTUM, ST_NORM, ST_NORMALISE, ST_SYRK1, ST_SYRK2,
-             ST_GEMM, ST_UPDATE, ST_FUSED };
+             ST_GEMM, ST_UPDATE, ST_CHAIN };
 
 struct UnitDesc {
     int param = 0, block = 0;
@@ -48,7 +48,7 @@ struct UnitDesc {
     bool transposed = false;
     float scale = 1.f;
     size_t x_bytes = 0, mm_bytes = 0, buf_bytes = 0;
-    size_t row_bytes = 0;       // fused launches: one counter per 256-row block
+    size_t row_bytes = 0;       // chained launches: X, A and B counters per 256-row block
     int shards = 1;             // distributed mode: slices of the long side
     int64_t ew_tiles = 0;
     size_t need = 0;   // scratch bytes of this unit inside a group
@@ -64,16 +64,18 @@ struct GroupDesc {
     // CTA-pair schedules: per-pair offsets into the tile lists
     size_t o_sx_off = 0, o_sa_off = 0, o_g_off = 0;
     int p_sx = 0, p_sa = 0, p_g = 0;
-    // fused launches (GEMM of iteration s + first product of s + 1)
-    size_t t_f_off = 0, o_f_off = 0;
-    int n_f = 0, p_f = 0;
-    bool fused_ok = false;
-    // fused launches since the counters were last zeroed; the counters sit
-    // in the metadata region (never aliased by a group's scratch) and only
-    // grow, so a launch waits for PAIR_EPI_WARPS * row tiles * its epoch
-    int64_t fuse_epoch = 0;
+    // chained launch (every product of iterations 1 .. ns but the last X
+    // update): one iteration's tiles per pair, pair offsets, and each pair's
+    // end without its X-update tiles
+    size_t t_c_off = 0, o_c_off = 0, e_c_off = 0;
+    int n_c = 0, p_c = 0;
+    bool chain_ok = false;
+    // completed rounds of the X, A and B row counters since they were last
+    // zeroed; the counters sit in the metadata region (never aliased by a
+    // group's scratch) and only grow
+    int64_t ep_x = 0, ep_a = 0, ep_b = 0;
     size_t rc_off = 0, rc_bytes = 0;         // this group's counter block
-    int64_t rc_step = 0;                     // largest per-launch increment
+    int64_t rc_step = 0;                     // largest per-round increment
     int64_t ew_tiles = 0;
     int shards = 1;                          // distributed mode: P
 };
@@ -121,7 +123,7 @@ struct muon_ctx {
     // (groups whose weights are all bf16 and 16-byte aligned; else pass 0)
     int fuse_update = 2;
     int stages = 5;            // pair mode: TMA pipeline depth (4 or 5)
-    bool fuse_stages = true;   // pair mode: GEMM(s) and first product of s+1 in one launch
+    bool fuse_stages = true;   // pair mode: iterations chained in one launch where it pays
     int64_t rc_limit = int64_t(1) << 30;   // row-counter target at which they are zeroed
     int max_pairs = 0;
 };
@@ -234,7 +236,7 @@ int build_units(muon_ctx* h, int mode, int nb, std::vector<UnitDesc>* out) {
                             std::to_string(shards) + " slices of n=" + std::to_string(u.n) +
                                 " (parameter " + std::to_string(i) +
                                 ") are not equal multiples of 64");
-            u.row_bytes = align_up(size_t(ceil_div(u.m, 256)) * 4, 256);
+            u.row_bytes = align_up(size_t(ceil_div(u.m, 256)) * 3 * 4, 256);
             u.buf_bytes = 2 * u.x_bytes + 2 * u.mm_bytes;
             u.ew_tiles = ceil_div(u.m, EW_TILE) * ceil_div(u.n, EW_TILE);
             u.need = u.buf_bytes + size_t(u.ew_tiles) * 4 * EW_PARTIALS_PER_TILE + 4;
@@ -380,57 +382,81 @@ void lpt_schedule(std::vector<TileItem>* v, int P, bool allow_split,
     (*off)[P] = static_cast<int32_t>(v->size());
 }
 
-// Groups with at most this many GEMM tiles per CTA pair fuse GEMM(s) with
-// the first product of s + 1.
+// Groups with at most this many X-update tiles per CTA pair chain their
+// iterations in one launch.  Chaining pays where stage tails are a large
+// share of a launch (few tiles per pair, as for one large matrix); with many
+// short tiles per pair the store completion the epilogue waits for before
+// counting a tile costs more (measured on a 388-matrix group: +3.6% for an
+// X update fused with the next first product).
 constexpr int FUSE_MAX_TILES_PER_PAIR = 8;
 
-// Schedule of a fused launch over P CTA pairs: the GEMM tiles by the LPT
-// rule above, then the first-product tiles of the next iteration in the
-// order their two row blocks of X' complete under that schedule (a row block
-// is complete when its last GEMM tile ends), each to the pair that is free
-// first.  Every pair's list has its GEMM tiles before its first-product
-// tiles, so a waiting tile only ever waits on tiles that never wait.
-void lpt_schedule_fused(std::vector<TileItem> gemm, const std::vector<TileItem>& syrk, int P,
-                        std::vector<TileItem>* v, std::vector<int32_t>* off) {
-    std::vector<int32_t> goff;
-    lpt_schedule(&gemm, P, false, &goff);
-    // finish time of every (unit, row block) under the GEMM schedule
-    std::vector<int64_t> load(P, 0);
-    std::map<std::pair<int32_t, int>, int64_t> row_end;
-    for (int p = 0; p < P; ++p)
-        for (int k = goff[p]; k < goff[p + 1]; ++k) {
-            const TileItem& t = gemm[k];
-            load[p] += int64_t(t.k_blocks) * t.n_len;
-            int64_t& e = row_end[{t.unit, t.ti}];
-            e = std::max(e, load[p]);
-        }
-    auto ready = [&](const TileItem& t) {
-        return std::max(row_end[{t.unit, t.ti}], row_end[{t.unit, t.tj}]);
-    };
-    std::vector<size_t> order(syrk.size());
-    for (size_t i = 0; i < order.size(); ++i) order[i] = i;
-    std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) {
-        return ready(syrk[a]) < ready(syrk[b]);
-    });
+bool chain_eligible(const muon_ctx* h, int shards, int64_t gemm_tiles) {
+    return h->pair && h->fuse_stages && shards == 1 && gemm_tiles > 0 &&
+           gemm_tiles <= int64_t(FUSE_MAX_TILES_PER_PAIR) * std::max(1, h->max_pairs);
+}
+
+// Schedule of a chained launch over P CTA pairs.  A list-scheduling
+// simulation runs the stages in order (first product, second product, X
+// update; costs k-blocks x columns): within a stage the tiles go in the
+// order their rows become ready (X rows ti, tj; A rows ti, tj; B row ti),
+// each to the pair that is free first, starting once its rows are ready.
+// Three iterations are simulated; the last one's per-pair lists are the
+// template every iteration walks.  Each list is in stage order, so a
+// waiting tile only waits on tiles of earlier stages.  end_last[p]: the end
+// of pair p's list without its X-update tiles.
+void lpt_schedule_chain(const std::vector<TileItem>& sx, const std::vector<TileItem>& sa,
+                        const std::vector<TileItem>& gm, int P, std::vector<TileItem>* v,
+                        std::vector<int32_t>* off, std::vector<int32_t>* end_last) {
+    using Row = std::pair<int32_t, int>;
     using Load = std::pair<int64_t, int>;
     std::priority_queue<Load, std::vector<Load>, std::greater<Load>> free_at;
-    for (int p = 0; p < P; ++p) free_at.push({load[p], p});
-    std::vector<std::vector<TileItem>> extra(P);
-    for (size_t i : order) {
-        const Load l = free_at.top();
-        free_at.pop();
-        TileItem t = syrk[i];
-        t.flags |= TILE_NEXT_SYRK;
-        extra[l.second].push_back(t);
-        free_at.push({std::max(l.first, ready(syrk[i])) + int64_t(t.k_blocks) * t.n_len,
-                      l.second});
+    for (int p = 0; p < P; ++p) free_at.push({0, p});
+    std::map<Row, int64_t> x_ready, a_ready, b_ready;
+    std::vector<std::vector<TileItem>> lists(P);
+    std::vector<int32_t> mid(P, 0);
+    // one stage: tiles by readiness, each to the pair free first; returns
+    // the time each written row completes
+    auto stage = [&](const std::vector<TileItem>& tiles, int op, std::map<Row, int64_t>& in,
+                     bool two_rows, bool mirrored, std::map<Row, int64_t>* out) {
+        auto ready = [&](const TileItem& t) {
+            const int64_t r0 = in[{t.unit, t.ti}];
+            return two_rows ? std::max(r0, in[{t.unit, t.tj}]) : r0;
+        };
+        std::vector<size_t> order(tiles.size());
+        for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+        std::stable_sort(order.begin(), order.end(),
+                         [&](size_t a, size_t b) { return ready(tiles[a]) < ready(tiles[b]); });
+        out->clear();
+        for (size_t i : order) {
+            TileItem t = tiles[i];
+            const Load l = free_at.top();
+            free_at.pop();
+            const int64_t end = std::max(l.first, ready(t)) + int64_t(t.k_blocks) * t.n_len;
+            free_at.push({end, l.second});
+            t.flags = (t.flags & ~TILE_OP_MASK) | op;
+            lists[l.second].push_back(t);
+            int64_t& e0 = (*out)[{t.unit, t.ti}];
+            e0 = std::max(e0, end);
+            if (mirrored) {
+                int64_t& e1 = (*out)[{t.unit, t.tj}];
+                e1 = std::max(e1, end);
+            }
+        }
+    };
+    for (int iter = 0; iter < 3; ++iter) {
+        for (auto& l : lists) l.clear();
+        stage(sx, OP_SYRK_X, x_ready, true, true, &a_ready);
+        stage(sa, OP_SYRK_A, a_ready, true, true, &b_ready);
+        for (int p = 0; p < P; ++p) mid[p] = static_cast<int32_t>(lists[p].size());
+        stage(gm, OP_GEMM_BX, b_ready, false, false, &x_ready);
     }
     v->clear();
     off->assign(P + 1, 0);
+    end_last->assign(P, 0);
     for (int p = 0; p < P; ++p) {
         (*off)[p] = static_cast<int32_t>(v->size());
-        v->insert(v->end(), gemm.begin() + goff[p], gemm.begin() + goff[p + 1]);
-        v->insert(v->end(), extra[p].begin(), extra[p].end());
+        (*end_last)[p] = (*off)[p] + mid[p];
+        v->insert(v->end(), lists[p].begin(), lists[p].end());
     }
     (*off)[P] = static_cast<int32_t>(v->size());
 }
@@ -483,6 +509,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         g.rc_step = 0;
         for (int i = g.u0; i < g.u1; ++i) {
             off += P.units[i].row_bytes;
+            // n >= m: X rows take the most per round
             g.rc_step = std::max<int64_t>(g.rc_step,
                                           int64_t(PAIR_EPI_WARPS) * ceil_div(P.units[i].n, 256));
         }
@@ -564,7 +591,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
             ns.x[1] = e.x[1];
             ns.a = reinterpret_cast<__nv_bfloat16*>(ab);
             ns.b = reinterpret_cast<__nv_bfloat16*>(bb);
-            ns.row_done = reinterpret_cast<int32_t*>(ws + rc_next);
+            ns.row_cnt = reinterpret_cast<int32_t*>(ws + rc_next);
             rc_next += u.row_bytes;
             ns.m = u.m;
             ns.n = u.n;
@@ -642,7 +669,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         sort_tiles(&tsx);
         sort_tiles(&tsa);
         sort_tiles(&tg);
-        const std::vector<TileItem> tsx0 = tsx, tg0 = tg;     // before put() reorders
+        const std::vector<TileItem> tsx0 = tsx, tsa0 = tsa, tg0 = tg;   // before put() reorders
         const int64_t base_sx = static_cast<int64_t>(tsx.size());
         const int64_t base_g = static_cast<int64_t>(tg.size());
         auto put = [&](std::vector<TileItem>& v, size_t* o, int* n, size_t* oo, int* np) {
@@ -668,31 +695,29 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         put(tsx, &g.t_sx_off, &g.n_sx, &g.o_sx_off, &g.p_sx);
         put(tsa, &g.t_sa_off, &g.n_sa, &g.o_sa_off, &g.p_sa);
         put(tg, &g.t_g_off, &g.n_g, &g.o_g_off, &g.p_g);
-        g.fuse_epoch = 0;
-        // Fusing pays where the GEMM's last wave is a large share of the
-        // launch (few tiles per pair, as for one large matrix); with many
-        // short tiles per pair the extra store completion per GEMM tile in
-        // the epilogue costs more (measured: 4096^2 -1.8%, a 388-matrix
-        // group +3.6%)
-        g.fused_ok = h->pair && h->fuse_stages && g.shards == 1 && !tg0.empty() &&
-                     tg0.size() <= size_t(FUSE_MAX_TILES_PER_PAIR) *
-                                       size_t(std::max(1, h->max_pairs));
-        if (g.fused_ok) {
+        g.ep_x = g.ep_a = g.ep_b = 0;
+        g.chain_ok = chain_eligible(h, g.shards, static_cast<int64_t>(tg0.size()));
+        if (g.chain_ok) {
             const int pairs = std::max(
-                1, std::min(h->max_pairs, static_cast<int>(tg0.size() + tsx0.size())));
-            std::vector<TileItem> vf;
-            std::vector<int32_t> offs;
-            lpt_schedule_fused(tg0, tsx0, pairs, &vf, &offs);
+                1, std::min(h->max_pairs,
+                            static_cast<int>(tg0.size() + tsx0.size() + tsa0.size())));
+            std::vector<TileItem> vc;
+            std::vector<int32_t> offs, ends;
+            lpt_schedule_chain(tsx0, tsa0, tg0, pairs, &vc, &offs, &ends);
             off = align_up(off, 256);
-            g.o_f_off = off;
-            g.p_f = pairs;
+            g.o_c_off = off;
+            g.p_c = pairs;
             std::memcpy(meta.data() + off, offs.data(), offs.size() * sizeof(int32_t));
             off += offs.size() * sizeof(int32_t);
             off = align_up(off, 256);
-            g.t_f_off = off;
-            g.n_f = static_cast<int>(vf.size());
-            std::memcpy(meta.data() + off, vf.data(), vf.size() * sizeof(TileItem));
-            off += vf.size() * sizeof(TileItem);
+            g.e_c_off = off;
+            std::memcpy(meta.data() + off, ends.data(), ends.size() * sizeof(int32_t));
+            off += ends.size() * sizeof(int32_t);
+            off = align_up(off, 256);
+            g.t_c_off = off;
+            g.n_c = static_cast<int>(vc.size());
+            std::memcpy(meta.data() + off, vc.data(), vc.size() * sizeof(TileItem));
+            off += vc.size() * sizeof(TileItem);
         }
         P.syrk_tiles += base_sx;
         P.gemm_tiles += base_g;
@@ -923,12 +948,12 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         ew.eps = NORM_EPS;
         const int ew_grid = static_cast<int>(std::min<int64_t>(g.ew_tiles, ew_grid_cap));
         const bool fused = h->pair && h->fuse;
-        if (g.fused_ok && ns_steps > 1 &&
-            g.rc_step * (g.fuse_epoch + ns_steps) > h->rc_limit) {
+        if (g.chain_ok &&
+            g.rc_step * (std::max({g.ep_x, g.ep_a, g.ep_b}) + ns_steps) > h->rc_limit) {
             // the targets would near int32 overflow: start the counters over
             const cudaError_t ce = cudaMemsetAsync(ws + g.rc_off, 0, g.rc_bytes, h->stream);
             if (ce != cudaSuccess) return cuda_fail(h, ce, "row counter reset");
-            g.fuse_epoch = 0;
+            g.ep_x = g.ep_a = g.ep_b = 0;
         }
         ew.write_x = fused ? 1 : 0;
         cudaError_t e;
@@ -957,10 +982,35 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         L.ew = ew.units;
         L.lr = lr;
         int cur = 0;
-        // GEMM(s) and the first product of s + 1 share a launch (all but the
-        // last iteration); that first product then does not run on its own
-        const bool fuse_it = g.fused_ok && ns_steps > 1;
-        for (int s = 0; s < ns_steps; ++s) {
+        // chained groups: one launch holds every product of iterations
+        // 1 .. ns_steps but the last X update, which then runs alone
+        const bool chain = g.chain_ok;
+        if (chain) {
+            L.src = 0;
+            L.first = fused ? 1 : 0;
+            L.last = 0;
+            L.tiles = reinterpret_cast<const TileItem*>(ws + g.t_c_off);
+            L.num_tiles = g.n_c;
+            L.pair_off = reinterpret_cast<const int32_t*>(ws + g.o_c_off);
+            L.pair_end_last = reinterpret_cast<const int32_t*>(ws + g.e_c_off);
+            L.iters = ns_steps;
+            L.ep_x = static_cast<int32_t>(g.ep_x);
+            L.ep_a = static_cast<int32_t>(g.ep_a);
+            L.ep_b = static_cast<int32_t>(g.ep_b);
+            L.shards = 1;
+            if (!begin(ST_CHAIN)) return fail(h, MUON_ERR_CUDA, "event create");
+            e = launch_ns_pair(OP_CHAIN, L, g.p_c, h->stages, h->stream);
+            end();
+            if (e != cudaSuccess) {
+                P.valid = false;              // rebuilt (and re-uploaded) next step
+                return cuda_fail(h, e, "chained launch");
+            }
+            g.ep_x += ns_steps - 1;
+            g.ep_a += ns_steps;
+            g.ep_b += ns_steps;
+            cur = (ns_steps - 1) & 1;
+        }
+        for (int s = chain ? ns_steps - 1 : 0; s < ns_steps; ++s) {
             L.src = cur;
             L.first = (fused && s == 0) ? 1 : 0;
             const bool last = s == ns_steps - 1;
@@ -970,20 +1020,19 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
             struct Q { NsOp op; size_t off; int n; int st; size_t oo; int np; };
             Q seq[3];
             int nq = 0;
-            if (!(fuse_it && s > 0))
+            if (!chain) {
                 seq[nq++] = {OP_SYRK_X, g.t_sx_off, g.n_sx, ST_SYRK1, g.o_sx_off, g.p_sx};
-            seq[nq++] = {OP_SYRK_A, g.t_sa_off, g.n_sa, ST_SYRK2, g.o_sa_off, g.p_sa};
-            if (fuse_it && !last)
-                seq[nq++] = {OP_FUSED, g.t_f_off, g.n_f, ST_FUSED, g.o_f_off, g.p_f};
-            else
-                seq[nq++] = {OP_GEMM_BX, g.t_g_off, g.n_g, ST_GEMM, g.o_g_off, g.p_g};
+                seq[nq++] = {OP_SYRK_A, g.t_sa_off, g.n_sa, ST_SYRK2, g.o_sa_off, g.p_sa};
+            }
+            seq[nq++] = {OP_GEMM_BX, g.t_g_off, g.n_g, ST_GEMM, g.o_g_off, g.p_g};
             for (int qi = 0; qi < nq; ++qi) {
                 const Q& q = seq[qi];
                 L.tiles = reinterpret_cast<const TileItem*>(ws + q.off);
                 L.num_tiles = q.n;
                 L.pair_off = h->pair ? reinterpret_cast<const int32_t*>(ws + q.oo) : nullptr;
+                L.pair_end_last = nullptr;
+                L.iters = 1;
                 L.shards = g.shards;
-                L.fuse_epoch = (q.op == OP_FUSED) ? static_cast<int32_t>(++g.fuse_epoch) : 0;
                 if (!begin(q.st)) return fail(h, MUON_ERR_CUDA, "event create");
                 if (h->pair && q.op == OP_GEMM_BX && L.last && upd_tma)
                     e = launch_ns_pair_update(L, q.np, h->stream);
@@ -1176,9 +1225,21 @@ int muon_get_plan_info(muon_handle h, int mode, int nb, muon_plan_info* out) {
     if (h->ws && h->ws_bytes >= min_b) {
         const size_t scratch = h->ws_bytes - align_up(HEADER_BYTES + meta_bound(units), 1024);
         make_groups(units, scratch, &groups);
-        out->groups = static_cast<int64_t>(groups.size());
     } else {
-        out->groups = 1;
+        GroupDesc g;
+        g.u0 = 0;
+        g.u1 = static_cast<int>(units.size());
+        groups.push_back(g);
+    }
+    out->groups = static_cast<int64_t>(groups.size());
+    for (const GroupDesc& g : groups) {
+        int64_t gemm = 0;
+        for (int i = g.u0; i < g.u1; ++i) {
+            int64_t s, gg, us, ex;
+            unit_tiles(units[i], h->pair, &s, &gg, &us, &ex);
+            gemm += gg;
+        }
+        if (chain_eligible(h, units[g.u0].shards, gemm)) ++out->chained_groups;
     }
     return MUON_OK;
 }

@@ -68,10 +68,12 @@ struct alignas(128) NsUnit {
     __nv_bfloat16* x[2];
     __nv_bfloat16* a;
     __nv_bfloat16* b;
-    // GEMM tiles of a launch that also holds the next iteration's first
-    // product: per 256-row block of X', the epilogue warps that finished
-    // storing their part (PAIR_EPI_WARPS per tile)
-    int32_t* row_done;
+    // Chained launches: per 256-row block, the epilogue warps that finished
+    // storing their part of a tile touching the block (PAIR_EPI_WARPS per
+    // tile and block): row_cnt[r] for X (X update tiles of row r), then
+    // row_cnt[T + r] for A and row_cnt[2T + r] for B (product tiles (r, j)
+    // and their mirrors), T = 256-row blocks of m.  They only grow.
+    int32_t* row_cnt;
     int32_t m, n, ld_x, ld_mm;
 };
 
@@ -86,17 +88,25 @@ struct TileItem {
     int32_t flags;           // TILE_*
 };
 
-// In a launch of OP_FUSED, a tile of the next iteration's first product
-// (A' = X' X'^T); the other tiles are this iteration's GEMM (X' = a X + B X).
-constexpr int TILE_NEXT_SYRK = 1;
-// epilogue warps of a CTA pair (each counts once per finished GEMM tile)
+// In a launch of OP_CHAIN the low two bits of TileItem::flags give the
+// tile's operation (OP_SYRK_X, OP_SYRK_A or OP_GEMM_BX).
+constexpr int TILE_OP_MASK = 3;
+// epilogue warps of a CTA pair (each counts once per finished tile and row)
 constexpr int PAIR_EPI_WARPS = 16;
 
-// OP_FUSED: one launch with iteration s's GEMM and iteration s+1's first
-// product.  A first-product tile starts once the two 256-row blocks of X' it
-// reads are complete (row counters of the GEMM tiles); every CTA pair runs
-// all its GEMM tiles first, so no wait depends on a tile that waits.
-enum NsOp { OP_SYRK_X = 0, OP_SYRK_A = 1, OP_GEMM_BX = 2, OP_FUSED = 3 };
+// OP_CHAIN: iterations 1 .. iters of Newton-Schulz in one launch, every
+// product but the last X update.  Each pair walks its one-iteration list
+// (first-product tiles, then second-product tiles, then X-update tiles)
+// once per iteration, the last time without the X-update tiles.  A tile
+// starts once the row blocks it reads are complete (row counters):
+//   first product (s > 1): X rows ti, tj, written by the X update of s - 1;
+//   second product:        A rows ti, tj, written by the first product of s;
+//   X update:              B row ti, written by the second product of s.
+// The waits also order the overwrites: every tile that still reads the
+// buffer a tile writes (A, B, the other X) is done before those rows
+// complete.  Each pair's walk is in stage order and a tile waits only on
+// earlier stages, so no wait depends on a tile that waits on it.
+enum NsOp { OP_SYRK_X = 0, OP_SYRK_A = 1, OP_GEMM_BX = 2, OP_CHAIN = 3 };
 
 struct NsLaunch {
     const NsUnit* units;
@@ -119,10 +129,15 @@ struct NsLaunch {
     // (a cost-balanced schedule built by the planner); nullptr = pair p takes
     // tiles p, p + pairs, ...
     const int32_t* pair_off;
-    // OP_FUSED: the launch's number since the plan was built (from 1); a row
-    // block of X' is complete when its counter reaches
-    // PAIR_EPI_WARPS * (GEMM tiles per row) * fuse_epoch
-    int32_t fuse_epoch;
+    // OP_CHAIN: iterations in the launch; pair_end_last[p]: end of pair p's
+    // list without its X-update tiles (the last iteration's walk); ep_x,
+    // ep_a, ep_b: completed rounds of the X, A and B counters before the
+    // launch (a row of X is complete in iteration s once its counter
+    // reaches PAIR_EPI_WARPS * (X-update tiles per row) * (ep_x + s - 1),
+    // a row of A once PAIR_EPI_WARPS * T * (ep_a + s), B likewise).
+    int32_t iters;
+    const int32_t* pair_end_last;
+    int32_t ep_x, ep_a, ep_b;
     // Distributed mode, first product (CTA-pair kernels): the K range of
     // every tile is `shards` equal slices.  The pair runs them in turn, slice
     // 0 into accumulator 0 and each later slice into accumulator 1, which

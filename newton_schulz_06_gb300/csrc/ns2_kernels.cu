@@ -97,15 +97,68 @@ __device__ __forceinline__ void commit_pair_local(uint32_t bar) {
         : "memory");
 }
 
-// The operation of tile t in a launch of OP (per tile only for OP_FUSED).
+// The operation of tile t in a launch of OP (per tile only for OP_CHAIN).
 template <int OP>
 __device__ __forceinline__ int tile_op(const TileItem& t) {
-    if (OP != OP_FUSED) return OP;
-    return (t.flags & TILE_NEXT_SYRK) ? OP_SYRK_X : OP_GEMM_BX;
+    if (OP != OP_CHAIN) return OP;
+    return t.flags & TILE_OP_MASK;
 }
 
-// GEMM tiles per 256-row block of X' (= column tiles of the unit).
+// The X buffer holding the iterate that a tile of iteration s reads (s
+// counts from 1 within a chained launch; other launches run one iteration).
+template <int OP>
+__device__ __forceinline__ int tile_src(const NsLaunch& p, int s) {
+    return OP == OP_CHAIN ? (p.src ^ ((s - 1) & 1)) : p.src;
+}
+
+// X-update tiles per 256-row block of X' (= column tiles of the unit).
 __device__ __forceinline__ int row_tiles(const NsUnit& U) { return (U.n + 255) / 256; }
+// 256-row blocks of m (= tiles (r, j) and mirrors touching a row of A or B).
+__device__ __forceinline__ int row_blocks(const NsUnit& U) { return (U.m + 255) / 256; }
+
+// The row counters a tile of a chained launch waits on before it reads, and
+// their target (c0 == c1 for an X-update tile); false: it waits on nothing.
+struct TileDeps {
+    const int32_t* c0;
+    const int32_t* c1;
+    int32_t target;
+};
+template <int OP>
+__device__ __forceinline__ bool tile_deps(const NsLaunch& p, const NsUnit& U, const TileItem& t,
+                                          int op, int s, TileDeps* d) {
+    if (OP != OP_CHAIN) return false;
+    const int T = row_blocks(U);
+    if (op == OP_SYRK_X) {
+        if (s == 1) return false;                // X from before the launch
+        d->c0 = U.row_cnt + t.ti;
+        d->c1 = U.row_cnt + t.tj;
+        d->target = PAIR_EPI_WARPS * row_tiles(U) * (p.ep_x + s - 1);
+    } else if (op == OP_SYRK_A) {
+        d->c0 = U.row_cnt + T + t.ti;
+        d->c1 = U.row_cnt + T + t.tj;
+        d->target = PAIR_EPI_WARPS * T * (p.ep_a + s);
+    } else {
+        d->c0 = d->c1 = U.row_cnt + 2 * T + t.ti;
+        d->target = PAIR_EPI_WARPS * T * (p.ep_b + s);
+    }
+    return true;
+}
+
+// After a tile of a chained launch: this warp's stores of the tile are
+// complete; count them for the rows the tile wrote (an X-update tile: X row
+// ti; a product tile: row ti of A or B and, through the mirror, row tj).
+__device__ __forceinline__ void release_rows(const NsUnit& U, const TileItem& t, int op) {
+    bulk_wait_all0();
+    fence_proxy_async_global();
+    const int T = row_blocks(U);
+    if (op == OP_GEMM_BX) {
+        count_release(U.row_cnt + t.ti);
+    } else {
+        int32_t* c = U.row_cnt + (op == OP_SYRK_X ? T : 2 * T);
+        count_release(c + t.ti);
+        if (t.tj != t.ti) count_release(c + t.tj);
+    }
+}
 
 // Tile-constant fields of a unit, copied into registers once per tile (the
 // kernels store through pointers the compiler cannot tell apart from the
@@ -130,20 +183,21 @@ struct EpiUnit {
     float step;
 };
 
-// op: the tile's operation (OP itself unless OP == OP_FUSED).
-template <int OP>
-__device__ __forceinline__ EpiUnit load_epi_unit(const NsLaunch& p, int unit, int op) {
+// op: the tile's operation (OP itself unless OP == OP_CHAIN); src: the X
+// buffer it reads; last: the update is folded into this X update.
+__device__ __forceinline__ EpiUnit load_epi_unit(const NsLaunch& p, int unit, int op, int src,
+                                                 bool last) {
     const NsUnit* U = p.units + unit;
     EpiUnit e;
-    e.te_in = (op == OP_GEMM_BX) ? &U->te_x[p.src] : &U->te_a;
-    e.te_out = (op == OP_SYRK_X) ? &U->te_a : (op == OP_SYRK_A) ? &U->te_b : &U->te_x[p.src ^ 1];
+    e.te_in = (op == OP_GEMM_BX) ? &U->te_x[src] : &U->te_a;
+    e.te_out = (op == OP_SYRK_X) ? &U->te_a : (op == OP_SYRK_A) ? &U->te_b : &U->te_x[src ^ 1];
     e.te_w = &U->te_w;
     e.m = U->m;
     e.n = U->n;
     e.ld_x = U->ld_x;
     e.ld_mm = U->ld_mm;
-    e.xin = U->x[p.src];
-    e.xout = U->x[p.src ^ 1];
+    e.xin = U->x[src];
+    e.xout = U->x[src ^ 1];
     e.ain = U->a;
     e.out = (op == OP_SYRK_X) ? U->a : U->b;
     e.w = nullptr;
@@ -152,7 +206,7 @@ __device__ __forceinline__ EpiUnit load_epi_unit(const NsLaunch& p, int unit, in
     e.ld_w = e.ld_dbg = 0;
     e.w_f32 = e.vec16 = e.transposed = 0;
     e.step = 0.f;
-    if (op == OP_GEMM_BX && p.last) {
+    if (op == OP_GEMM_BX && last) {
         const EwUnit* E = p.ew + unit;
         e.w = E->w;
         e.w_dbg = E->w_dbg;
@@ -378,6 +432,10 @@ struct InPlan {
     int r0w, col0;               // first row, first column of the warp's part
     int n;                       // needed blocks
     int uses_in;                 // the tile reads input blocks
+    // chained launches: may its input blocks be loaded (1), not known yet
+    // (0: the rows they come from are tested once, then waited for), or
+    // tested and not complete (-1: the blocks wait until the tile starts)
+    int ready;
     uint32_t order;              // their column-block indices, 2 bits each
     __device__ __forceinline__ int block(int k) const {
         return static_cast<int>((order >> (2 * k)) & 3u);
@@ -385,15 +443,16 @@ struct InPlan {
 };
 
 template <int OP>
-__device__ __forceinline__ InPlan plan_blocks(const NsLaunch& p, const TileItem& t,
+__device__ __forceinline__ InPlan plan_blocks(const NsLaunch& p, const TileItem& t, int s,
                                               uint32_t rank, int lg, int half) {
     const NsUnit* U = p.units + t.unit;
     const int op = tile_op<OP>(t);
     InPlan q;
-    q.te_in = (op == OP_GEMM_BX) ? &U->te_x[p.src] : &U->te_a;
+    q.te_in = (op == OP_GEMM_BX) ? &U->te_x[tile_src<OP>(p, s)] : &U->te_a;
     q.te_w = &U->te_w;
-    q.transposed = (op == OP_GEMM_BX && p.last) ? p.ew[t.unit].transposed : 0;
+    q.transposed = (OP != OP_CHAIN && op == OP_GEMM_BX && p.last) ? p.ew[t.unit].transposed : 0;
     q.uses_in = op != OP_SYRK_X;
+    q.ready = (OP == OP_CHAIN && q.uses_in) ? 0 : 1;
     q.r0w = t.ti * 256 + static_cast<int>(rank) * P_HALF + lg * 32;
     q.col0 = t.tj * 256 + half * 128;
     const int m = U->m;
@@ -490,6 +549,39 @@ __device__ __forceinline__ TileRange tile_range(const NsLaunch& p, int pair, int
     return r;
 }
 
+// A pair's walk over its tiles: the range once, or in a chained launch once
+// per iteration s = 1 .. iters, the last time up to pair_end_last.
+template <int OP>
+struct TileCursor {
+    int it, end, step, s;
+    int begin, end_all, end_last, iters;
+    __device__ __forceinline__ bool valid() const { return it < end; }
+    __device__ __forceinline__ void next() {
+        it += step;
+        if (OP == OP_CHAIN && it >= end && s < iters) {
+            ++s;
+            it = begin;
+            end = (s == iters) ? end_last : end_all;
+        }
+    }
+};
+template <int OP>
+__device__ __forceinline__ TileCursor<OP> tile_cursor(const NsLaunch& p, int pair, int npairs) {
+    const TileRange r = tile_range(p, pair, npairs);
+    TileCursor<OP> c;
+    c.it = c.begin = r.begin;
+    c.end_all = c.end_last = r.end;
+    c.step = r.step;
+    c.s = 1;
+    c.iters = 1;
+    if (OP == OP_CHAIN && r.begin < r.end) {
+        c.iters = p.iters;
+        c.end_last = p.pair_end_last[pair];
+    }
+    c.end = (c.iters == 1) ? c.end_last : c.end_all;
+    return c;
+}
+
 // SL: distributed mode's first product (K in p.shards slices, OP_SYRK_X).
 template <int OP, int P_STAGES, int FW, int SL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
@@ -562,26 +654,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             int issued[P_STAGES];
             for (int s = 0; s < P_STAGES; ++s) issued[s] = 0;
             bool ok = true;
-            const TileRange tr = tile_range(p, pair, npairs);
+            TileCursor<OP> cur = tile_cursor<OP>(p, pair, npairs);
             // the next tile's record is fetched while this tile streams
-            TileItem t_next = tr.begin < tr.end ? p.tiles[tr.begin] : TileItem{};
-            for (int it = tr.begin; ok && it < tr.end; it += tr.step) {
+            TileItem t_next = cur.valid() ? p.tiles[cur.it] : TileItem{};
+            int s_next = cur.s;
+            while (ok && cur.valid()) {
                 const TileItem t = t_next;
-                if (it + tr.step < tr.end) t_next = p.tiles[it + tr.step];
+                const int s_it = s_next;
+                cur.next();
+                if (cur.valid()) {
+                    t_next = p.tiles[cur.it];
+                    s_next = cur.s;
+                }
                 const NsUnit* U = p.units + t.unit;
                 const int op = tile_op<OP>(t);
-                // in a fused launch the first-product tiles read X' (the
-                // other buffer), once the GEMM tiles wrote both row blocks
-                const bool next_syrk = (OP == OP_FUSED) && op == OP_SYRK_X;
+                const int src = tile_src<OP>(p, s_it);
                 const void* tmA;
                 const void* tmB;
-                if (op == OP_SYRK_X) { tmA = &U->tm_x[next_syrk ? p.src ^ 1 : p.src]; tmB = tmA; }
+                if (op == OP_SYRK_X) { tmA = &U->tm_x[src]; tmB = tmA; }
                 else if (op == OP_SYRK_A) { tmA = &U->tm_a; tmB = tmA; }
-                else { tmA = &U->tm_b; tmB = &U->tm_x[p.src]; }
-                if (next_syrk) {
-                    const int32_t target = PAIR_EPI_WARPS * row_tiles(*U) * p.fuse_epoch;
-                    if (!wait_count(U->row_done + t.ti, target, abort_flag, p.err, limit) ||
-                        !wait_count(U->row_done + t.tj, target, abort_flag, p.err, limit)) {
+                else { tmA = &U->tm_b; tmB = &U->tm_x[src]; }
+                TileDeps d;
+                if (tile_deps<OP>(p, *U, t, op, s_it, &d)) {
+                    // the rows this tile reads are complete
+                    if (!wait_count(d.c0, d.target, abort_flag, p.err, limit) ||
+                        (d.c1 != d.c0 && !wait_count(d.c1, d.target, abort_flag, p.err, limit))) {
                         ok = false;
                         break;
                     }
@@ -644,11 +741,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             // B operand: MN-major for the GEMM (X), K-major otherwise
             const uint64_t b_desc_mn = smem_desc(smem_u32(sB), P_BOX, 1024);
             const uint64_t b_desc_k = smem_desc(smem_u32(sB), 16, 1024);
-            const TileRange tr = tile_range(p, pair, npairs);
-            TileItem t_next = tr.begin < tr.end ? p.tiles[tr.begin] : TileItem{};
-            for (int it = tr.begin; ok && it < tr.end; it += tr.step, ++local) {
+            TileCursor<OP> cur = tile_cursor<OP>(p, pair, npairs);
+            TileItem t_next = cur.valid() ? p.tiles[cur.it] : TileItem{};
+            for (; ok && cur.valid(); ++local) {
                 const TileItem t = t_next;
-                if (it + tr.step < tr.end) t_next = p.tiles[it + tr.step];
+                cur.next();
+                if (cur.valid()) t_next = p.tiles[cur.it];
                 const int op = tile_op<OP>(t);
                 const uint32_t idesc = instr_desc(256, t.n_len, op == OP_GEMM_BX ? 1 : 0);
                 const uint64_t b_desc0 = (op == OP_GEMM_BX) ? b_desc_mn : b_desc_k;
@@ -739,12 +837,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         tempty_leader[1] = map_to_rank(smem_u32(&tempty_bar[1]), 0);
         int local = 0;
         bool ok = true;
-        const TileRange tr = tile_range(p, pair, npairs);
-        TileItem t_next = tr.begin < tr.end ? p.tiles[tr.begin] : TileItem{};
+        TileCursor<OP> tc = tile_cursor<OP>(p, pair, npairs);
+        TileItem t_next = tc.valid() ? p.tiles[tc.it] : TileItem{};
+        int s_next = tc.s;
         // input blocks stream through the slots in tile order, across tile
         // boundaries: cur is this tile's plan, nxt the next tile's
         InPlan cur{}, nxt{};
-        if (tr.begin < tr.end) cur = plan_blocks<OP>(p, t_next, rank, lg, half);
+        if (tc.valid()) cur = plan_blocks<OP>(p, t_next, s_next, rank, lg, half);
         int cur_issued = 0, nxt_issued = 0;
         auto issue_from = [&](const InPlan& q, int k) {
             const uint32_t sl = in_seq % NS;
@@ -752,27 +851,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 issue_inputs<FW>(q, k, s_in + sl * p_in_blk<FW>(), smem_u32(&in_bar[NS * ew + sl]));
             ++in_seq;
         };
-        for (int it = tr.begin; ok && it < tr.end; it += tr.step, ++local) {
+        // chained launches: the rows a tile's input blocks come from are
+        // complete (lane 0 issues the loads: its acquire, then its proxy
+        // fence).  Blocking at a tile's start; a single test for the next
+        // tile, which must not wait while this one holds work others need.
+        auto rows_ready = [&](const TileItem& tt, int ss, bool block) -> bool {
+            TileDeps d;
+            const NsUnit& U = p.units[tt.unit];
+            int r = 1;
+            if (lane == 0 && tile_deps<OP>(p, U, tt, tile_op<OP>(tt), ss, &d)) {
+                if (block)
+                    r = wait_count(d.c0, d.target, abort_flag, p.err, limit) &&
+                        (d.c1 == d.c0 || wait_count(d.c1, d.target, abort_flag, p.err, limit));
+                else
+                    r = count_reached(d.c0, d.target) && count_reached(d.c1, d.target);
+                if (r) fence_proxy_async_global();
+            }
+            return __shfl_sync(0xffffffffu, r, 0) != 0;
+        };
+        while (ok && tc.valid()) {
             const TileItem t = t_next;
-            const bool has_next = it + tr.step < tr.end;
-            if (has_next) t_next = p.tiles[it + tr.step];
+            const int s_it = s_next;
+            tc.next();
+            const bool has_next = tc.valid();
+            if (has_next) {
+                t_next = p.tiles[tc.it];
+                s_next = tc.s;
+            }
+            if (OP == OP_CHAIN && cur.uses_in && cur.ready != 1) {
+                if (!rows_ready(t, s_it, true)) {
+                    ok = false;
+                    break;
+                }
+                cur.ready = 1;
+            }
             if (cur.uses_in)
                 while (cur_issued < cur.n && in_seq - in_use < static_cast<uint32_t>(NS))
                     issue_from(cur, cur_issued++);
             nxt.n = 0;
             nxt_issued = 0;
-            if (has_next) nxt = plan_blocks<OP>(p, t_next, rank, lg, half);
+            if (has_next) nxt = plan_blocks<OP>(p, t_next, s_next, rank, lg, half);
             const int op = tile_op<OP>(t);
             const bool uses_in = cur.uses_in;
-            const EpiUnit u = load_epi_unit<OP>(p, t.unit, op);
+            const EpiUnit u =
+                load_epi_unit(p, t.unit, op, tile_src<OP>(p, s_it), OP != OP_CHAIN && p.last);
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             const int r0w = cur.r0w;
             const int col0 = cur.col0;
             float scale = 1.f;
-            // iteration 1 scales by the norm; a fused launch's first-product
-            // tiles belong to the next iteration
-            if (p.first && op != OP_SYRK_A && !(OP == OP_FUSED && op == OP_SYRK_X)) {
+            // iteration 1 scales by the norm
+            if (p.first && op != OP_SYRK_A && s_it == 1) {
                 const float inv = p.inv_norm[t.unit];
                 scale = (op == OP_SYRK_X) ? inv * inv : inv;
             }
@@ -843,15 +972,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                     __syncwarp();      // every lane's reads of the slot are done
                     // refill the slot: this tile's next block, else the next
                     // tile's first
-                    if (cur_issued < cur.n) issue_from(cur, cur_issued++);
-                    else if (nxt.uses_in && nxt_issued < nxt.n) issue_from(nxt, nxt_issued++);
+                    if (cur_issued < cur.n) {
+                        issue_from(cur, cur_issued++);
+                    } else if (nxt.uses_in && nxt_issued < nxt.n) {
+                        if (OP == OP_CHAIN && nxt.ready == 0)
+                            nxt.ready = rows_ready(t_next, s_next, false) ? 1 : -1;
+                        if (OP != OP_CHAIN || nxt.ready == 1) issue_from(nxt, nxt_issued++);
+                    }
                     if (FW) continue;
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] *= scale;
                 }
                 if (op == OP_GEMM_BX) {
-                    if (p.last) {
+                    if (OP != OP_CHAIN && p.last) {     // a chain never holds the last
                         stage_free(lane);
                         gemm_update_block(u, r0w, gc0, lane, v, s_st + (st_seq & 1u) * P_BLK);
                     } else {
@@ -883,16 +1017,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 }
             }
             if (!__all_sync(0xffffffffu, ok)) break;
-            if (OP == OP_FUSED && op == OP_GEMM_BX) {
-                // this warp's part of row block ti of X' is in memory: count
-                // it for the first-product tiles waiting on the row
-                if (lane == 0) {
-                    bulk_wait_all0();
-                    fence_proxy_async_global();
-                    count_release(p.units[t.unit].row_done + t.ti);
-                }
-                __syncwarp();
-            }
             cur = nxt;
             cur_issued = nxt_issued;
             tc_fence_before();
@@ -904,7 +1028,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 } else {
                     mbar_arrive_cluster_relaxed(tempty_leader[acc]);
                 }
+                // chained launches: once this warp's stores of the tile are
+                // complete, count them for the rows they belong to
+                if (OP == OP_CHAIN) release_rows(p.units[t.unit], t, op);
             }
+            __syncwarp();
+            ++local;
         }
         // after an abort: let input loads in flight land before leaving
         for (uint32_t q = in_use; q != in_seq; ++q)
@@ -980,7 +1109,7 @@ cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, int stages,
         case OP_SYRK_X: return launch_pair_op<OP_SYRK_X>(p, pairs, stages, s);
         case OP_SYRK_A: return launch_pair_op<OP_SYRK_A>(p, pairs, stages, s);
         case OP_GEMM_BX: return launch_pair_op<OP_GEMM_BX>(p, pairs, stages, s);
-        case OP_FUSED: return launch_pair_op<OP_FUSED>(p, pairs, stages, s);
+        case OP_CHAIN: return launch_pair_st<OP_CHAIN, 5, 0>(p, pairs, s);
     }
     return cudaErrorInvalidValue;
 }

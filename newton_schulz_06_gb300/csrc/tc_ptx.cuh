@@ -118,6 +118,13 @@ __device__ __noinline__ bool wait_count(const int32_t* cnt, int32_t target,
     }
 }
 
+// One acquire load of a global counter: has it reached target?
+__device__ __forceinline__ bool count_reached(const int32_t* cnt, int32_t target) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    return v >= target;
+}
+
 // Adds 1 to a global counter with release semantics.
 __device__ __forceinline__ void count_release(int32_t* cnt) {
     asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(cnt) : "memory");

@@ -177,3 +177,19 @@ def test_distributed_mode_plan_and_validation(L):
     with pytest.raises(L.MuonError) as e:
         p.plan_info(L.MUON_DISTRIBUTED, 0)
     assert e.value.code == L.MUON_ERR_INVALID_ARG
+
+
+def test_chained_launch_only_for_few_large_matrices(L):
+    """One chained launch per step (every product but the last X update) is
+    planned where a group has at most 8 X-update tiles per CTA pair, in full
+    and blockwise mode; distributed mode and large groups keep one launch per
+    product."""
+    from newton_schulz_06_gb300.inputs import qwen3_30b_a3b_block_shapes
+    sq = _planner([(4096, 4096)])
+    assert sq.plan_info(L.MUON_FULL, 1)["chained_groups"] == 1
+    assert sq.plan_info(L.MUON_BLOCKWISE, 4)["chained_groups"] == 1
+    assert sq.plan_info(L.MUON_DISTRIBUTED, 4)["chained_groups"] == 0
+    # 76 pairs x 8 = 608 X-update tiles: 24 x 24 tiles of 256 chain, 25 x 25 not
+    assert _planner([(6144, 6144)]).plan_info()["chained_groups"] == 1
+    assert _planner([(6400, 6400)]).plan_info()["chained_groups"] == 0
+    assert _planner(qwen3_30b_a3b_block_shapes()).plan_info()["chained_groups"] == 0

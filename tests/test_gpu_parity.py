@@ -264,26 +264,46 @@ def test_layerwise_single_rank_is_the_grouped_step_bitexact():
 
 
 @pytest.mark.parametrize("ns_steps", [1, 2, 5])
-def test_fused_gemm_and_next_first_product_bitexact(ns_steps, monkeypatch):
-    """One launch holding iteration s's GEMM and iteration s+1's first
-    product (the latter waiting on row-block counters) computes every tile as
-    the separate launches do: identical bits, over two steps (the counters
-    carry across launches and steps)."""
+def test_chained_launch_bitexact(ns_steps, monkeypatch):
+    """One launch holding every product of the step but the last X update
+    (tiles waiting on row-block counters) computes every tile as the
+    separate launches do: identical bits, over two steps (the counters carry
+    across launches and steps)."""
     shapes = [(512, 768), (768, 2048), (300, 300), (2048, 640), (96, 1000)]
     trips = [case(r, c, 900 + i) for i, (r, c) in enumerate(shapes)]
     clones = [[t.clone() for t in tr] for tr in trips]
-    _, w1, o1, _ = gpu_step(trips, ns_steps=ns_steps, steps=2)
+    _, w1, o1, opt = gpu_step(trips, ns_steps=ns_steps, steps=2)
+    assert opt.plan_info()["chained_groups"] == 1
     monkeypatch.setenv("MUON_FUSE_STAGES", "0")
-    _, w2, o2, _ = gpu_step(clones, ns_steps=ns_steps, steps=2)
+    _, w2, o2, opt2 = gpu_step(clones, ns_steps=ns_steps, steps=2)
+    assert opt2.plan_info()["chained_groups"] == 0
     for i in range(len(shapes)):
         assert torch.equal(o1[i], o2[i]), shapes[i]
         assert torch.equal(trips[i][0], clones[i][0]), shapes[i]
 
 
-def test_fused_counters_zeroed_and_restarted_bitexact(monkeypatch):
-    """The fused launches' row counters only grow across steps; when a
+@pytest.mark.parametrize("rows,cols,ns_steps", [(200, 200, 1), (200, 200, 3),
+                                                (256, 1024, 2), (1000, 300, 5)])
+def test_chained_launch_small_matrix_matches_oracle(rows, cols, ns_steps, monkeypatch):
+    """A chain over a few tiles leaves most CTA pairs idle and gives some
+    pairs only X-update tiles (which they skip in the last iteration): same
+    bits as separate launches, within tolerance of the oracle."""
+    trip = case(rows, cols, 970)
+    clone = [t.clone() for t in trip]
+    inp, wexp, oexp, opt = gpu_step([trip], ns_steps=ns_steps)
+    assert opt.plan_info()["chained_groups"] == 1
+    ref = oracle_step(inp[0], ns_steps=ns_steps)
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref)
+    monkeypatch.setenv("MUON_FUSE_STAGES", "0")
+    _, _, o2, _ = gpu_step([clone], ns_steps=ns_steps)
+    assert torch.equal(oexp[0], o2[0])
+    assert torch.equal(trip[0], clone[0])
+
+
+def test_chain_counters_zeroed_and_restarted_bitexact(monkeypatch):
+    """The chained launches' row counters only grow across steps; when a
     step's targets would pass the limit the group's counters are zeroed and
-    the epochs start over.  With a limit of 1 that happens before every
+    the rounds start over.  With a limit of 1 that happens before every
     step: three steps give the same bits as counters that never restart."""
     shapes = [(1024, 1536), (640, 640)]
     trips = [case(r, c, 950 + i) for i, (r, c) in enumerate(shapes)]
