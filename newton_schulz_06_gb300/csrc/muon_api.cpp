@@ -125,6 +125,7 @@ struct muon_ctx {
     int stages = 5;            // pair mode: TMA pipeline depth (4 or 5)
     bool fuse_stages = true;   // pair mode: iterations chained in one launch where it pays
     int64_t rc_limit = int64_t(1) << 30;   // row-counter target at which they are zeroed
+    int chain_max_tiles = 8;   // X-update tiles per CTA pair up to which groups chain
     int max_pairs = 0;
 };
 
@@ -301,10 +302,10 @@ bool make_groups(const std::vector<UnitDesc>& units, size_t scratch,
 }
 
 int encode_map(muon_ctx* h, CUtensorMap* tm, void* base, int64_t inner,
-               int64_t outer, int64_t ld, uint32_t box = 64) {
+               int64_t outer, int64_t ld, uint32_t box = 64, uint32_t box_rows = 0) {
     cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
     cuuint64_t strides[1] = {cuuint64_t(ld) * 2};
-    cuuint32_t boxd[2] = {box, box};
+    cuuint32_t boxd[2] = {box, box_rows ? box_rows : box};
     cuuint32_t es[2] = {1, 1};
     // {64, 64} boxes: 128-byte rows, 128-byte swizzle (operand tiles);
     // {32, 32} boxes: 64-byte rows, 64-byte swizzle (epilogue blocks)
@@ -382,17 +383,16 @@ void lpt_schedule(std::vector<TileItem>* v, int P, bool allow_split,
     (*off)[P] = static_cast<int32_t>(v->size());
 }
 
-// Groups with at most this many X-update tiles per CTA pair chain their
-// iterations in one launch.  Chaining pays where stage tails are a large
-// share of a launch (few tiles per pair, as for one large matrix); with many
-// short tiles per pair the store completion the epilogue waits for before
-// counting a tile costs more (measured on a 388-matrix group: +3.6% for an
-// X update fused with the next first product).
-constexpr int FUSE_MAX_TILES_PER_PAIR = 8;
-
+// Groups with at most chain_max_tiles X-update tiles per CTA pair (8 unless
+// MUON_CHAIN_MAX_TILES says otherwise) chain their iterations in one launch.
+// Chaining pays where stage tails are a large share of a launch (few tiles
+// per pair, as for one large matrix); with many short tiles per pair the
+// store completion the epilogue waits for before counting a tile costs more
+// (measured on a 388-matrix group: +3.6% for an X update fused with the
+// next first product).
 bool chain_eligible(const muon_ctx* h, int shards, int64_t gemm_tiles) {
     return h->pair && h->fuse_stages && shards == 1 && gemm_tiles > 0 &&
-           gemm_tiles <= int64_t(FUSE_MAX_TILES_PER_PAIR) * std::max(1, h->max_pairs);
+           gemm_tiles <= int64_t(h->chain_max_tiles) * std::max(1, h->max_pairs);
 }
 
 // Schedule of a chained launch over P CTA pairs.  A list-scheduling
@@ -574,6 +574,10 @@ int build_plan(muon_ctx* h, int mode, int nb) {
             if ((rc = encode_map(h, &ns.tm_x[1], xb1, u.n, u.m, u.ld_x))) return rc;
             if ((rc = encode_map(h, &ns.tm_a, ab, u.m, u.m, u.ld_mm))) return rc;
             if ((rc = encode_map(h, &ns.tm_b, bb, u.m, u.m, u.ld_mm))) return rc;
+            if ((rc = encode_map(h, &ns.tk_x[0], xb0, u.n, u.m, u.ld_x, 64, 128))) return rc;
+            if ((rc = encode_map(h, &ns.tk_x[1], xb1, u.n, u.m, u.ld_x, 64, 128))) return rc;
+            if ((rc = encode_map(h, &ns.tk_a, ab, u.m, u.m, u.ld_mm, 64, 128))) return rc;
+            if ((rc = encode_map(h, &ns.tk_b, bb, u.m, u.m, u.ld_mm, 64, 128))) return rc;
             if ((rc = encode_map(h, &ns.te_x[0], xb0, u.n, u.m, u.ld_x, 32))) return rc;
             if ((rc = encode_map(h, &ns.te_x[1], xb1, u.n, u.m, u.ld_x, 32))) return rc;
             if ((rc = encode_map(h, &ns.te_a, ab, u.m, u.m, u.ld_mm, 32))) return rc;
@@ -807,6 +811,10 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     h->fuse_update = fuse_update;
     if (const char* pd = std::getenv("MUON_PDL")) set_programmatic_launch(std::string(pd) != "0");
     if (const char* fs = std::getenv("MUON_FUSE_STAGES")) h->fuse_stages = std::string(fs) != "0";
+    if (const char* cm = std::getenv("MUON_CHAIN_MAX_TILES")) {
+        const int v = std::atoi(cm);
+        if (v >= 0) h->chain_max_tiles = v;
+    }
     if (const char* rl = std::getenv("MUON_FUSE_COUNTER_LIMIT")) {
         const long long v = std::atoll(rl);
         if (v > 0 && v <= (1ll << 30)) h->rc_limit = v;

@@ -57,6 +57,11 @@ struct alignas(128) NsUnit {
     CUtensorMap tm_x[2];     // X ping/pong: dims {n, m}, box {64, 64}
     CUtensorMap tm_a;        // A = X X^T : dims {m, m}, box {64, 64}
     CUtensorMap tm_b;        // B = bA+cAA: dims {m, m}, box {64, 64}
+    // X, A and B with {64, 128} boxes: a CTA's 128 rows of a K-major
+    // operand in one load (CTA-pair kernels)
+    CUtensorMap tk_x[2];
+    CUtensorMap tk_a;
+    CUtensorMap tk_b;
     // The same four matrices with {32, 32} boxes and 64-byte swizzle, for the
     // epilogue's TMA loads (A, X) and TMA stores (A, B, X').
     CUtensorMap te_x[2];

@@ -45,6 +45,9 @@ constexpr int P_HALF = 128;                        // rows per CTA
 constexpr int P_A_BYTES = P_HALF * BK * 2;         // 16 KB
 constexpr int P_B_BYTES = P_HALF * BK * 2;         // 16 KB
 constexpr int P_BOX = 64 * 64 * 2;                 // one {64,64} box
+// K-major operands (A of every product, B of the symmetric ones) come in as
+// one {64, 128} box per CTA and k-block rather than two {64, 64} boxes
+constexpr bool P_WIDE_BOX = true;
 constexpr int P_TMEM_COLS = 512;
 constexpr int P_EPI_WARPS = 8;                     // 2 per TMEM lane group
 constexpr int P_THREADS = 64 + 32 * P_EPI_WARPS;
@@ -671,9 +674,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 const int src = tile_src<OP>(p, s_it);
                 const void* tmA;
                 const void* tmB;
-                if (op == OP_SYRK_X) { tmA = &U->tm_x[src]; tmB = tmA; }
-                else if (op == OP_SYRK_A) { tmA = &U->tm_a; tmB = tmA; }
-                else { tmA = &U->tm_b; tmB = &U->tm_x[src]; }
+                if (P_WIDE_BOX) {
+                    if (op == OP_SYRK_X) { tmA = &U->tk_x[src]; tmB = tmA; }
+                    else if (op == OP_SYRK_A) { tmA = &U->tk_a; tmB = tmA; }
+                    else { tmA = &U->tk_b; tmB = &U->tm_x[src]; }
+                } else {
+                    if (op == OP_SYRK_X) { tmA = &U->tm_x[src]; tmB = tmA; }
+                    else if (op == OP_SYRK_A) { tmA = &U->tm_a; tmB = tmA; }
+                    else { tmA = &U->tm_b; tmB = &U->tm_x[src]; }
+                }
                 TileDeps d;
                 if (tile_deps<OP>(p, *U, t, op, s_it, &d)) {
                     // the rows this tile reads are complete
@@ -690,6 +699,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 const int hb = t.n_len >> 1;
                 const int b0 = t.tj * 256 + t.n_off + static_cast<int>(rank) * hb;
                 const uint32_t tx_bytes = 2u * (P_A_BYTES + hb * BK * 2);
+                if (P_WIDE_BOX && op != OP_GEMM_BX && hb != 128) {
+                    // a K-major B half is one 128-row box: full-width tiles only
+                    atomicCAS(p.err, 0, DEV_ERR_BAD_TILE);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_try_wait(smem_u32(&empty_bar[stage]), phase ^ 1) &&
                         !wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag,
@@ -704,13 +720,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                     const uint32_t b_dst = smem_u32(sB + stage * P_B_BYTES);
                     const int k0 = kb * BK;
                     tma_load_2d_pair(a_dst, tmA, fb, k0, r0);
-                    tma_load_2d_pair(a_dst + P_BOX, tmA, fb, k0, r0 + 64);
+                    if (!P_WIDE_BOX) tma_load_2d_pair(a_dst + P_BOX, tmA, fb, k0, r0 + 64);
                     if (op == OP_GEMM_BX) {
                         tma_load_2d_pair(b_dst, tmB, fb, b0, k0);
                         if (hb > 64) tma_load_2d_pair(b_dst + P_BOX, tmB, fb, b0 + 64, k0);
                     } else {
                         tma_load_2d_pair(b_dst, tmB, fb, k0, b0);
-                        if (hb > 64) tma_load_2d_pair(b_dst + P_BOX, tmB, fb, k0, b0 + 64);
+                        if (!P_WIDE_BOX && hb > 64)
+                            tma_load_2d_pair(b_dst + P_BOX, tmB, fb, k0, b0 + 64);
                     }
                     issued[stage] = static_cast<int>(phase) + 1;
                     if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
