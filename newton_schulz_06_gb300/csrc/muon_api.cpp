@@ -14,6 +14,7 @@
 #include <algorithm>
 #include <cmath>
 #include <map>
+#include <tuple>
 #include <queue>
 #include <cstdio>
 #include <cstdlib>
@@ -48,7 +49,7 @@ struct UnitDesc {
     bool transposed = false;
     float scale = 1.f;
     size_t x_bytes = 0, mm_bytes = 0, buf_bytes = 0;
-    size_t row_bytes = 0;       // chained launches: X, A and B counters per 256-row block
+    size_t row_bytes = 0;       // chained launches: one counter per X, A and B tile
     int shards = 1;             // distributed mode: slices of the long side
     int64_t ew_tiles = 0;
     size_t need = 0;   // scratch bytes of this unit inside a group
@@ -237,7 +238,10 @@ int build_units(muon_ctx* h, int mode, int nb, std::vector<UnitDesc>* out) {
                             std::to_string(shards) + " slices of n=" + std::to_string(u.n) +
                                 " (parameter " + std::to_string(i) +
                                 ") are not equal multiples of 64");
-            u.row_bytes = align_up(size_t(ceil_div(u.m, 256)) * 3 * 4, 256);
+            {
+                const size_t T = size_t(ceil_div(u.m, 256)), RT = size_t(ceil_div(u.n, 256));
+                u.row_bytes = align_up((T * RT + 2 * T * T) * 4, 256);
+            }
             u.buf_bytes = 2 * u.x_bytes + 2 * u.mm_bytes;
             u.ew_tiles = ceil_div(u.m, EW_TILE) * ceil_div(u.n, EW_TILE);
             u.need = u.buf_bytes + size_t(u.ew_tiles) * 4 * EW_PARTIALS_PER_TILE + 4;
@@ -397,58 +401,73 @@ bool chain_eligible(const muon_ctx* h, int shards, int64_t gemm_tiles) {
 
 // Schedule of a chained launch over P CTA pairs.  A list-scheduling
 // simulation runs the stages in order (first product, second product, X
-// update; costs k-blocks x columns): within a stage the tiles go in the
-// order their rows become ready (X rows ti, tj; A rows ti, tj; B row ti),
-// each to the pair that is free first, starting once its rows are ready.
-// Three iterations are simulated; the last one's per-pair lists are the
-// template every iteration walks.  Each list is in stage order, so a
-// waiting tile only waits on tiles of earlier stages.  end_last[p]: the end
-// of pair p's list without its X-update tiles.
+// update; costs k-blocks x columns, K in 256-wide chunks).  Chunk c of a
+// tile is ready when the tiles it reads end: X tiles (ti, c), (tj, c) for
+// the first product, A tiles {ti, c}, {tj, c} for the second, B tile
+// {ti, c} for the X update.  Within a stage the tiles go in the order their
+// first chunk is ready (ties: the natural order, column-major for the X
+// update so that column 0 of X', which the next first products read first,
+// comes first), each to the pair that is free first; a tile runs its chunks
+// in order, each no earlier than it is ready.  Three iterations are
+// simulated; the last one's per-pair lists are the template every iteration
+// walks.  Each list is in stage order, so a waiting tile only waits on
+// tiles of earlier stages.  end_last[p]: the end of pair p's list without
+// its X-update tiles.
 void lpt_schedule_chain(const std::vector<TileItem>& sx, const std::vector<TileItem>& sa,
-                        const std::vector<TileItem>& gm, int P, std::vector<TileItem>* v,
+                        std::vector<TileItem> gm, int P, std::vector<TileItem>* v,
                         std::vector<int32_t>* off, std::vector<int32_t>* end_last) {
-    using Row = std::pair<int32_t, int>;
+    using Key = std::tuple<int32_t, int, int>;            // unit, tile row, tile column
     using Load = std::pair<int64_t, int>;
     std::priority_queue<Load, std::vector<Load>, std::greater<Load>> free_at;
     for (int p = 0; p < P; ++p) free_at.push({0, p});
-    std::map<Row, int64_t> x_ready, a_ready, b_ready;
+    std::map<Key, int64_t> x_end, a_end, b_end;
+    auto sym = [](int32_t u, int i, int j) { return Key{u, std::min(i, j), std::max(i, j)}; };
     std::vector<std::vector<TileItem>> lists(P);
     std::vector<int32_t> mid(P, 0);
-    // one stage: tiles by readiness, each to the pair free first; returns
-    // the time each written row completes
-    auto stage = [&](const std::vector<TileItem>& tiles, int op, std::map<Row, int64_t>& in,
-                     bool two_rows, bool mirrored, std::map<Row, int64_t>* out) {
-        auto ready = [&](const TileItem& t) {
-            const int64_t r0 = in[{t.unit, t.ti}];
-            return two_rows ? std::max(r0, in[{t.unit, t.tj}]) : r0;
-        };
+    // ready time of chunk c of tile t of stage op
+    auto chunk_ready = [&](const TileItem& t, int op, int c) -> int64_t {
+        if (op == OP_SYRK_X) {
+            auto e0 = x_end.find(Key{t.unit, t.ti, c}), e1 = x_end.find(Key{t.unit, t.tj, c});
+            return std::max(e0 == x_end.end() ? 0 : e0->second,
+                            e1 == x_end.end() ? 0 : e1->second);
+        }
+        if (op == OP_SYRK_A) return std::max(a_end[sym(t.unit, t.ti, c)], a_end[sym(t.unit, t.tj, c)]);
+        return b_end[sym(t.unit, t.ti, c)];
+    };
+    auto stage = [&](const std::vector<TileItem>& tiles, int op, std::map<Key, int64_t>* out) {
+        std::vector<int64_t> r0(tiles.size());
+        for (size_t i = 0; i < tiles.size(); ++i) r0[i] = chunk_ready(tiles[i], op, 0);
         std::vector<size_t> order(tiles.size());
         for (size_t i = 0; i < order.size(); ++i) order[i] = i;
         std::stable_sort(order.begin(), order.end(),
-                         [&](size_t a, size_t b) { return ready(tiles[a]) < ready(tiles[b]); });
-        out->clear();
+                         [&](size_t a, size_t b) { return r0[a] < r0[b]; });
+        std::map<Key, int64_t> ends;
         for (size_t i : order) {
             TileItem t = tiles[i];
             const Load l = free_at.top();
             free_at.pop();
-            const int64_t end = std::max(l.first, ready(t)) + int64_t(t.k_blocks) * t.n_len;
-            free_at.push({end, l.second});
+            const int nch = static_cast<int>(ceil_div(t.k_blocks, 4));
+            const int64_t per = int64_t(t.k_blocks) * t.n_len / std::max(1, nch);
+            int64_t now = l.first;
+            for (int c = 0; c < nch; ++c) now = std::max(now, chunk_ready(t, op, c)) + per;
+            free_at.push({now, l.second});
             t.flags = (t.flags & ~TILE_OP_MASK) | op;
             lists[l.second].push_back(t);
-            int64_t& e0 = (*out)[{t.unit, t.ti}];
-            e0 = std::max(e0, end);
-            if (mirrored) {
-                int64_t& e1 = (*out)[{t.unit, t.tj}];
-                e1 = std::max(e1, end);
-            }
+            ends[op == OP_GEMM_BX ? Key{t.unit, t.ti, t.tj} : sym(t.unit, t.ti, t.tj)] = now;
         }
+        *out = std::move(ends);
     };
+    // the X update's natural order: column-major
+    std::stable_sort(gm.begin(), gm.end(), [](const TileItem& a, const TileItem& b) {
+        return a.unit != b.unit ? a.unit < b.unit : a.tj != b.tj ? a.tj < b.tj : a.ti < b.ti;
+    });
     for (int iter = 0; iter < 3; ++iter) {
         for (auto& l : lists) l.clear();
-        stage(sx, OP_SYRK_X, x_ready, true, true, &a_ready);
-        stage(sa, OP_SYRK_A, a_ready, true, true, &b_ready);
+        if (iter == 0) x_end.clear();        // X from before the launch
+        stage(sx, OP_SYRK_X, &a_end);
+        stage(sa, OP_SYRK_A, &b_end);
         for (int p = 0; p < P; ++p) mid[p] = static_cast<int32_t>(lists[p].size());
-        stage(gm, OP_GEMM_BX, b_ready, false, false, &x_ready);
+        stage(gm, OP_GEMM_BX, &x_end);
     }
     v->clear();
     off->assign(P + 1, 0);
@@ -506,13 +525,8 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         // row-block counters of fused launches, zero in the uploaded image
         off = align_up(off, 256);
         g.rc_off = off;
-        g.rc_step = 0;
-        for (int i = g.u0; i < g.u1; ++i) {
-            off += P.units[i].row_bytes;
-            // n >= m: X rows take the most per round
-            g.rc_step = std::max<int64_t>(g.rc_step,
-                                          int64_t(PAIR_EPI_WARPS) * ceil_div(P.units[i].n, 256));
-        }
+        g.rc_step = PAIR_EPI_WARPS;             // every tile counter, per round
+        for (int i = g.u0; i < g.u1; ++i) off += P.units[i].row_bytes;
         g.rc_bytes = off - g.rc_off;
         size_t rc_next = g.rc_off;
         std::vector<TileItem> tsx, tsa, tg;

@@ -73,11 +73,12 @@ struct alignas(128) NsUnit {
     __nv_bfloat16* x[2];
     __nv_bfloat16* a;
     __nv_bfloat16* b;
-    // Chained launches: per 256-row block, the epilogue warps that finished
-    // storing their part of a tile touching the block (PAIR_EPI_WARPS per
-    // tile and block): row_cnt[r] for X (X update tiles of row r), then
-    // row_cnt[T + r] for A and row_cnt[2T + r] for B (product tiles (r, j)
-    // and their mirrors), T = 256-row blocks of m.  They only grow.
+    // Chained launches: per 256 x 256 output tile, the epilogue warps that
+    // finished storing their part of it (PAIR_EPI_WARPS per tile and round):
+    // X tiles (ti, cj) at row_cnt[ti * RT + cj], then A tiles (i <= j) at
+    // row_cnt[T * RT + i * T + j] and B tiles at row_cnt[T * RT + T * T +
+    // i * T + j]; T = 256-row blocks of m, RT = 256-column blocks of n.
+    // They only grow.
     int32_t* row_cnt;
     int32_t m, n, ld_x, ld_mm;
 };
@@ -102,15 +103,17 @@ constexpr int PAIR_EPI_WARPS = 16;
 // OP_CHAIN: iterations 1 .. iters of Newton-Schulz in one launch, every
 // product but the last X update.  Each pair walks its one-iteration list
 // (first-product tiles, then second-product tiles, then X-update tiles)
-// once per iteration, the last time without the X-update tiles.  A tile
-// starts once the row blocks it reads are complete (row counters):
-//   first product (s > 1): X rows ti, tj, written by the X update of s - 1;
-//   second product:        A rows ti, tj, written by the first product of s;
-//   X update:              B row ti, written by the second product of s.
+// once per iteration, the last time without the X-update tiles.  The K
+// range of a tile comes in 256-wide chunks; chunk c is loaded once the
+// tiles it reads are complete (tile counters):
+//   first product (s > 1): X tiles (ti, c), (tj, c), from the X update of s-1;
+//   second product:        A tiles {ti, c}, {tj, c}, from the first product of s;
+//   X update:              B tile {ti, c}, from the second product of s (which
+//                          implies X row c of iteration s is complete).
 // The waits also order the overwrites: every tile that still reads the
-// buffer a tile writes (A, B, the other X) is done before those rows
-// complete.  Each pair's walk is in stage order and a tile waits only on
-// earlier stages, so no wait depends on a tile that waits on it.
+// buffer a tile writes (A, B, the other X) is done before the tile's first
+// chunk may load.  Each pair's walk is in stage order and a tile waits only
+// on earlier stages, so no wait depends on a tile that waits on it.
 enum NsOp { OP_SYRK_X = 0, OP_SYRK_A = 1, OP_GEMM_BX = 2, OP_CHAIN = 3 };
 
 struct NsLaunch {
@@ -137,9 +140,9 @@ struct NsLaunch {
     // OP_CHAIN: iterations in the launch; pair_end_last[p]: end of pair p's
     // list without its X-update tiles (the last iteration's walk); ep_x,
     // ep_a, ep_b: completed rounds of the X, A and B counters before the
-    // launch (a row of X is complete in iteration s once its counter
-    // reaches PAIR_EPI_WARPS * (X-update tiles per row) * (ep_x + s - 1),
-    // a row of A once PAIR_EPI_WARPS * T * (ep_a + s), B likewise).
+    // launch (an X tile read in iteration s is complete once its counter
+    // reaches PAIR_EPI_WARPS * (ep_x + s - 1), an A tile once
+    // PAIR_EPI_WARPS * (ep_a + s), a B tile once PAIR_EPI_WARPS * (ep_b + s)).
     int32_t iters;
     const int32_t* pair_end_last;
     int32_t ep_x, ep_a, ep_b;

@@ -51,6 +51,10 @@ constexpr bool P_WIDE_BOX = true;
 constexpr int P_TMEM_COLS = 512;
 constexpr int P_EPI_WARPS = 8;                     // 2 per TMEM lane group
 constexpr int P_THREADS = 64 + 32 * P_EPI_WARPS;
+// chained launches add one warp that watches the tile counters
+template <int OP> __host__ __device__ constexpr int p_threads() {
+    return P_THREADS + (OP == OP_CHAIN ? 32 : 0);
+}
 constexpr int P_BLK = 32 * 32 * 2;                 // one 32x32 bf16 block
 // Per epilogue warp: input slots (an X or A block, plus a W block when the
 // update is folded into the last GEMM) and two staging blocks, so a block is
@@ -114,53 +118,100 @@ __device__ __forceinline__ int tile_src(const NsLaunch& p, int s) {
     return OP == OP_CHAIN ? (p.src ^ ((s - 1) & 1)) : p.src;
 }
 
-// X-update tiles per 256-row block of X' (= column tiles of the unit).
+// 256-column blocks of n (X-update tiles per 256-row block of X').
 __device__ __forceinline__ int row_tiles(const NsUnit& U) { return (U.n + 255) / 256; }
-// 256-row blocks of m (= tiles (r, j) and mirrors touching a row of A or B).
+// 256-row blocks of m.
 __device__ __forceinline__ int row_blocks(const NsUnit& U) { return (U.m + 255) / 256; }
 
-// The row counters a tile of a chained launch waits on before it reads, and
-// their target (c0 == c1 for an X-update tile); false: it waits on nothing.
-struct TileDeps {
+// Tile counters of a chained launch (layout in NsUnit::row_cnt).
+__device__ __forceinline__ int32_t* x_cnt(const NsUnit& U, int ti, int cj) {
+    return U.row_cnt + ti * row_tiles(U) + cj;
+}
+__device__ __forceinline__ int32_t* ab_cnt(const NsUnit& U, int which_b, int i, int j) {
+    const int T = row_blocks(U);
+    const int lo = i < j ? i : j, hi = i < j ? j : i;
+    return U.row_cnt + T * row_tiles(U) + which_b * T * T + lo * T + hi;
+}
+
+// Chunk c (256 of K) of tile t of iteration s in a chained launch: the two
+// counters it waits for (equal for an X-update tile) and their target.
+struct ChunkDeps {
     const int32_t* c0;
     const int32_t* c1;
     int32_t target;
 };
-template <int OP>
-__device__ __forceinline__ bool tile_deps(const NsLaunch& p, const NsUnit& U, const TileItem& t,
-                                          int op, int s, TileDeps* d) {
-    if (OP != OP_CHAIN) return false;
-    const int T = row_blocks(U);
+__device__ __forceinline__ ChunkDeps chunk_deps(const NsLaunch& p, const NsUnit& U,
+                                                const TileItem& t, int op, int s, int c) {
+    ChunkDeps d;
     if (op == OP_SYRK_X) {
-        if (s == 1) return false;                // X from before the launch
-        d->c0 = U.row_cnt + t.ti;
-        d->c1 = U.row_cnt + t.tj;
-        d->target = PAIR_EPI_WARPS * row_tiles(U) * (p.ep_x + s - 1);
+        d.c0 = x_cnt(U, t.ti, c);
+        d.c1 = x_cnt(U, t.tj, c);
+        d.target = PAIR_EPI_WARPS * (p.ep_x + s - 1);
     } else if (op == OP_SYRK_A) {
-        d->c0 = U.row_cnt + T + t.ti;
-        d->c1 = U.row_cnt + T + t.tj;
-        d->target = PAIR_EPI_WARPS * T * (p.ep_a + s);
+        d.c0 = ab_cnt(U, 0, t.ti, c);
+        d.c1 = ab_cnt(U, 0, t.tj, c);
+        d.target = PAIR_EPI_WARPS * (p.ep_a + s);
     } else {
-        d->c0 = d->c1 = U.row_cnt + 2 * T + t.ti;
-        d->target = PAIR_EPI_WARPS * T * (p.ep_b + s);
+        d.c0 = d.c1 = ab_cnt(U, 1, t.ti, c);
+        d.target = PAIR_EPI_WARPS * (p.ep_b + s);
     }
-    return true;
+    return d;
+}
+
+// Does a tile of a chained launch wait for anything?  (The first product of
+// iteration 1 reads X from before the launch.)
+template <int OP>
+__device__ __forceinline__ bool tile_waits(int op, int s) {
+    return OP == OP_CHAIN && !(op == OP_SYRK_X && s == 1);
+}
+
+// Producer of a chained tile: waits until the watcher warp has published,
+// for this CTA's tile number tno, more than c ready chunks; returns how
+// many, or -1 when the wait ran out or the CTA aborts.
+__device__ __noinline__ int wait_published(const uint64_t* slot, uint32_t tno, uint32_t c,
+                                           volatile int* abort_flag, int* err, uint64_t limit) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        const uint64_t v = ld_acquire_cta_u64(slot);
+        if (static_cast<uint32_t>(v >> 32) == tno && static_cast<uint32_t>(v) > c)
+            return static_cast<int>(static_cast<uint32_t>(v));
+        if ((i & 15) == 15) {
+            if (*abort_flag) return -1;
+            if (global_ns() - t0 > limit) {
+                *abort_flag = 1;
+                atomicCAS(err, 0, DEV_ERR_TIMEOUT);
+                return -1;
+            }
+        }
+    }
+}
+
+// Epilogue input block of a chained tile: the counter of the tile it comes
+// from (X update: the X tile (ti, tj) of iteration s; second product: the A
+// tile (ti, tj)); false if it waits for nothing.
+__device__ __forceinline__ bool input_dep(const NsLaunch& p, const NsUnit& U, const TileItem& t,
+                                          int op, int s, const int32_t** c, int32_t* target) {
+    if (op == OP_GEMM_BX) {
+        if (s == 1) return false;
+        *c = x_cnt(U, t.ti, t.tj);
+        *target = PAIR_EPI_WARPS * (p.ep_x + s - 1);
+        return true;
+    }
+    if (op == OP_SYRK_A) {
+        *c = ab_cnt(U, 0, t.ti, t.tj);
+        *target = PAIR_EPI_WARPS * (p.ep_a + s);
+        return true;
+    }
+    return false;
 }
 
 // After a tile of a chained launch: this warp's stores of the tile are
-// complete; count them for the rows the tile wrote (an X-update tile: X row
-// ti; a product tile: row ti of A or B and, through the mirror, row tj).
-__device__ __forceinline__ void release_rows(const NsUnit& U, const TileItem& t, int op) {
+// complete; count them on the tile's counter.
+__device__ __forceinline__ void release_tile(const NsUnit& U, const TileItem& t, int op) {
     bulk_wait_all0();
     fence_proxy_async_global();
-    const int T = row_blocks(U);
-    if (op == OP_GEMM_BX) {
-        count_release(U.row_cnt + t.ti);
-    } else {
-        int32_t* c = U.row_cnt + (op == OP_SYRK_X ? T : 2 * T);
-        count_release(c + t.ti);
-        if (t.tj != t.ti) count_release(c + t.tj);
-    }
+    count_release(op == OP_GEMM_BX ? x_cnt(U, t.ti, t.tj)
+                                   : ab_cnt(U, op == OP_SYRK_A ? 1 : 0, t.ti, t.tj));
 }
 
 // Tile-constant fields of a unit, copied into registers once per tile (the
@@ -587,7 +638,7 @@ __device__ __forceinline__ TileCursor<OP> tile_cursor(const NsLaunch& p, int pai
 
 // SL: distributed mode's first product (K in p.shards slices, OP_SYRK_X).
 template <int OP, int P_STAGES, int FW, int SL>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
     ns2_kernel(const __grid_constant__ NsLaunch p) {
     static_assert(!SL || (OP == OP_SYRK_X && !FW), "slices: first product only");
     constexpr int P_EPI_OFF = p_epi_off<P_STAGES>();
@@ -606,9 +657,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     uint64_t* in_bar = bars + 2 * P_STAGES + 5;    // NS per epilogue warp
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_bar + P_IN_SLOTS_MAX * P_EPI_WARPS);
     static_assert(p_smem<P_STAGES, FW>() <= 232448, "shared memory per CTA");
-    static_assert((2 * P_STAGES + 5 + P_IN_SLOTS_MAX * P_EPI_WARPS) * 8 + 8 <= 1024,
+    static_assert((2 * P_STAGES + 5 + P_IN_SLOTS_MAX * P_EPI_WARPS) * 8 + 8 + 24 <= 1024,
                   "barrier area");
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // chained launches: the watcher warp's ready chunks of tile number tno
+    // (tno << 32 | chunks) in dep_slot[tno & 1]; the producer's tile number
+    // in prod_seq
+    uint64_t* dep_slot = reinterpret_cast<uint64_t*>(tmem_slot + 2);
+    uint64_t* prod_seq = dep_slot + 2;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -628,6 +684,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         mbar_init(smem_u32(drain_bar), 1);
         for (int w = 0; w < NS * P_EPI_WARPS; ++w) mbar_init(smem_u32(&in_bar[w]), 1);
         *abort_flag = 0;
+        dep_slot[0] = dep_slot[1] = 0;
+        *prod_seq = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -661,9 +719,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             // the next tile's record is fetched while this tile streams
             TileItem t_next = cur.valid() ? p.tiles[cur.it] : TileItem{};
             int s_next = cur.s;
+            uint32_t tno = 0;        // chained launches: this tile's number
             while (ok && cur.valid()) {
                 const TileItem t = t_next;
                 const int s_it = s_next;
+                if (OP == OP_CHAIN) st_release_cta_u64(prod_seq, ++tno);
                 cur.next();
                 if (cur.valid()) {
                     t_next = p.tiles[cur.it];
@@ -683,17 +743,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                     else if (op == OP_SYRK_A) { tmA = &U->tm_a; tmB = tmA; }
                     else { tmA = &U->tm_b; tmB = &U->tm_x[src]; }
                 }
-                TileDeps d;
-                if (tile_deps<OP>(p, *U, t, op, s_it, &d)) {
-                    // the rows this tile reads are complete
-                    if (!wait_count(d.c0, d.target, abort_flag, p.err, limit) ||
-                        (d.c1 != d.c0 && !wait_count(d.c1, d.target, abort_flag, p.err, limit))) {
-                        ok = false;
-                        break;
-                    }
-                    fence_proxy_async_global();      // TMA reads after the acquire
-                }
                 const int kblocks = t.k_blocks;
+                // chained launches: K in 256-wide chunks (4 k-blocks), chunk
+                // c loaded once the tiles it reads are complete; chunks below
+                // ready_c are known to be
+                const int nchunks = (kblocks + 3) >> 2;
+                int ready_c = tile_waits<OP>(op, s_it) ? 0 : nchunks;
                 const int r0 = t.ti * 256 + static_cast<int>(rank) * P_HALF;
                 // N = n_len columns split evenly over the pair (64 or 128 each)
                 const int hb = t.n_len >> 1;
@@ -707,6 +762,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                     break;
                 }
                 for (int kb = 0; kb < kblocks; ++kb) {
+                    if (OP == OP_CHAIN && (kb >> 2) >= ready_c) {
+                        // the watcher warp publishes how many leading chunks
+                        // of this tile may be loaded
+                        const uint64_t v = ld_acquire_cta_u64(&dep_slot[tno & 1]);
+                        if (static_cast<uint32_t>(v >> 32) == tno &&
+                            static_cast<int>(static_cast<uint32_t>(v)) > (kb >> 2))
+                            ready_c = static_cast<int>(static_cast<uint32_t>(v));
+                        else
+                            ready_c = wait_published(&dep_slot[tno & 1], tno, kb >> 2,
+                                                     abort_flag, p.err, limit);
+                        if (ready_c < 0) {
+                            ok = false;
+                            break;
+                        }
+                        fence_proxy_async_global();    // TMA reads after the acquire
+                    }
                     if (!mbar_try_wait(smem_u32(&empty_bar[stage]), phase ^ 1) &&
                         !wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag,
                                       p.err, limit)) {
@@ -829,6 +900,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 wait_quiet(smem_u32(drain_bar), 0, limit);
             }
         }
+    } else if (OP == OP_CHAIN && warp == 2 + P_EPI_WARPS) {
+        // ------------------------------ counter watcher (chained launches)
+        // Walks this CTA's tiles as the producer does.  For a tile that
+        // waits, each lane polls one chunk (relaxed loads of its counters);
+        // the complete leading chunks are published, after an acquire
+        // fence, in dep_slot[tno & 1] (the producer has left tile tno - 2,
+        // the slot's previous user, once it works on tile tno - 1).
+        TileCursor<OP> cur = tile_cursor<OP>(p, pair, npairs);
+        uint32_t tno = 0;
+        bool ok = true;
+        while (ok && cur.valid()) {
+            const TileItem t = p.tiles[cur.it];
+            const int s_it = cur.s;
+            cur.next();
+            ++tno;
+            const int op = tile_op<OP>(t);
+            if (!tile_waits<OP>(op, s_it)) continue;
+            const NsUnit& U = p.units[t.unit];
+            const int nch = (t.k_blocks + 3) >> 2;
+            uint64_t t0 = global_ns();
+            while (ld_acquire_cta_u64(prod_seq) + 1 < tno) {
+                const bool stop = lane == 0 && (*abort_flag || global_ns() - t0 > limit);
+                if (__any_sync(0xffffffffu, stop)) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(64);
+            }
+            if (!ok) break;
+            t0 = global_ns();
+            for (int c = 0; c < nch;) {
+                int ready = 1;
+                if (lane < nch - c) {
+                    const ChunkDeps d = chunk_deps(p, U, t, op, s_it, c + lane);
+                    ready = load_relaxed(d.c0) >= d.target && load_relaxed(d.c1) >= d.target;
+                }
+                const uint32_t mask = __ballot_sync(0xffffffffu, ready);
+                int lead = (mask == 0xffffffffu) ? 32 : __ffs(~mask) - 1;
+                if (lead > nch - c) lead = nch - c;
+                if (lead > 0) {
+                    fence_acq_rel_gpu();
+                    __syncwarp();
+                    c += lead;
+                    if (lane == 0)
+                        st_release_cta_u64(&dep_slot[tno & 1],
+                                           (static_cast<uint64_t>(tno) << 32) | uint32_t(c));
+                    t0 = global_ns();
+                } else {
+                    bool stop = false;
+                    if (lane == 0) {
+                        if (*abort_flag) {
+                            stop = true;
+                        } else if (global_ns() - t0 > limit) {
+                            *abort_flag = 1;
+                            atomicCAS(p.err, 0, DEV_ERR_TIMEOUT);
+                            stop = true;
+                        }
+                    }
+                    if (__any_sync(0xffffffffu, stop)) {
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+        }
     } else {
         // -------------------------------------------- epilogue (both CTAs)
         // warps 2..9: lane group warp % 4 (TMEM rows), column half
@@ -868,20 +1005,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 issue_inputs<FW>(q, k, s_in + sl * p_in_blk<FW>(), smem_u32(&in_bar[NS * ew + sl]));
             ++in_seq;
         };
-        // chained launches: the rows a tile's input blocks come from are
+        // chained launches: the tile a tile's input blocks come from is
         // complete (lane 0 issues the loads: its acquire, then its proxy
         // fence).  Blocking at a tile's start; a single test for the next
         // tile, which must not wait while this one holds work others need.
         auto rows_ready = [&](const TileItem& tt, int ss, bool block) -> bool {
-            TileDeps d;
-            const NsUnit& U = p.units[tt.unit];
+            const int32_t* c;
+            int32_t target;
             int r = 1;
-            if (lane == 0 && tile_deps<OP>(p, U, tt, tile_op<OP>(tt), ss, &d)) {
-                if (block)
-                    r = wait_count(d.c0, d.target, abort_flag, p.err, limit) &&
-                        (d.c1 == d.c0 || wait_count(d.c1, d.target, abort_flag, p.err, limit));
-                else
-                    r = count_reached(d.c0, d.target) && count_reached(d.c1, d.target);
+            if (lane == 0 && input_dep(p, p.units[tt.unit], tt, tile_op<OP>(tt), ss, &c, &target)) {
+                r = block ? wait_count(c, target, abort_flag, p.err, limit)
+                          : count_reached(c, target);
                 if (r) fence_proxy_async_global();
             }
             return __shfl_sync(0xffffffffu, r, 0) != 0;
@@ -1047,7 +1181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 }
                 // chained launches: once this warp's stores of the tile are
                 // complete, count them for the rows they belong to
-                if (OP == OP_CHAIN) release_rows(p.units[t.unit], t, op);
+                if (OP == OP_CHAIN) release_tile(p.units[t.unit], t, op);
             }
             __syncwarp();
             ++local;
@@ -1080,7 +1214,7 @@ cudaError_t launch_pair_st(const NsLaunch& p, int pairs, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_done[dev] = 1;
     }
-    return launch_kernel(ns2_kernel<OP, ST, FW, SL>, dim3(2 * pairs), dim3(P_THREADS),
+    return launch_kernel(ns2_kernel<OP, ST, FW, SL>, dim3(2 * pairs), dim3(p_threads<OP>()),
                          p_smem<ST, FW>(), s, p);
 }
 

@@ -118,6 +118,36 @@ __device__ __noinline__ bool wait_count(const int32_t* cnt, int32_t target,
     }
 }
 
+// A relaxed load of a global counter (polling; follow a successful poll by
+// fence_acq_rel_gpu before reading what the counter guards).
+__device__ __forceinline__ int32_t load_relaxed(const int32_t* cnt) {
+    int32_t v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// Shared-memory words one warp publishes for another warp of the CTA.
+__device__ __forceinline__ uint64_t ld_acquire_cta_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.cta.shared::cta.b64 %0, [%1];" : "=l"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_cta_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(p)), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_relaxed_cta_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_cta_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.relaxed.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
 // One acquire load of a global counter: has it reached target?
 __device__ __forceinline__ bool count_reached(const int32_t* cnt, int32_t target) {
     int32_t v;
