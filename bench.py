@@ -350,10 +350,12 @@ def run_ours(args, wl, world, rank, local, pg):
         "syrk1": sum(m * (m + 1) * n for m, n in units),
         "syrk2": sum(m * (m + 1) * m for m, n in units),
     }
-    # a chained launch runs every product of the step but the last X update
+    # a chained launch runs every product of the step, the last X update too
+    # unless that one ran as its own launch
     ns = kw.get("ns_steps", 5)
+    gemm_alone = stage_tot.get("gemm", (0, 0))[1] > 0
     per_launch["chain"] = (ns * (per_launch["syrk1"] + per_launch["syrk2"])
-                           + (ns - 1) * per_launch["gemm"])
+                           + (ns - 1 if gemm_alone else ns) * per_launch["gemm"])
     dom = max((k for k in per_launch if stage_tot.get(k, (0, 0))[1]),
               key=lambda k: stage_tot[k][0])
     t_dom, n_dom = stage_tot[dom]

@@ -127,6 +127,7 @@ struct muon_ctx {
     bool fuse_stages = true;   // pair mode: iterations chained in one launch where it pays
     int64_t rc_limit = int64_t(1) << 30;   // row-counter target at which they are zeroed
     int chain_max_tiles = 8;   // X-update tiles per CTA pair up to which groups chain
+    bool chain_last = true;    // a chain also runs the last X update (weight update folded in)
     int max_pairs = 0;
 };
 
@@ -825,6 +826,7 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     h->fuse_update = fuse_update;
     if (const char* pd = std::getenv("MUON_PDL")) set_programmatic_launch(std::string(pd) != "0");
     if (const char* fs = std::getenv("MUON_FUSE_STAGES")) h->fuse_stages = std::string(fs) != "0";
+    if (const char* cl = std::getenv("MUON_CHAIN_LAST")) h->chain_last = std::string(cl) != "0";
     if (const char* cm = std::getenv("MUON_CHAIN_MAX_TILES")) {
         const int v = std::atoi(cm);
         if (v >= 0) h->chain_max_tiles = v;
@@ -1005,12 +1007,20 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         L.lr = lr;
         int cur = 0;
         // chained groups: one launch holds every product of iterations
-        // 1 .. ns_steps but the last X update, which then runs alone
+        // 1 .. ns_steps, the last X update too when the weight update folds
+        // into it through TMA (and no validation exports are registered: the
+        // chained kernel does not write them); else that one runs alone
         const bool chain = g.chain_ok;
+        const bool exports_on =
+            std::any_of(h->exp_w.begin(), h->exp_w.end(), [](float* q) { return q != nullptr; }) ||
+            std::any_of(h->exp_o.begin(), h->exp_o.end(), [](void* q) { return q != nullptr; });
+        const bool chain_last = chain && h->chain_last && fused && h->fuse_update == 2 &&
+                                g.w_tma && !exports_on;
         if (chain) {
             L.src = 0;
             L.first = fused ? 1 : 0;
             L.last = 0;
+            L.chain_last = chain_last ? 1 : 0;
             L.tiles = reinterpret_cast<const TileItem*>(ws + g.t_c_off);
             L.num_tiles = g.n_c;
             L.pair_off = reinterpret_cast<const int32_t*>(ws + g.o_c_off);
@@ -1031,8 +1041,10 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
             g.ep_a += ns_steps;
             g.ep_b += ns_steps;
             cur = (ns_steps - 1) & 1;
+            if (chain_last) cur ^= 1;
         }
-        for (int s = chain ? ns_steps - 1 : 0; s < ns_steps; ++s) {
+        const int s_begin = chain_last ? ns_steps : chain ? ns_steps - 1 : 0;
+        for (int s = s_begin; s < ns_steps; ++s) {
             L.src = cur;
             L.first = (fused && s == 0) ? 1 : 0;
             const bool last = s == ns_steps - 1;
@@ -1054,6 +1066,7 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
                 L.pair_off = h->pair ? reinterpret_cast<const int32_t*>(ws + q.oo) : nullptr;
                 L.pair_end_last = nullptr;
                 L.iters = 1;
+                L.chain_last = 0;
                 L.shards = g.shards;
                 if (!begin(q.st)) return fail(h, MUON_ERR_CUDA, "event create");
                 if (h->pair && q.op == OP_GEMM_BX && L.last && upd_tma)

@@ -145,6 +145,9 @@ struct NsLaunch {
     // PAIR_EPI_WARPS * (ep_a + s), a B tile once PAIR_EPI_WARPS * (ep_b + s)).
     int32_t iters;
     const int32_t* pair_end_last;
+    // OP_CHAIN: 1 = the last iteration's X-update tiles run too, with the
+    // weight update folded in (W read and written by TMA; no X' stored)
+    int32_t chain_last;
     int32_t ep_x, ep_a, ep_b;
     // Distributed mode, first product (CTA-pair kernels): the K range of
     // every tile is `shards` equal slices.  The pair runs them in turn, slice

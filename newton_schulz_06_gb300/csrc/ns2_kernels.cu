@@ -118,6 +118,13 @@ __device__ __forceinline__ int tile_src(const NsLaunch& p, int s) {
     return OP == OP_CHAIN ? (p.src ^ ((s - 1) & 1)) : p.src;
 }
 
+// A tile of a chained launch that is the last iteration's X update with
+// the weight update folded in.
+template <int OP>
+__device__ __forceinline__ bool chain_update_tile(const NsLaunch& p, int op, int s) {
+    return OP == OP_CHAIN && p.chain_last && op == OP_GEMM_BX && s == p.iters;
+}
+
 // 256-column blocks of n (X-update tiles per 256-row block of X').
 __device__ __forceinline__ int row_tiles(const NsUnit& U) { return (U.n + 255) / 256; }
 // 256-row blocks of m.
@@ -486,6 +493,7 @@ struct InPlan {
     int r0w, col0;               // first row, first column of the warp's part
     int n;                       // needed blocks
     int uses_in;                 // the tile reads input blocks
+    int wb;                      // chained weight-update tile: a W item after each X item
     // chained launches: may its input blocks be loaded (1), not known yet
     // (0: the rows they come from are tested once, then waited for), or
     // tested and not complete (-1: the blocks wait until the tile starts)
@@ -507,6 +515,8 @@ __device__ __forceinline__ InPlan plan_blocks(const NsLaunch& p, const TileItem&
     q.transposed = (OP != OP_CHAIN && op == OP_GEMM_BX && p.last) ? p.ew[t.unit].transposed : 0;
     q.uses_in = op != OP_SYRK_X;
     q.ready = (OP == OP_CHAIN && q.uses_in) ? 0 : 1;
+    q.wb = chain_update_tile<OP>(p, op, s) ? 1 : 0;
+    if (q.wb) q.transposed = p.ew[t.unit].transposed;
     q.r0w = t.ti * 256 + static_cast<int>(rank) * P_HALF + lg * 32;
     q.col0 = t.tj * 256 + half * 128;
     const int m = U->m;
@@ -524,20 +534,28 @@ __device__ __forceinline__ InPlan plan_blocks(const NsLaunch& p, const TileItem&
     return q;
 }
 
-// Lane 0: TMA loads of the input block of needed block k of plan q into
-// input slot `slot` and, when the update is folded in (FW), of the matching
-// W block (at (x, y) in the weight's orientation, or (y, x) for a
-// transposed unit), both on the slot's barrier.
+// Input items of plan q: one per needed block, two (X, then W) for a
+// chained weight-update tile.
+__device__ __forceinline__ int in_items(const InPlan& q) { return q.n << q.wb; }
+
+// Lane 0: TMA load of input item j of plan q into input slot `slot`, on the
+// slot's barrier.  An item is the input block of needed block k (X or A)
+// and, when the update is folded in (FW), the matching W block beside it;
+// with q.wb, items alternate between the X block and the W block.  W blocks
+// sit at (x, y) in the weight's orientation, or (y, x) for a transposed unit.
 template <int FW>
-__device__ __forceinline__ void issue_inputs(const InPlan& q, int k, uint8_t* slot,
+__device__ __forceinline__ void issue_inputs(const InPlan& q, int j, uint8_t* slot,
                                              uint32_t bar) {
+    const int k = j >> q.wb;
+    const bool w_item = q.wb && (j & 1);
     const int x = q.col0 + 32 * q.block(k), y = q.r0w;
     fence_proxy_async_smem();
     mbar_expect_tx(bar, p_in_blk<FW>());
-    tma_load_2d(smem_u32(slot), q.te_in, bar, x, y);
-    if (FW) {
-        if (q.transposed) tma_load_2d(smem_u32(slot + P_BLK), q.te_w, bar, y, x);
-        else tma_load_2d(smem_u32(slot + P_BLK), q.te_w, bar, x, y);
+    if (!w_item) tma_load_2d(smem_u32(slot), q.te_in, bar, x, y);
+    if (FW || w_item) {
+        uint8_t* wdst = FW ? slot + P_BLK : slot;
+        if (q.transposed) tma_load_2d(smem_u32(wdst), q.te_w, bar, y, x);
+        else tma_load_2d(smem_u32(wdst), q.te_w, bar, x, y);
     }
 }
 
@@ -545,9 +563,56 @@ __device__ __forceinline__ void issue_inputs(const InPlan& q, int k, uint8_t* sl
 // final iterate), W <- W - lr * shape_scale * O in W's own orientation, the
 // new W staged in `stage` and TMA-stored.  Same arithmetic as the separate
 // update pass (fp32 fma on the bf16 O, stored with round-to-nearest-even).
+// DBG: the optional fp32 W / bf16 O exports are written (not in chained
+// launches, which the planner does not give the update while exports are on).
+template <bool DBG>
 __device__ __forceinline__ void fused_update_block(const EpiUnit& u, int r0w, int gc0, int lane,
                                                    const float (&v)[32], const uint8_t* s_w,
                                                    uint8_t* stage) {
+    if (!DBG) {
+        // the same arithmetic, eight elements at a time (fewer live
+        // registers): O = bf16(v), through the stage as O^T when the unit is
+        // transposed (then each lane reads and rewrites only its own row)
+        if (u.transposed) {
+            st_col_bf16(stage, lane, v);
+            __syncwarp();
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float o8[8], w8[8];
+            if (u.transposed) {
+                const uint4 ob = *reinterpret_cast<const uint4*>(stage + sw64(lane, q));
+                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&ob);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 f = __bfloat1622float2(h[k]);
+                    o8[2 * k] = f.x;
+                    o8[2 * k + 1] = f.y;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    o8[k] = __bfloat162float(__float2bfloat16_rn(v[8 * q + k]));
+            }
+            const uint4 wb = *reinterpret_cast<const uint4*>(s_w + sw64(lane, q));
+            const __nv_bfloat162* hw = reinterpret_cast<const __nv_bfloat162*>(&wb);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f = __bfloat1622float2(hw[k]);
+                w8[2 * k] = f.x;
+                w8[2 * k + 1] = f.y;
+            }
+            uint4 out;
+            __nv_bfloat162* ho = reinterpret_cast<__nv_bfloat162*>(&out);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                ho[k] = __floats2bfloat162_rn(fmaf(-u.step, o8[2 * k], w8[2 * k]),
+                                              fmaf(-u.step, o8[2 * k + 1], w8[2 * k + 1]));
+            *reinterpret_cast<uint4*>(stage + sw64(lane, q)) = out;
+        }
+        store_block(u.te_w, stage, u.transposed ? r0w : gc0, u.transposed ? gc0 : r0w, lane);
+        return;
+    }
     float o[32], w[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) o[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
@@ -573,7 +638,7 @@ __device__ __forceinline__ void fused_update_block(const EpiUnit& u, int r0w, in
 #pragma unroll
     for (int e = 0; e < 32; ++e) w[e] = fmaf(-u.step, o[e], w[e]);
     st_row_bf16(stage, lane, w);
-    if ((u.w_dbg || u.o_dbg) && wrow < wrows) {
+    if (DBG && (u.w_dbg || u.o_dbg) && wrow < wrows) {
         const int64_t doff = static_cast<int64_t>(wrow) * u.ld_dbg + wcol0;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
@@ -630,7 +695,7 @@ __device__ __forceinline__ TileCursor<OP> tile_cursor(const NsLaunch& p, int pai
     c.iters = 1;
     if (OP == OP_CHAIN && r.begin < r.end) {
         c.iters = p.iters;
-        c.end_last = p.pair_end_last[pair];
+        c.end_last = p.chain_last ? r.end : p.pair_end_last[pair];
     }
     c.end = (c.iters == 1) ? c.end_last : c.end_all;
     return c;
@@ -1037,15 +1102,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                 cur.ready = 1;
             }
             if (cur.uses_in)
-                while (cur_issued < cur.n && in_seq - in_use < static_cast<uint32_t>(NS))
+                while (cur_issued < in_items(cur) && in_seq - in_use < static_cast<uint32_t>(NS))
                     issue_from(cur, cur_issued++);
             nxt.n = 0;
             nxt_issued = 0;
             if (has_next) nxt = plan_blocks<OP>(p, t_next, s_next, rank, lg, half);
             const int op = tile_op<OP>(t);
             const bool uses_in = cur.uses_in;
-            const EpiUnit u =
-                load_epi_unit(p, t.unit, op, tile_src<OP>(p, s_it), OP != OP_CHAIN && p.last);
+            // a chained weight-update tile: W read and written, no X' stored
+            const bool upd = chain_update_tile<OP>(p, op, s_it);
+            const EpiUnit u = load_epi_unit(p, t.unit, op, tile_src<OP>(p, s_it),
+                                            (OP != OP_CHAIN && p.last) || upd);
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             const int r0w = cur.r0w;
@@ -1105,32 +1172,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                 if (uses_in) {
                     const uint32_t sl = in_use % NS;
                     const uint8_t* slot = s_in + sl * p_in_blk<FW>();
-                    const bool got = wait_bounded(smem_u32(&in_bar[NS * ew + sl]),
-                                                  (in_use / NS) & 1u, abort_flag, p.err, limit);
+                    bool got = wait_bounded(smem_u32(&in_bar[NS * ew + sl]),
+                                            (in_use / NS) & 1u, abort_flag, p.err, limit);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     ++in_use;
+                    const uint8_t* s_w = slot + P_BLK;       // FW: W beside X
+                    if (OP == OP_CHAIN && upd) {
+                        // the W block is the next item
+                        const uint32_t sw = in_use % NS;
+                        s_w = s_in + sw * p_in_blk<FW>();
+                        got = wait_bounded(smem_u32(&in_bar[NS * ew + sw]), (in_use / NS) & 1u,
+                                           abort_flag, p.err, limit);
+                        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                        ++in_use;
+                    }
                     float x[32];
                     ld_row_bf16(slot, lane, x);
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         v[e] = (op == OP_SYRK_A) ? fmaf(p.b, x[e], p.c * v[e])
                                                  : scale * fmaf(p.a, x[e], v[e]);
-                    if (FW) {
+                    const bool fold = FW || (OP == OP_CHAIN && upd);
+                    if (fold) {
                         // W <- W - lr*scale*O, O = bf16(v); no X' output
-                        fused_update_block(u, r0w, gc0, lane, v, slot + P_BLK,
+                        fused_update_block<OP != OP_CHAIN>(u, r0w, gc0, lane, v, s_w,
                                            next_stage(s_st, st_seq, lane));
                     }
-                    __syncwarp();      // every lane's reads of the slot are done
-                    // refill the slot: this tile's next block, else the next
-                    // tile's first
-                    if (cur_issued < cur.n) {
-                        issue_from(cur, cur_issued++);
-                    } else if (nxt.uses_in && nxt_issued < nxt.n) {
-                        if (OP == OP_CHAIN && nxt.ready == 0)
-                            nxt.ready = rows_ready(t_next, s_next, false) ? 1 : -1;
-                        if (OP != OP_CHAIN || nxt.ready == 1) issue_from(nxt, nxt_issued++);
+                    __syncwarp();      // every lane's reads of the slots are done
+                    // refill the free slots: this tile's next items, else the
+                    // next tile's first
+                    while (in_seq - in_use < static_cast<uint32_t>(NS)) {
+                        if (cur_issued < in_items(cur)) {
+                            issue_from(cur, cur_issued++);
+                        } else if (nxt.uses_in && nxt_issued < in_items(nxt)) {
+                            if (OP == OP_CHAIN && nxt.ready == 0)
+                                nxt.ready = rows_ready(t_next, s_next, false) ? 1 : -1;
+                            if (OP == OP_CHAIN && nxt.ready != 1) break;
+                            issue_from(nxt, nxt_issued++);
+                        } else {
+                            break;
+                        }
                     }
-                    if (FW) continue;
+                    if (fold) continue;
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] *= scale;
@@ -1181,7 +1264,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                 }
                 // chained launches: once this warp's stores of the tile are
                 // complete, count them for the rows they belong to
-                if (OP == OP_CHAIN) release_tile(p.units[t.unit], t, op);
+                if (OP == OP_CHAIN && !upd) release_tile(p.units[t.unit], t, op);
             }
             __syncwarp();
             ++local;

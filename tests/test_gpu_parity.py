@@ -300,6 +300,45 @@ def test_chained_launch_small_matrix_matches_oracle(rows, cols, ns_steps, monkey
     assert torch.equal(trip[0], clone[0])
 
 
+@pytest.mark.parametrize("ns_steps", [1, 2, 5])
+def test_chained_last_update_bitexact(ns_steps, monkeypatch):
+    """With no validation exports registered the chained launch also runs the
+    last X update, the weight update folded in: the weights come out
+    bit-identical to the last X update run alone and to one launch per
+    product, over two steps (plain and transposed units, one pair holding a
+    few tiles)."""
+    shapes = [(512, 768), (768, 2048), (300, 300), (2048, 640), (96, 1000)]
+    runs = []
+    for env in ({}, {"MUON_CHAIN_LAST": "0"}, {"MUON_FUSE_STAGES": "0"}):
+        for k in ("MUON_CHAIN_LAST", "MUON_FUSE_STAGES"):
+            monkeypatch.delenv(k, raising=False)
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
+        trips = [case(r, c, 990 + i) for i, (r, c) in enumerate(shapes)]
+        _, _, _, opt = gpu_step(trips, ns_steps=ns_steps, steps=2, exports=False)
+        runs.append([t[0].clone() for t in trips])
+        if not env:
+            assert opt.plan_info()["chained_groups"] == 1
+    for i in range(len(shapes)):
+        assert torch.equal(runs[0][i], runs[1][i]), shapes[i]
+        assert torch.equal(runs[0][i], runs[2][i]), shapes[i]
+
+
+def test_chained_last_update_single_small_matrix_bitexact(monkeypatch):
+    """A chain over three tiles (some pairs hold only X-update tiles, which
+    now also run in the last iteration) gives the same weights as separate
+    launches."""
+    out = []
+    for env in ({}, {"MUON_FUSE_STAGES": "0"}):
+        monkeypatch.delenv("MUON_FUSE_STAGES", raising=False)
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
+        trip = case(200, 456, 995)
+        gpu_step([trip], ns_steps=3, steps=2, exports=False)
+        out.append(trip[0].clone())
+    assert torch.equal(out[0], out[1])
+
+
 def test_chain_counters_zeroed_and_restarted_bitexact(monkeypatch):
     """The chained launches' row counters only grow across steps; when a
     step's targets would pass the limit the group's counters are zeroed and
