@@ -1070,7 +1070,7 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
                 L.shards = g.shards;
                 if (!begin(q.st)) return fail(h, MUON_ERR_CUDA, "event create");
                 if (h->pair && q.op == OP_GEMM_BX && L.last && upd_tma)
-                    e = launch_ns_pair_update(L, q.np, h->stream);
+                    e = launch_ns_pair_update(L, q.np, exports_on, h->stream);
                 else if (h->pair)
                     e = launch_ns_pair(q.op, L, q.np, h->stages, h->stream);
                 else

@@ -216,7 +216,7 @@ size_t ns_smem_bytes();
 // CTA-pair (cta_group::2) kernels on 256 x 256 tiles; `pairs` clusters of 2.
 cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, int stages, cudaStream_t s);
 // Last GEMM with W <- W - lr*scale*O folded in (W blocks by TMA; bf16 W).
-cudaError_t launch_ns_pair_update(const NsLaunch& p, int pairs, cudaStream_t s);
+cudaError_t launch_ns_pair_update(const NsLaunch& p, int pairs, bool exports, cudaStream_t s);
 int ns_pair_max_clusters();
 // One-block kernel whose bounded wait must run out (failure-path check).
 cudaError_t launch_wait_timeout_check(int* err, unsigned long long limit_ns, cudaStream_t s);

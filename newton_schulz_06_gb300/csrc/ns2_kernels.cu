@@ -563,8 +563,8 @@ __device__ __forceinline__ void issue_inputs(const InPlan& q, int j, uint8_t* sl
 // final iterate), W <- W - lr * shape_scale * O in W's own orientation, the
 // new W staged in `stage` and TMA-stored.  Same arithmetic as the separate
 // update pass (fp32 fma on the bf16 O, stored with round-to-nearest-even).
-// DBG: the optional fp32 W / bf16 O exports are written (not in chained
-// launches, which the planner does not give the update while exports are on).
+// DBG: the optional fp32 W / bf16 O exports are written (the FW == 2
+// instantiation, used while exports are registered).
 template <bool DBG>
 __device__ __forceinline__ void fused_update_block(const EpiUnit& u, int r0w, int gc0, int lane,
                                                    const float (&v)[32], const uint8_t* s_w,
@@ -701,6 +701,8 @@ __device__ __forceinline__ TileCursor<OP> tile_cursor(const NsLaunch& p, int pai
     return c;
 }
 
+// FW: the last X update with the weight update folded in through TMA-loaded
+// W blocks (1; 2 also writes the validation exports).
 // SL: distributed mode's first product (K in p.shards slices, OP_SYRK_X).
 template <int OP, int P_STAGES, int FW, int SL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
@@ -1195,7 +1197,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                     const bool fold = FW || (OP == OP_CHAIN && upd);
                     if (fold) {
                         // W <- W - lr*scale*O, O = bf16(v); no X' output
-                        fused_update_block<OP != OP_CHAIN>(u, r0w, gc0, lane, v, s_w,
+                        fused_update_block<FW == 2>(u, r0w, gc0, lane, v, s_w,
                                            next_stage(s_st, st_seq, lane));
                     }
                     __syncwarp();      // every lane's reads of the slots are done
@@ -1350,8 +1352,9 @@ cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, int stages,
 
 // The last GEMM with the update folded in through TMA-loaded W blocks (one
 // input slot of X and W blocks, five pipeline stages).
-cudaError_t launch_ns_pair_update(const NsLaunch& p, int pairs, cudaStream_t s) {
-    return launch_pair_st<OP_GEMM_BX, 5, 1>(p, pairs, s);
+cudaError_t launch_ns_pair_update(const NsLaunch& p, int pairs, bool exports, cudaStream_t s) {
+    return exports ? launch_pair_st<OP_GEMM_BX, 5, 2>(p, pairs, s)
+                   : launch_pair_st<OP_GEMM_BX, 5, 1>(p, pairs, s);
 }
 
 }  // namespace muon

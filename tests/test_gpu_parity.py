@@ -324,6 +324,23 @@ def test_chained_last_update_bitexact(ns_steps, monkeypatch):
         assert torch.equal(runs[0][i], runs[2][i]), shapes[i]
 
 
+@pytest.mark.parametrize("chain_max", ["8", "0"])
+def test_update_without_exports_matches_exported_bitexact(chain_max, monkeypatch):
+    """The weight update folded into the last X update has an export-writing
+    form (validated against the oracle elsewhere) and the production forms
+    (8-element pieces; inside the chained launch when the group chains):
+    identical weights, plain and transposed units."""
+    monkeypatch.setenv("MUON_CHAIN_MAX_TILES", chain_max)
+    shapes = [(768, 1024), (1024, 384), (300, 700)]
+    a = [case(r, c, 1000 + i) for i, (r, c) in enumerate(shapes)]
+    b = [[t.clone() for t in tr] for tr in a]
+    _, _, _, opt = gpu_step(a, steps=2, exports=True)
+    gpu_step(b, steps=2, exports=False)
+    assert opt.plan_info()["chained_groups"] == (1 if chain_max == "8" else 0)
+    for i in range(len(shapes)):
+        assert torch.equal(a[i][0], b[i][0]), shapes[i]
+
+
 def test_chained_last_update_single_small_matrix_bitexact(monkeypatch):
     """A chain over three tiles (some pairs hold only X-update tiles, which
     now also run in the last iteration) gives the same weights as separate
