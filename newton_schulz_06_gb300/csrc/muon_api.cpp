@@ -970,7 +970,11 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         ew.lr = lr;
         ew.src = 0;
         ew.eps = NORM_EPS;
-        const int ew_grid = static_cast<int>(std::min<int64_t>(g.ew_tiles, ew_grid_cap));
+        // grid-stride over the tiles with the same number of tiles per block
+        // (no part-empty last round)
+        const int64_t ew_per_block =
+            std::max<int64_t>(1, ceil_div(g.ew_tiles, int64_t(ew_grid_cap)));
+        const int ew_grid = static_cast<int>(ceil_div(g.ew_tiles, ew_per_block));
         const bool fused = h->pair && h->fuse;
         if (g.chain_ok &&
             g.rc_step * (std::max({g.ep_x, g.ep_a, g.ep_b}) + ns_steps) > h->rc_limit) {
