@@ -127,6 +127,7 @@ struct muon_ctx {
     bool fuse_stages = true;   // pair mode: iterations chained in one launch where it pays
     int64_t rc_limit = int64_t(1) << 30;   // row-counter target at which they are zeroed
     int chain_max_tiles = 8;   // X-update tiles per CTA pair up to which groups chain
+    int chain_min_tiles = -1;  // X-update tiles from which groups chain (-1: one per pair)
     bool chain_last = true;    // a chain also runs the last X update (weight update folded in)
     int max_pairs = 0;
 };
@@ -388,16 +389,21 @@ void lpt_schedule(std::vector<TileItem>* v, int P, bool allow_split,
     (*off)[P] = static_cast<int32_t>(v->size());
 }
 
-// Groups with at most chain_max_tiles X-update tiles per CTA pair (8 unless
-// MUON_CHAIN_MAX_TILES says otherwise) chain their iterations in one launch.
-// Chaining pays where stage tails are a large share of a launch (few tiles
-// per pair, as for one large matrix); with many short tiles per pair the
+// Groups with at least one X-update tile per CTA pair and at most
+// chain_max_tiles of them per pair (8 unless MUON_CHAIN_MAX_TILES says
+// otherwise) chain their iterations in one launch.  Chaining pays where
+// stage tails are a large share of a launch (a few full waves, as for one
+// large matrix: 3072^2 -28%, 2048 x 8192 -10%).  Below one wave every stage
+// is a short dependent hop either way and separate launches are slightly
+// faster (256 x 512 up to 2048^2: 2-5%); with many short tiles per pair the
 // store completion the epilogue waits for before counting a tile costs more
-// (measured on a 388-matrix group: +3.6% for an X update fused with the
-// next first product).
+// than the tails (a 388-matrix group: +9..20%).  MUON_CHAIN_MIN_TILES
+// overrides the lower bound (tiles, not per pair).
 bool chain_eligible(const muon_ctx* h, int shards, int64_t gemm_tiles) {
-    return h->pair && h->fuse_stages && shards == 1 && gemm_tiles > 0 &&
-           gemm_tiles <= int64_t(h->chain_max_tiles) * std::max(1, h->max_pairs);
+    const int64_t pairs = std::max(1, h->max_pairs);
+    const int64_t lo = h->chain_min_tiles >= 0 ? h->chain_min_tiles : pairs;
+    return h->pair && h->fuse_stages && shards == 1 && gemm_tiles > 0 && gemm_tiles >= lo &&
+           gemm_tiles <= int64_t(h->chain_max_tiles) * pairs;
 }
 
 // Schedule of a chained launch over P CTA pairs.  A list-scheduling
@@ -827,6 +833,7 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     if (const char* pd = std::getenv("MUON_PDL")) set_programmatic_launch(std::string(pd) != "0");
     if (const char* fs = std::getenv("MUON_FUSE_STAGES")) h->fuse_stages = std::string(fs) != "0";
     if (const char* cl = std::getenv("MUON_CHAIN_LAST")) h->chain_last = std::string(cl) != "0";
+    if (const char* cn = std::getenv("MUON_CHAIN_MIN_TILES")) h->chain_min_tiles = std::atoi(cn);
     if (const char* cm = std::getenv("MUON_CHAIN_MAX_TILES")) {
         const int v = std::atoi(cm);
         if (v >= 0) h->chain_max_tiles = v;

@@ -180,10 +180,10 @@ def test_distributed_mode_plan_and_validation(L):
 
 
 def test_chained_launch_only_for_few_large_matrices(L):
-    """One chained launch per step (every product but the last X update) is
-    planned where a group has at most 8 X-update tiles per CTA pair, in full
-    and blockwise mode; distributed mode and large groups keep one launch per
-    product."""
+    """One chained launch per step is planned where a group has at least one
+    and at most 8 X-update tiles per CTA pair (76 pairs), in full and
+    blockwise mode; distributed mode, small steps and large groups keep one
+    launch per product."""
     from newton_schulz_06_gb300.inputs import qwen3_30b_a3b_block_shapes
     sq = _planner([(4096, 4096)])
     assert sq.plan_info(L.MUON_FULL, 1)["chained_groups"] == 1
@@ -193,3 +193,7 @@ def test_chained_launch_only_for_few_large_matrices(L):
     assert _planner([(6144, 6144)]).plan_info()["chained_groups"] == 1
     assert _planner([(6400, 6400)]).plan_info()["chained_groups"] == 0
     assert _planner(qwen3_30b_a3b_block_shapes()).plan_info()["chained_groups"] == 0
+    # below one wave: 2048^2 has 8 x 8 X-update tiles, 2048 x 8192 has 8 x 32
+    assert _planner([(2048, 2048)]).plan_info()["chained_groups"] == 0
+    assert _planner([(2048, 8192)]).plan_info()["chained_groups"] == 1
+    assert _planner([(256, 512)]).plan_info()["chained_groups"] == 0

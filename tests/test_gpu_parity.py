@@ -269,6 +269,7 @@ def test_chained_launch_bitexact(ns_steps, monkeypatch):
     (tiles waiting on row-block counters) computes every tile as the
     separate launches do: identical bits, over two steps (the counters carry
     across launches and steps)."""
+    monkeypatch.setenv("MUON_CHAIN_MIN_TILES", "0")     # small shapes chain too
     shapes = [(512, 768), (768, 2048), (300, 300), (2048, 640), (96, 1000)]
     trips = [case(r, c, 900 + i) for i, (r, c) in enumerate(shapes)]
     clones = [[t.clone() for t in tr] for tr in trips]
@@ -288,6 +289,7 @@ def test_chained_launch_small_matrix_matches_oracle(rows, cols, ns_steps, monkey
     """A chain over a few tiles leaves most CTA pairs idle and gives some
     pairs only X-update tiles (which they skip in the last iteration): same
     bits as separate launches, within tolerance of the oracle."""
+    monkeypatch.setenv("MUON_CHAIN_MIN_TILES", "0")     # small shapes chain too
     trip = case(rows, cols, 970)
     clone = [t.clone() for t in trip]
     inp, wexp, oexp, opt = gpu_step([trip], ns_steps=ns_steps)
@@ -307,6 +309,7 @@ def test_chained_last_update_bitexact(ns_steps, monkeypatch):
     bit-identical to the last X update run alone and to one launch per
     product, over two steps (plain and transposed units, one pair holding a
     few tiles)."""
+    monkeypatch.setenv("MUON_CHAIN_MIN_TILES", "0")     # small shapes chain too
     shapes = [(512, 768), (768, 2048), (300, 300), (2048, 640), (96, 1000)]
     runs = []
     for env in ({}, {"MUON_CHAIN_LAST": "0"}, {"MUON_FUSE_STAGES": "0"}):
@@ -330,6 +333,7 @@ def test_update_without_exports_matches_exported_bitexact(chain_max, monkeypatch
     form (validated against the oracle elsewhere) and the production forms
     (8-element pieces; inside the chained launch when the group chains):
     identical weights, plain and transposed units."""
+    monkeypatch.setenv("MUON_CHAIN_MIN_TILES", "0")     # small shapes chain too
     monkeypatch.setenv("MUON_CHAIN_MAX_TILES", chain_max)
     shapes = [(768, 1024), (1024, 384), (300, 700)]
     a = [case(r, c, 1000 + i) for i, (r, c) in enumerate(shapes)]
@@ -345,6 +349,7 @@ def test_chained_last_update_single_small_matrix_bitexact(monkeypatch):
     """A chain over three tiles (some pairs hold only X-update tiles, which
     now also run in the last iteration) gives the same weights as separate
     launches."""
+    monkeypatch.setenv("MUON_CHAIN_MIN_TILES", "0")     # small shapes chain too
     out = []
     for env in ({}, {"MUON_FUSE_STAGES": "0"}):
         monkeypatch.delenv("MUON_FUSE_STAGES", raising=False)
@@ -361,6 +366,7 @@ def test_chain_counters_zeroed_and_restarted_bitexact(monkeypatch):
     step's targets would pass the limit the group's counters are zeroed and
     the rounds start over.  With a limit of 1 that happens before every
     step: three steps give the same bits as counters that never restart."""
+    monkeypatch.setenv("MUON_CHAIN_MIN_TILES", "0")     # small shapes chain too
     shapes = [(1024, 1536), (640, 640)]
     trips = [case(r, c, 950 + i) for i, (r, c) in enumerate(shapes)]
     clones = [[t.clone() for t in tr] for tr in trips]
