@@ -49,7 +49,7 @@ struct UnitDesc {
     bool transposed = false;
     float scale = 1.f;
     size_t x_bytes = 0, mm_bytes = 0, buf_bytes = 0;
-    size_t row_bytes = 0;       // chained launches: one counter per X, A and B tile
+    size_t cnt_bytes = 0;       // chained launches: one counter per X, A and B tile
     int shards = 1;             // distributed mode: slices of the long side
     int64_t ew_tiles = 0;
     size_t need = 0;   // scratch bytes of this unit inside a group
@@ -71,12 +71,12 @@ struct GroupDesc {
     size_t t_c_off = 0, o_c_off = 0, e_c_off = 0;
     int n_c = 0, p_c = 0;
     bool chain_ok = false;
-    // completed rounds of the X, A and B row counters since they were last
+    // completed rounds of the X, A and B tile counters since they were last
     // zeroed; the counters sit in the metadata region (never aliased by a
     // group's scratch) and only grow
     int64_t ep_x = 0, ep_a = 0, ep_b = 0;
     size_t rc_off = 0, rc_bytes = 0;         // this group's counter block
-    int64_t rc_step = 0;                     // largest per-round increment
+    int64_t rc_step = 0;                     // a counter's increment per round
     int64_t ew_tiles = 0;
     int shards = 1;                          // distributed mode: P
 };
@@ -242,7 +242,7 @@ int build_units(muon_ctx* h, int mode, int nb, std::vector<UnitDesc>* out) {
                                 ") are not equal multiples of 64");
             {
                 const size_t T = size_t(ceil_div(u.m, 256)), RT = size_t(ceil_div(u.n, 256));
-                u.row_bytes = align_up((T * RT + 2 * T * T) * 4, 256);
+                u.cnt_bytes = align_up((T * RT + 2 * T * T) * 4, 256);
             }
             u.buf_bytes = 2 * u.x_bytes + 2 * u.mm_bytes;
             u.ew_tiles = ceil_div(u.m, EW_TILE) * ceil_div(u.n, EW_TILE);
@@ -264,7 +264,7 @@ size_t meta_bound(const std::vector<UnitDesc>& units) {
         g = std::max(g, g2);
         // tile lists (room for twice the tiles, as if every tile were split in
         // halves) and pair offsets
-        b += sizeof(EwUnit) + sizeof(NsUnit) + 8 * 256 + u.row_bytes +
+        b += sizeof(EwUnit) + sizeof(NsUnit) + 8 * 256 + u.cnt_bytes +
              2 * size_t(2 * s + g) * sizeof(TileItem) + 3 * 4 * 1024;
     }
     return align_up(b, 1024);
@@ -529,11 +529,11 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         g.ns_off = off;
         off += sizeof(NsUnit) * nu;
         g.shards = P.units[g.u0].shards;
-        // row-block counters of fused launches, zero in the uploaded image
+        // tile counters of chained launches, zero in the uploaded image
         off = align_up(off, 256);
         g.rc_off = off;
         g.rc_step = PAIR_EPI_WARPS;             // every tile counter, per round
-        for (int i = g.u0; i < g.u1; ++i) off += P.units[i].row_bytes;
+        for (int i = g.u0; i < g.u1; ++i) off += P.units[i].cnt_bytes;
         g.rc_bytes = off - g.rc_off;
         size_t rc_next = g.rc_off;
         std::vector<TileItem> tsx, tsa, tg;
@@ -616,8 +616,8 @@ int build_plan(muon_ctx* h, int mode, int nb) {
             ns.x[1] = e.x[1];
             ns.a = reinterpret_cast<__nv_bfloat16*>(ab);
             ns.b = reinterpret_cast<__nv_bfloat16*>(bb);
-            ns.row_cnt = reinterpret_cast<int32_t*>(ws + rc_next);
-            rc_next += u.row_bytes;
+            ns.tile_cnt = reinterpret_cast<int32_t*>(ws + rc_next);
+            rc_next += u.cnt_bytes;
             ns.m = u.m;
             ns.n = u.n;
             ns.ld_x = u.ld_x;
@@ -987,7 +987,7 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
             g.rc_step * (std::max({g.ep_x, g.ep_a, g.ep_b}) + ns_steps) > h->rc_limit) {
             // the targets would near int32 overflow: start the counters over
             const cudaError_t ce = cudaMemsetAsync(ws + g.rc_off, 0, g.rc_bytes, h->stream);
-            if (ce != cudaSuccess) return cuda_fail(h, ce, "row counter reset");
+            if (ce != cudaSuccess) return cuda_fail(h, ce, "tile counter reset");
             g.ep_x = g.ep_a = g.ep_b = 0;
         }
         ew.write_x = fused ? 1 : 0;

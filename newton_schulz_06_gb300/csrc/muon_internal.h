@@ -75,11 +75,11 @@ struct alignas(128) NsUnit {
     __nv_bfloat16* b;
     // Chained launches: per 256 x 256 output tile, the epilogue warps that
     // finished storing their part of it (PAIR_EPI_WARPS per tile and round):
-    // X tiles (ti, cj) at row_cnt[ti * RT + cj], then A tiles (i <= j) at
-    // row_cnt[T * RT + i * T + j] and B tiles at row_cnt[T * RT + T * T +
+    // X tiles (ti, cj) at tile_cnt[ti * RT + cj], then A tiles (i <= j) at
+    // tile_cnt[T * RT + i * T + j] and B tiles at tile_cnt[T * RT + T * T +
     // i * T + j]; T = 256-row blocks of m, RT = 256-column blocks of n.
     // They only grow.
-    int32_t* row_cnt;
+    int32_t* tile_cnt;
     int32_t m, n, ld_x, ld_mm;
 };
 

@@ -22,6 +22,15 @@
 // barrier inline and call the bounded wait only when the stage is not ready,
 // and the MMA thread adds offsets to precomputed descriptors.
 //
+// A chained launch (OP_CHAIN) runs all of a step's products (iterations
+// 1 .. ns, the weight update folded into the last X update) as one tile
+// list per pair, walked once per iteration.  Each 256-wide K chunk of a tile
+// is loaded once the tiles it reads are complete: epilogue warps count
+// finished tiles on per-tile counters (after their TMA stores complete),
+// and an eleventh warp per CTA polls the counters of the producer's coming
+// chunks and publishes how many are ready through shared memory, so the
+// producer's loop never waits on global memory.
+//
 // Distributed mode's first product (SL = 1) runs each tile's K slices in
 // turn on the same pair and sums them in tensor memory (accumulator 0 holds
 // the running sum, accumulator 1 the newest slice).
@@ -130,14 +139,14 @@ __device__ __forceinline__ int row_tiles(const NsUnit& U) { return (U.n + 255) /
 // 256-row blocks of m.
 __device__ __forceinline__ int row_blocks(const NsUnit& U) { return (U.m + 255) / 256; }
 
-// Tile counters of a chained launch (layout in NsUnit::row_cnt).
+// Tile counters of a chained launch (layout in NsUnit::tile_cnt).
 __device__ __forceinline__ int32_t* x_cnt(const NsUnit& U, int ti, int cj) {
-    return U.row_cnt + ti * row_tiles(U) + cj;
+    return U.tile_cnt + ti * row_tiles(U) + cj;
 }
 __device__ __forceinline__ int32_t* ab_cnt(const NsUnit& U, int which_b, int i, int j) {
     const int T = row_blocks(U);
     const int lo = i < j ? i : j, hi = i < j ? j : i;
-    return U.row_cnt + T * row_tiles(U) + which_b * T * T + lo * T + hi;
+    return U.tile_cnt + T * row_tiles(U) + which_b * T * T + lo * T + hi;
 }
 
 // Chunk c (256 of K) of tile t of iteration s in a chained launch: the two
@@ -1076,7 +1085,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
         // complete (lane 0 issues the loads: its acquire, then its proxy
         // fence).  Blocking at a tile's start; a single test for the next
         // tile, which must not wait while this one holds work others need.
-        auto rows_ready = [&](const TileItem& tt, int ss, bool block) -> bool {
+        auto input_ready = [&](const TileItem& tt, int ss, bool block) -> bool {
             const int32_t* c;
             int32_t target;
             int r = 1;
@@ -1097,7 +1106,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                 s_next = tc.s;
             }
             if (OP == OP_CHAIN && cur.uses_in && cur.ready != 1) {
-                if (!rows_ready(t, s_it, true)) {
+                if (!input_ready(t, s_it, true)) {
                     ok = false;
                     break;
                 }
@@ -1208,7 +1217,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                             issue_from(cur, cur_issued++);
                         } else if (nxt.uses_in && nxt_issued < in_items(nxt)) {
                             if (OP == OP_CHAIN && nxt.ready == 0)
-                                nxt.ready = rows_ready(t_next, s_next, false) ? 1 : -1;
+                                nxt.ready = input_ready(t_next, s_next, false) ? 1 : -1;
                             if (OP == OP_CHAIN && nxt.ready != 1) break;
                             issue_from(nxt, nxt_issued++);
                         } else {

@@ -9,7 +9,7 @@ import torch
 
 from gpu_helpers import (check_against_oracle, gpu_step, oracle_step, relF,
                          to_np)
-from newton_schulz_06_gb300 import Muon
+from newton_schulz_06_gb300 import Muon, mode_code
 from newton_schulz_06_gb300.inputs import random_case, workload, make_state
 
 pytestmark = pytest.mark.gpu
@@ -359,6 +359,25 @@ def test_chained_last_update_single_small_matrix_bitexact(monkeypatch):
         gpu_step([trip], ns_steps=3, steps=2, exports=False)
         out.append(trip[0].clone())
     assert torch.equal(out[0], out[1])
+
+
+@pytest.mark.parametrize("rows,cols,mode,nb", [(6144, 1536, "full", 1),
+                                               (2048, 4096, "blockwise", 2)])
+def test_chained_default_sizes_match_oracle(rows, cols, mode, nb, monkeypatch):
+    """Steps that chain under the default bounds (at least one X-update tile
+    per CTA pair): a tall matrix (transposed unit) and two column blocks.
+    Within tolerance of the oracle, and the same bits as one launch per
+    product."""
+    trip = case(rows, cols, 1010)
+    clone = [t.clone() for t in trip]
+    inp, wexp, oexp, opt = gpu_step([trip], mode=mode, nb=nb)
+    assert opt.plan_info(mode_code(mode), nb)["chained_groups"] == 1
+    ref = oracle_step(inp[0], mode=mode, nb=nb)
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref, mode=mode, nb=nb)
+    monkeypatch.setenv("MUON_FUSE_STAGES", "0")
+    _, _, o2, _ = gpu_step([clone], mode=mode, nb=nb)
+    assert torch.equal(oexp[0], o2[0])
+    assert torch.equal(trip[0], clone[0])
 
 
 def test_chain_counters_zeroed_and_restarted_bitexact(monkeypatch):
