@@ -129,6 +129,9 @@ struct muon_ctx {
     int chain_max_tiles = 8;   // X-update tiles per CTA pair up to which groups chain
     int chain_min_tiles = -1;  // X-update tiles from which groups chain (-1: one per pair)
     bool chain_last = true;    // a chain also runs the last X update (weight update folded in)
+    // failure test only: rounds added to what a chained launch's second
+    // products wait for, so their waits run out (MUON_DEBUG_CHAIN_SKEW)
+    int debug_chain_skew = 0;
     int max_pairs = 0;
 };
 
@@ -833,6 +836,7 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     if (const char* pd = std::getenv("MUON_PDL")) set_programmatic_launch(std::string(pd) != "0");
     if (const char* fs = std::getenv("MUON_FUSE_STAGES")) h->fuse_stages = std::string(fs) != "0";
     if (const char* cl = std::getenv("MUON_CHAIN_LAST")) h->chain_last = std::string(cl) != "0";
+    if (const char* sk = std::getenv("MUON_DEBUG_CHAIN_SKEW")) h->debug_chain_skew = std::atoi(sk);
     if (const char* cn = std::getenv("MUON_CHAIN_MIN_TILES")) h->chain_min_tiles = std::atoi(cn);
     if (const char* cm = std::getenv("MUON_CHAIN_MAX_TILES")) {
         const int v = std::atoi(cm);
@@ -1038,7 +1042,7 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
             L.pair_end_last = reinterpret_cast<const int32_t*>(ws + g.e_c_off);
             L.iters = ns_steps;
             L.ep_x = static_cast<int32_t>(g.ep_x);
-            L.ep_a = static_cast<int32_t>(g.ep_a);
+            L.ep_a = static_cast<int32_t>(g.ep_a + h->debug_chain_skew);
             L.ep_b = static_cast<int32_t>(g.ep_b);
             L.shards = 1;
             if (!begin(ST_CHAIN)) return fail(h, MUON_ERR_CUDA, "event create");
