@@ -139,14 +139,6 @@ __device__ __forceinline__ uint64_t ld_acquire_cta_u64(const uint64_t* p) {
 __device__ __forceinline__ void st_release_cta_u64(uint64_t* p, uint64_t v) {
     asm volatile("st.release.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(p)), "l"(v) : "memory");
 }
-__device__ __forceinline__ uint32_t ld_relaxed_cta_u32(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.relaxed.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_relaxed_cta_u32(uint32_t* p, uint32_t v) {
-    asm volatile("st.relaxed.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
 
 // One acquire load of a global counter: has it reached target?
 __device__ __forceinline__ bool count_reached(const int32_t* cnt, int32_t target) {
