@@ -204,6 +204,17 @@ MUON_API int muon_debug_set_exports(muon_handle h, int n, float* const* w_f32,
  * CUDA context stays usable.  Makes no other change. */
 MUON_API int muon_debug_wait_timeout(muon_handle h, int* err_word, int limit_ms);
 
+/* Host-only check of the chained launch's schedule for `mode`/`nb`: for every
+ * group of the registered matrices (ignoring the size bounds that decide
+ * whether a group chains), builds the per-pair tile lists and checks that
+ * every tile appears once, that each pair's list is in stage order (first
+ * products, second products, X updates: the order that keeps every wait on
+ * tiles of earlier stages) and that the pair offsets and last-iteration ends
+ * are consistent.  No CUDA call; works on MUON_HOST_ONLY handles.  Returns
+ * MUON_OK, or MUON_ERR_STATE with the violated property in
+ * muon_last_error. */
+MUON_API int muon_debug_check_chain_schedule(muon_handle h, int mode, int nb);
+
 /* Plan statistics for `mode`/`nb`: number of units (matrices or blocks),
  * groups, and tiles of the symmetric-product and GEMM stages. */
 typedef struct {

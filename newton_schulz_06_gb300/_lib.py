@@ -35,7 +35,8 @@ EXPORTS = ("muon_create", "muon_set_stream", "muon_register_params",
            "muon_sync", "muon_destroy", "muon_last_error",
            "muon_set_profiling", "muon_stage_times", "muon_last_launch_count",
            "muon_debug_set_exports", "muon_get_plan_info",
-           "muon_step_noalloc", "muon_debug_wait_timeout", "muon_step_host")
+           "muon_step_noalloc", "muon_debug_wait_timeout", "muon_step_host",
+           "muon_debug_check_chain_schedule")
 
 
 class MuonParam(ctypes.Structure):
@@ -101,6 +102,7 @@ def lib() -> ctypes.CDLL:
         "muon_step_noalloc": [ctypes.POINTER(MuonParam), f32, f32, i32, i32,
                               f32, f32, f32, vp, ctypes.c_char_p, sz],
         "muon_debug_wait_timeout": [H, vp, i32],
+        "muon_debug_check_chain_schedule": [H, i32, i32],
         "muon_step_host": [H, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), f32,
                            f32, i32, i32, f32, f32, f32, i32, i32],
     }

@@ -490,6 +490,72 @@ void lpt_schedule_chain(const std::vector<TileItem>& sx, const std::vector<TileI
     (*off)[P] = static_cast<int32_t>(v->size());
 }
 
+// The tiles of one unit (local index li) for the three products: symmetric
+// tiles (ti <= tj) of the first and second product, X-update tiles.
+void append_unit_tiles(const UnitDesc& u, int li, bool pair, std::vector<TileItem>* tsx,
+                       std::vector<TileItem>* tsa, std::vector<TileItem>* tg) {
+    const int kx = static_cast<int>(ceil_div(u.n, BK));
+    const int km = static_cast<int>(ceil_div(u.m, BK));
+    if (pair) {
+        const int64_t T2 = ceil_div(u.m, 256);
+        for (int64_t ti = 0; ti < T2; ++ti)
+            for (int64_t tj = ti; tj < T2; ++tj) {
+                TileItem t{};
+                t.unit = li;
+                t.ti = static_cast<int16_t>(ti);
+                t.tj = static_cast<int16_t>(tj);
+                t.n_off = 0;
+                t.n_len = 256;
+                t.k_blocks = kx;
+                tsx->push_back(t);
+                t.k_blocks = km;
+                tsa->push_back(t);
+            }
+        for (int64_t ti = 0; ti < T2; ++ti)
+            for (int64_t tj = 0; tj < ceil_div(u.n, 256); ++tj) {
+                TileItem t{};
+                t.unit = li;
+                t.ti = static_cast<int16_t>(ti);
+                t.tj = static_cast<int16_t>(tj);
+                t.n_off = 0;
+                t.n_len = 256;
+                t.k_blocks = km;
+                tg->push_back(t);
+            }
+    } else {
+        const int64_t T = ceil_div(u.m, BM);
+        for (int64_t ti = 0; ti < T; ++ti)
+            for (int64_t tj = 0; tj < ceil_div(T, 2); ++tj) {
+                const int64_t bl = 2 * tj, br = 2 * tj + 1;
+                const bool lneed = bl < T && bl >= ti;
+                const bool rneed = br < T && br >= ti;
+                if (!lneed && !rneed) continue;
+                TileItem t{};
+                t.unit = li;
+                t.ti = static_cast<int16_t>(ti);
+                t.tj = static_cast<int16_t>(tj);
+                t.n_off = lneed ? 0 : 128;
+                t.n_len = static_cast<int16_t>(128 * (int(lneed) + int(rneed)));
+                t.k_blocks = kx;
+                tsx->push_back(t);
+                t.k_blocks = km;
+                tsa->push_back(t);
+            }
+        for (int64_t ti = 0; ti < T; ++ti)
+            for (int64_t tj = 0; tj < ceil_div(u.n, BN); ++tj) {
+                TileItem t{};
+                t.unit = li;
+                t.ti = static_cast<int16_t>(ti);
+                t.tj = static_cast<int16_t>(tj);
+                t.n_off = 0;
+                t.n_len = static_cast<int16_t>(
+                    std::min<int64_t>(BN, align_up(u.n - tj * BN, 16)));
+                t.k_blocks = km;
+                tg->push_back(t);
+            }
+    }
+}
+
 int build_plan(muon_ctx* h, int mode, int nb) {
     Plan& P = h->plan;
     P = Plan();
@@ -628,67 +694,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
             std::memcpy(meta.data() + g.ns_off + sizeof(NsUnit) * (i - g.u0), &ns, sizeof(ns));
 
             // tile lists
-            const int li = i - g.u0;
-            const int kx = static_cast<int>(ceil_div(u.n, BK));
-            const int km = static_cast<int>(ceil_div(u.m, BK));
-            if (h->pair) {
-                const int64_t T2 = ceil_div(u.m, 256);
-                for (int64_t ti = 0; ti < T2; ++ti)
-                    for (int64_t tj = ti; tj < T2; ++tj) {
-                        TileItem t{};
-                        t.unit = li;
-                        t.ti = static_cast<int16_t>(ti);
-                        t.tj = static_cast<int16_t>(tj);
-                        t.n_off = 0;
-                        t.n_len = 256;
-                        t.k_blocks = kx;
-                        tsx.push_back(t);
-                        t.k_blocks = km;
-                        tsa.push_back(t);
-                    }
-                for (int64_t ti = 0; ti < T2; ++ti)
-                    for (int64_t tj = 0; tj < ceil_div(u.n, 256); ++tj) {
-                        TileItem t{};
-                        t.unit = li;
-                        t.ti = static_cast<int16_t>(ti);
-                        t.tj = static_cast<int16_t>(tj);
-                        t.n_off = 0;
-                        t.n_len = 256;
-                        t.k_blocks = km;
-                        tg.push_back(t);
-                    }
-            } else {
-                const int64_t T = ceil_div(u.m, BM);
-                for (int64_t ti = 0; ti < T; ++ti)
-                    for (int64_t tj = 0; tj < ceil_div(T, 2); ++tj) {
-                        const int64_t bl = 2 * tj, br = 2 * tj + 1;
-                        const bool lneed = bl < T && bl >= ti;
-                        const bool rneed = br < T && br >= ti;
-                        if (!lneed && !rneed) continue;
-                        TileItem t{};
-                        t.unit = li;
-                        t.ti = static_cast<int16_t>(ti);
-                        t.tj = static_cast<int16_t>(tj);
-                        t.n_off = lneed ? 0 : 128;
-                        t.n_len = static_cast<int16_t>(128 * (int(lneed) + int(rneed)));
-                        t.k_blocks = kx;
-                        tsx.push_back(t);
-                        t.k_blocks = km;
-                        tsa.push_back(t);
-                    }
-                for (int64_t ti = 0; ti < T; ++ti)
-                    for (int64_t tj = 0; tj < ceil_div(u.n, BN); ++tj) {
-                        TileItem t{};
-                        t.unit = li;
-                        t.ti = static_cast<int16_t>(ti);
-                        t.tj = static_cast<int16_t>(tj);
-                        t.n_off = 0;
-                        t.n_len = static_cast<int16_t>(
-                            std::min<int64_t>(BN, align_up(u.n - tj * BN, 16)));
-                        t.k_blocks = km;
-                        tg.push_back(t);
-                    }
-            }
+            append_unit_tiles(u, i - g.u0, h->pair, &tsx, &tsa, &tg);
             int64_t s, gg, us, ex;
             unit_tiles(u, h->pair, &s, &gg, &us, &ex);
             P.useful_flops_iter += us;
@@ -1290,6 +1296,75 @@ int muon_get_plan_info(muon_handle h, int mode, int nb, muon_plan_info* out) {
             gemm += gg;
         }
         if (chain_eligible(h, units[g.u0].shards, gemm)) ++out->chained_groups;
+    }
+    return MUON_OK;
+}
+
+int muon_debug_check_chain_schedule(muon_handle h, int mode, int nb) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (h->params.empty()) return fail(h, MUON_ERR_STATE, "no parameters registered");
+    if (!h->pair) return MUON_OK;                 // chains run on CTA pairs only
+    std::vector<UnitDesc> units;
+    int rc = build_units(h, mode, nb, &units);
+    if (rc) return rc;
+    std::vector<GroupDesc> groups;
+    size_t min_b, full_b;
+    sizes_for(units, &min_b, &full_b);
+    if (h->ws && h->ws_bytes >= min_b) {
+        make_groups(units, h->ws_bytes - align_up(HEADER_BYTES + meta_bound(units), 1024),
+                    &groups);
+    } else {
+        GroupDesc g;
+        g.u0 = 0;
+        g.u1 = static_cast<int>(units.size());
+        groups.push_back(g);
+    }
+    for (size_t gi = 0; gi < groups.size(); ++gi) {
+        const GroupDesc& g = groups[gi];
+        std::vector<TileItem> tsx, tsa, tg;
+        for (int i = g.u0; i < g.u1; ++i)
+            append_unit_tiles(units[i], i - g.u0, true, &tsx, &tsa, &tg);
+        sort_tiles(&tsx);
+        sort_tiles(&tsa);
+        sort_tiles(&tg);
+        const int pairs = std::max(
+            1, std::min(h->max_pairs, static_cast<int>(tsx.size() + tsa.size() + tg.size())));
+        std::vector<TileItem> v;
+        std::vector<int32_t> offs, ends;
+        lpt_schedule_chain(tsx, tsa, tg, pairs, &v, &offs, &ends);
+        const std::string where = "group " + std::to_string(gi) + ": ";
+        // every tile of the three products exactly once
+        using Key = std::tuple<int, int32_t, int, int, int>;
+        std::map<Key, int> want;
+        for (const TileItem& t : tsx) ++want[Key{OP_SYRK_X, t.unit, t.ti, t.tj, t.n_off}];
+        for (const TileItem& t : tsa) ++want[Key{OP_SYRK_A, t.unit, t.ti, t.tj, t.n_off}];
+        for (const TileItem& t : tg) ++want[Key{OP_GEMM_BX, t.unit, t.ti, t.tj, t.n_off}];
+        for (const TileItem& t : v)
+            --want[Key{t.flags & TILE_OP_MASK, t.unit, t.ti, t.tj, t.n_off}];
+        for (const auto& kv : want)
+            if (kv.second != 0)
+                return fail(h, MUON_ERR_STATE, where + "a tile is missing or repeated");
+        if (static_cast<int>(offs.size()) != pairs + 1 || offs[0] != 0 ||
+            offs[pairs] != static_cast<int32_t>(v.size()) ||
+            static_cast<int>(ends.size()) != pairs)
+            return fail(h, MUON_ERR_STATE, where + "pair offsets do not cover the list");
+        for (int p = 0; p < pairs; ++p) {
+            if (offs[p] > offs[p + 1])
+                return fail(h, MUON_ERR_STATE, where + "pair offsets decrease");
+            // stage order: first products, second products, X updates
+            int prev = OP_SYRK_X, first_gemm = offs[p + 1];
+            for (int k = offs[p]; k < offs[p + 1]; ++k) {
+                const int op = v[k].flags & TILE_OP_MASK;
+                if (op < prev)
+                    return fail(h, MUON_ERR_STATE,
+                                where + "pair " + std::to_string(p) + " is not in stage order");
+                if (op == OP_GEMM_BX && first_gemm == offs[p + 1]) first_gemm = k;
+                prev = op;
+            }
+            if (ends[p] != first_gemm)
+                return fail(h, MUON_ERR_STATE,
+                            where + "pair " + std::to_string(p) + ": wrong end before X updates");
+        }
     }
     return MUON_OK;
 }

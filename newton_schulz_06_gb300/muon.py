@@ -213,6 +213,11 @@ class HostPlanner:
               self._h)
         return {k: getattr(info, k) for k, _ in info._fields_}
 
+    def check_chain_schedule(self, mode=_lib.MUON_FULL, nb=1) -> None:
+        """Raises if a chained launch's per-pair tile lists for these shapes
+        would break the properties its waits rely on."""
+        check(lib().muon_debug_check_chain_schedule(self._h, mode, nb), self._h)
+
     def close(self):
         if self._h:
             lib().muon_destroy(self._h)

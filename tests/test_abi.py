@@ -197,3 +197,20 @@ def test_chained_launch_only_for_few_large_matrices(L):
     assert _planner([(2048, 2048)]).plan_info()["chained_groups"] == 0
     assert _planner([(2048, 8192)]).plan_info()["chained_groups"] == 1
     assert _planner([(256, 512)]).plan_info()["chained_groups"] == 0
+
+
+@pytest.mark.parametrize("shapes,mode,nb", [
+    ([(4096, 4096)], "full", 1),
+    ([(6144, 1536), (300, 300), (96, 1000)], "full", 1),
+    ([(2048, 4096)], "blockwise", 2),
+    ([(512, 768), (768, 2048), (2048, 640), (256, 4096), (1000, 1000)], "full", 1),
+    ([(256, 512)], "full", 1),
+    ([(7168, 2048)] * 6 + [(2048, 7168)] * 6 + [(1536, 7168), (7168, 8192)], "full", 1),
+])
+def test_chain_schedule_stage_order_and_coverage(L, shapes, mode, nb):
+    """The chained launch's per-pair lists (built on the host, whatever the
+    size bounds) hold every tile once, in stage order per pair, with
+    consistent offsets and last-iteration ends: the properties its waits need
+    to end (each wait only on earlier stages)."""
+    from newton_schulz_06_gb300 import mode_code
+    _planner(shapes).check_chain_schedule(mode_code(mode), nb)
