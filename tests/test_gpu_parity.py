@@ -380,6 +380,43 @@ def test_chained_default_sizes_match_oracle(rows, cols, mode, nb, monkeypatch):
     assert torch.equal(trip[0], clone[0])
 
 
+def test_chained_groups_from_a_small_workspace_bitexact(monkeypatch):
+    """A workspace that holds one matrix at a time: every group runs its own
+    chained launch (own counter block and rounds), over two steps, with the
+    same bits as one launch per product."""
+    monkeypatch.setenv("MUON_CHAIN_MIN_TILES", "0")
+    shapes = [(1024, 2048), (768, 1536), (1536, 768), (512, 2048)]
+    a = [case(r, c, 1030 + i) for i, (r, c) in enumerate(shapes)]
+    b = [[t.clone() for t in tr] for tr in a]
+    probe = Muon(a)
+    mn, _ = probe.workspace_size()
+    probe.close()
+    _, _, o1, opt = gpu_step(a, steps=2, max_workspace=mn)
+    info = opt.plan_info()
+    assert info["groups"] > 1 and info["chained_groups"] == info["groups"], info
+    monkeypatch.setenv("MUON_FUSE_STAGES", "0")
+    _, _, o2, _ = gpu_step(b, steps=2, max_workspace=mn)
+    for i in range(len(shapes)):
+        assert torch.equal(o1[i], o2[i]), shapes[i]
+        assert torch.equal(a[i][0], b[i][0]), shapes[i]
+
+
+def test_chained_fp32_weights_match_oracle(monkeypatch):
+    """fp32 weights (no TMA-folded update): the chain stops before the last X
+    update and the separate update pass writes W; within tolerance of the
+    oracle and the same bits as one launch per product."""
+    monkeypatch.setenv("MUON_CHAIN_MIN_TILES", "0")
+    trip = case(768, 1536, 1040, w_dtype=torch.float32, g_dtype=torch.float32)
+    clone = [t.clone() for t in trip]
+    inp, wexp, oexp, opt = gpu_step([trip])
+    assert opt.plan_info()["chained_groups"] == 1
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], oracle_step(inp[0]))
+    monkeypatch.setenv("MUON_FUSE_STAGES", "0")
+    _, _, o2, _ = gpu_step([clone])
+    assert torch.equal(oexp[0], o2[0])
+    assert torch.equal(trip[0], clone[0])
+
+
 def test_chain_counters_zeroed_and_restarted_bitexact(monkeypatch):
     """The chained launches' row counters only grow across steps; when a
     step's targets would pass the limit the group's counters are zeroed and
