@@ -1048,9 +1048,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
         // (warp - 2) / 4 (chunks 4h .. 4h + 3 of the 256 columns).  Blocks of
         // 32 x 32 go out through two alternating swizzled shared-memory
         // stages and TMA stores (which also clip at the matrix edge); the
-        // epilogue's input blocks (X for the GEMM, A for SYRK-2, plus W when
-        // the update is folded in) come in by TMA two blocks ahead, the first
-        // two of a tile while its main loop still runs.
+        // epilogue's input blocks (X for the GEMM, A for SYRK-2) come in by
+        // TMA two blocks ahead, the first two of a tile while its main loop
+        // still runs.  With the update folded in, the W block of each output
+        // block comes too: beside the X block in one slot (FW), or as the
+        // next item in the ring (a chained launch's last X update), so one
+        // block ahead.
         const int ew = warp - 2;
         const int lg = warp & 3;
         const int half = ew >> 2;
