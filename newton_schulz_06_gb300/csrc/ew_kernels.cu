@@ -105,21 +105,6 @@ __device__ __forceinline__ TileGeom tile_geom(const EwUnit& U, int u,
     return g;
 }
 
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, off);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float s = 0.f;
-    if (threadIdx.x == 0) {
-#pragma unroll
-        for (int w = 0; w < EW_THREADS / 32; ++w) s += red[w];
-    }
-    return s;   // valid in thread 0
-}
-
 // Tile-constant fields of a unit in registers (the kernels store through
 // pointers the compiler cannot tell apart from the unit table).
 struct EwU {

@@ -578,7 +578,7 @@ template <bool DBG>
 __device__ __forceinline__ void fused_update_block(const EpiUnit& u, int r0w, int gc0, int lane,
                                                    const float (&v)[32], const uint8_t* s_w,
                                                    uint8_t* stage) {
-    if (!DBG) {
+    if constexpr (!DBG) {
         // the same arithmetic, eight elements at a time (fewer live
         // registers): O = bf16(v), through the stage as O^T when the unit is
         // transposed (then each lane reads and rewrites only its own row)
@@ -620,43 +620,43 @@ __device__ __forceinline__ void fused_update_block(const EpiUnit& u, int r0w, in
             *reinterpret_cast<uint4*>(stage + sw64(lane, q)) = out;
         }
         store_block(u.te_w, stage, u.transposed ? r0w : gc0, u.transposed ? gc0 : r0w, lane);
-        return;
-    }
-    float o[32], w[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) o[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
-    int wrow, wcol0, wrows, wcols;      // this lane's W row segment
-    if (!u.transposed) {
-        ld_row_bf16(s_w, lane, w);
-        wrow = r0w + lane;
-        wcol0 = gc0;
-        wrows = u.m;
-        wcols = u.n;
     } else {
-        // O^T through the stage: lane jj then owns W row gc0 + jj
-        st_col_bf16(stage, lane, o);
-        __syncwarp();
-        ld_row_bf16(stage, lane, o);
-        ld_row_bf16(s_w, lane, w);
-        __syncwarp();                   // all reads of the stage are done
-        wrow = gc0 + lane;
-        wcol0 = r0w;
-        wrows = u.n;
-        wcols = u.m;
-    }
-#pragma unroll
-    for (int e = 0; e < 32; ++e) w[e] = fmaf(-u.step, o[e], w[e]);
-    st_row_bf16(stage, lane, w);
-    if (DBG && (u.w_dbg || u.o_dbg) && wrow < wrows) {
-        const int64_t doff = static_cast<int64_t>(wrow) * u.ld_dbg + wcol0;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            if (wcol0 + e >= wcols) break;
-            if (u.w_dbg) u.w_dbg[doff + e] = w[e];
-            if (u.o_dbg) u.o_dbg[doff + e] = __float2bfloat16_rn(o[e]);
+        float o[32], w[32];
+    #pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
+        int wrow, wcol0, wrows, wcols;      // this lane's W row segment
+        if (!u.transposed) {
+            ld_row_bf16(s_w, lane, w);
+            wrow = r0w + lane;
+            wcol0 = gc0;
+            wrows = u.m;
+            wcols = u.n;
+        } else {
+            // O^T through the stage: lane jj then owns W row gc0 + jj
+            st_col_bf16(stage, lane, o);
+            __syncwarp();
+            ld_row_bf16(stage, lane, o);
+            ld_row_bf16(s_w, lane, w);
+            __syncwarp();                   // all reads of the stage are done
+            wrow = gc0 + lane;
+            wcol0 = r0w;
+            wrows = u.n;
+            wcols = u.m;
         }
+    #pragma unroll
+        for (int e = 0; e < 32; ++e) w[e] = fmaf(-u.step, o[e], w[e]);
+        st_row_bf16(stage, lane, w);
+        if ((u.w_dbg || u.o_dbg) && wrow < wrows) {
+            const int64_t doff = static_cast<int64_t>(wrow) * u.ld_dbg + wcol0;
+    #pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                if (wcol0 + e >= wcols) break;
+                if (u.w_dbg) u.w_dbg[doff + e] = w[e];
+                if (u.o_dbg) u.o_dbg[doff + e] = __float2bfloat16_rn(o[e]);
+            }
+        }
+        store_block(u.te_w, stage, u.transposed ? r0w : gc0, u.transposed ? gc0 : r0w, lane);
     }
-    store_block(u.te_w, stage, u.transposed ? r0w : gc0, u.transposed ? gc0 : r0w, lane);
 }
 
 // The tiles of pair `pair`: a planner-built range, or a stride over all.

@@ -556,6 +556,7 @@ cudaError_t launch_ns(NsOp op, const NsLaunch& p, int grid, cudaStream_t s) {
         case OP_SYRK_X: return launch_op<OP_SYRK_X>(p, grid, s);
         case OP_SYRK_A: return launch_op<OP_SYRK_A>(p, grid, s);
         case OP_GEMM_BX: return launch_op<OP_GEMM_BX>(p, grid, s);
+        case OP_CHAIN: break;                  // chained launches run on CTA pairs only
     }
     return cudaErrorInvalidValue;
 }
