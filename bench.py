@@ -6,6 +6,9 @@
 A step is one full Muon step (momentum, normalisation, five Newton-Schulz
 iterations, weight update) over every matrix of the workload, with a fresh
 synthetic gradient written before each step (outside the timed events).
+The headline workload is the 4096 x 4096 bf16 matrix; the Qwen3-30B-A3B
+block (388 matrices) is timed in the same run and reported under
+"workloads" (--extra-workloads).
 The metric is Muon-step TFLOP/s in useful FLOPs (symmetric products counted
 on their upper triangle); GEMM-equivalent TFLOP/s, % of the measured dense
 bf16 peak, ms/step and matrices/s are reported beside it.  L2 is flushed
@@ -242,24 +245,20 @@ def run_reference(args, wl, world, rank):
 E2E_MAX_HOST_BYTES = 8 << 30
 
 
-def run_ours(args, wl, world, rank, local, pg):
+def device_timing(wl, args, dev, pg, steps):
+    """Builds the workload's state on `dev` and times `steps` Muon steps
+    (after the warm-up), each between CUDA events on the launch stream with
+    L2 flushed before it; then `steps` more with libmuon's per-launch events
+    for the stage split.  Returns the handle, its tensors and the timings."""
     import torch
-    import __graft_entry__
-    __graft_entry__.build()
-    from newton_schulz_06_gb300 import Muon, flops, mode_code
+    from newton_schulz_06_gb300 import Muon, mode_code
     from newton_schulz_06_gb300 import inputs as I
-
-    torch.cuda.set_device(local)
-    dev = f"cuda:{local}"
-    peaks, peak_kind = load_peaks()
     Ws, Gs, Ms = I.make_state(wl, dev)
     trips = list(zip(Ws, Gs, Ms))
     opt = Muon(trips)
     mode = mode_code(wl.mode)
     opt.ensure_workspace(mode, wl.nb, args.max_workspace)
     info = opt.plan_info(mode, wl.nb)
-    useful = flops.useful_flops(wl.shapes, mode=wl.mode, nb=wl.nb)
-    gemm_eq = flops.gemm_equiv_flops(wl.shapes, mode=wl.mode, nb=wl.nb)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -270,10 +269,6 @@ def run_ours(args, wl, world, rank, local, pg):
 
     kw = dict(lr=0.02, beta=0.95, nesterov=True, ns_steps=5, mode=mode,
               nb=wl.nb)
-    # clocks are sampled from the first warm-up step to the end of the
-    # end-to-end loop, a window that contains the timed region
-    sampler = ClockSampler(local)
-    sampler.start()
     for k in range(args.warmup):
         fresh_grads(k + 1)
         opt.step(**kw)
@@ -284,12 +279,12 @@ def run_ours(args, wl, world, rank, local, pg):
     # no per-launch events here (they would serialise the kernels'
     # programmatic launch overlap)
     ev = [(torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     barrier(pg)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     launches = 0
-    for k in range(args.steps):
+    for k in range(steps):
         fresh_grads(args.warmup + k + 1)
         flush.zero_()
         ev[k][0].record(stream)
@@ -299,17 +294,15 @@ def run_ours(args, wl, world, rank, local, pg):
     torch.cuda.synchronize()
     barrier(pg)
     wall = time.perf_counter() - wall0
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = statistics.mean(step_ms)
-    ms = max_over_ranks(pg, ms)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
 
     # per-kernel durations: K more steps right after, with CUDA events
     # around every launch (libmuon's stage timing, on the same stream)
     opt.set_profiling(True)
     stage_tot = {}
     prof_ms = []
-    for k in range(args.steps):
-        fresh_grads(args.warmup + args.steps + k + 1)
+    for k in range(steps):
+        fresh_grads(args.warmup + steps + k + 1)
         flush.zero_()
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
@@ -322,6 +315,76 @@ def run_ours(args, wl, world, rank, local, pg):
             t, c = stage_tot.get(name, (0.0, 0))
             stage_tot[name] = (t + tms, c + n)
     opt.set_profiling(False)
+    del flush
+    return dict(opt=opt, trips=trips, kw=kw, info=info, ms=ms, wall=wall,
+                launches=launches, stage_tot=stage_tot, prof_ms=prof_ms,
+                fresh_grads=fresh_grads)
+
+
+def roofline_of(wl, t, peak, peak_kind):
+    """The dominant tensor-core kernel of a timed workload: per-launch
+    algorithmic FLOPs / its mean event-timed launch duration."""
+    from newton_schulz_06_gb300 import flops
+    stage_tot, info = t["stage_tot"], t["info"]
+    units = []
+    for r, c in wl.shapes:
+        units += flops.unit_shapes(r, c, wl.mode, wl.nb)
+    per_launch = {
+        "gemm": sum(2 * m * m * n for m, n in units),
+        "syrk1": sum(m * (m + 1) * n for m, n in units),
+        "syrk2": sum(m * (m + 1) * m for m, n in units),
+    }
+    # a chained launch runs every product of the step, the last X update too
+    # unless that one ran as its own launch
+    ns = t["kw"].get("ns_steps", 5)
+    gemm_alone = stage_tot.get("gemm", (0, 0))[1] > 0
+    per_launch["chain"] = (ns * (per_launch["syrk1"] + per_launch["syrk2"])
+                           + (ns - 1 if gemm_alone else ns) * per_launch["gemm"])
+    dom = max((k for k in per_launch if stage_tot.get(k, (0, 0))[1]),
+              key=lambda k: stage_tot[k][0])
+    t_dom, n_dom = stage_tot[dom]
+    avg_launch_s = t_dom / n_dom / 1e3
+    # per_launch counts every unit; with the workspace split into groups each
+    # unit is in one group's launch, so the mean launch holds 1/groups of it
+    # (all groups chained alike, as they are for these workloads)
+    achieved = per_launch[dom] / max(1, info["groups"]) / avg_launch_s / 1e12
+    op = {"gemm": 2, "syrk1": 0, "syrk2": 1, "chain": 3}[dom]
+    pair = os.environ.get("MUON_CTA_GROUP", "2") != "1"
+    kname = f"ns2_kernel<{op}>" if pair else f"ns_kernel<{op}>"
+    return {"bound": "tensor", "kernel": kname, "stage": dom,
+            "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "peak_kind": f"{peak_kind} dense bf16 (burst)",
+            "traffic": traffic_for(kname, wl.name),
+            "avg_launch_ms": t_dom / n_dom,
+            "timing": "CUDA events around each launch of the kernel, on its stream, "
+                      "over K steps run right after the timed region"}
+
+
+def run_ours(args, wl, world, rank, local, pg):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from newton_schulz_06_gb300 import Muon, flops
+    from newton_schulz_06_gb300 import inputs as I
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    peaks, peak_kind = load_peaks()
+    peak = peaks["bf16_tflops"]
+    useful = flops.useful_flops(wl.shapes, mode=wl.mode, nb=wl.nb)
+    gemm_eq = flops.gemm_equiv_flops(wl.shapes, mode=wl.mode, nb=wl.nb)
+    # clocks are sampled from the first warm-up step to the end of the
+    # last measurement, a window that contains the timed regions
+    sampler = ClockSampler(local)
+    sampler.start()
+    t = device_timing(wl, args, dev, pg, args.steps)
+    opt, trips, kw, info = t["opt"], t["trips"], t["kw"], t["info"]
+    Ws = [x[0] for x in trips]
+    Gs = [x[1] for x in trips]
+    ms = max_over_ranks(pg, t["ms"])
+    stage_tot = t["stage_tot"]
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     # end to end through the C ABI with host buffers (muon_step_host): the
     # step's gradients in from pinned memory, the step, the weights back out.
@@ -339,7 +402,7 @@ def run_ours(args, wl, world, rank, local, pg):
     e2e_useful = useful
     if e2e_n < len(Gs):
         e2e_opt = Muon(trips[:e2e_n])
-        e2e_opt.ensure_workspace(mode, wl.nb, args.max_workspace)
+        e2e_opt.ensure_workspace(kw["mode"], wl.nb, args.max_workspace)
         e2e_useful = flops.useful_flops(wl.shapes[:e2e_n], mode=wl.mode, nb=wl.nb)
     pinned_g = [torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
                 for G in Gs[:e2e_n]]
@@ -347,8 +410,8 @@ def run_ours(args, wl, world, rank, local, pg):
         pinned_g[i].copy_(G)
     pinned_w = [torch.empty(W.shape, dtype=W.dtype, pin_memory=True)
                 for W in Ws[:e2e_n]]
-    h2d = sum(t.numel() * t.element_size() for t in pinned_g)
-    d2h = sum(t.numel() * t.element_size() for t in pinned_w)
+    h2d = sum(x.numel() * x.element_size() for x in pinned_g)
+    d2h = sum(x.numel() * x.element_size() for x in pinned_w)
     e2e_ms = []
     for k in range(max(3, min(args.steps, 10))):
         flush.zero_()
@@ -361,44 +424,41 @@ def run_ours(args, wl, world, rank, local, pg):
     e2e = max_over_ranks(pg, e2e)
     if e2e_opt is not opt:
         e2e_opt.close()
-    del pinned_g, pinned_w
-    clocks = sampler.stop()
+    del pinned_g, pinned_w, flush
+    roofline = roofline_of(wl, t, peak, peak_kind)
+    prof_ms, wall, launches = t["prof_ms"], t["wall"], t["launches"]
+    n_e2e_all = len(Gs)
+    opt.close()
+    del opt, trips, Ws, Gs, t
 
-    # dominant tensor-core kernel: per-launch algorithmic FLOPs / event time
-    units = []
-    for r, c in wl.shapes:
-        units += flops.unit_shapes(r, c, wl.mode, wl.nb)
-    per_launch = {
-        "gemm": sum(2 * m * m * n for m, n in units),
-        "syrk1": sum(m * (m + 1) * n for m, n in units),
-        "syrk2": sum(m * (m + 1) * m for m, n in units),
-    }
-    # a chained launch runs every product of the step, the last X update too
-    # unless that one ran as its own launch
-    ns = kw.get("ns_steps", 5)
-    gemm_alone = stage_tot.get("gemm", (0, 0))[1] > 0
-    per_launch["chain"] = (ns * (per_launch["syrk1"] + per_launch["syrk2"])
-                           + (ns - 1 if gemm_alone else ns) * per_launch["gemm"])
-    dom = max((k for k in per_launch if stage_tot.get(k, (0, 0))[1]),
-              key=lambda k: stage_tot[k][0])
-    t_dom, n_dom = stage_tot[dom]
-    avg_launch_s = t_dom / n_dom / 1e3
-    # per_launch counts every unit; with the workspace split into groups each
-    # unit is in one group's launch, so the mean launch holds 1/groups of it
-    # (all groups chained alike, as they are for these workloads)
-    achieved = per_launch[dom] / max(1, info["groups"]) / avg_launch_s / 1e12
-    peak = peaks["bf16_tflops"]
-    op = {"gemm": 2, "syrk1": 0, "syrk2": 1, "chain": 3}[dom]
-    pair = os.environ.get("MUON_CTA_GROUP", "2") != "1"
-    kname = f"ns2_kernel<{op}>" if pair else f"ns_kernel<{op}>"
-    roofline = {"bound": "tensor", "kernel": kname, "stage": dom,
-                "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak,
-                "peak_kind": f"{peak_kind} dense bf16 (burst)",
-                "traffic": traffic_for(kname, wl.name),
-                "avg_launch_ms": t_dom / n_dom,
-                "timing": "CUDA events around each launch of the kernel, on its stream, "
-                          "over K steps run right after the timed region"}
+    # further workloads timed in the same run (the target configs besides
+    # the headline one), each with its own state, freed before the next
+    extra = {}
+    for name in [x for x in args.extra_workloads.split(",") if x and x != "none"]:
+        xw = I.workload(name)
+        torch.cuda.empty_cache()
+        xt = device_timing(xw, args, dev, pg, min(args.steps, 10))
+        xu = flops.useful_flops(xw.shapes, mode=xw.mode, nb=xw.nb)
+        xg = flops.gemm_equiv_flops(xw.shapes, mode=xw.mode, nb=xw.nb)
+        xms = max_over_ranks(pg, xt["ms"])
+        extra[name] = {
+            "matrices": xw.n_matrices, "mode": xw.mode, "nb": xw.nb,
+            "steps": min(args.steps, 10), "warmup": args.warmup,
+            "ms_per_step": xms,
+            "useful_tflops": world * xu / (xms / 1e3) / 1e12,
+            "gemm_equiv_tflops": world * xg / (xms / 1e3) / 1e12,
+            "pct_bf16_peak_useful": 100.0 * xu / (xms / 1e3) / 1e12 / peak,
+            "pct_bf16_peak_gemm_equiv": 100.0 * xg / (xms / 1e3) / 1e12 / peak,
+            "stage_ms_per_step": {k: v[0] / len(xt["prof_ms"])
+                                  for k, v in xt["stage_tot"].items()},
+            "ms_per_step_with_stage_events": statistics.mean(xt["prof_ms"]),
+            "gpu_launches": xt["launches"],
+            "roofline": roofline_of(xw, xt, peak, peak_kind),
+        }
+        xt["opt"].close()
+        del xt
+        torch.cuda.empty_cache()
+    clocks = sampler.stop()
 
     value = world * useful / (ms / 1e3) / 1e12
     line = {
@@ -425,10 +485,12 @@ def run_ours(args, wl, world, rank, local, pg):
                 "unit": "TFLOP/s", "ms_per_step": e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "muon_step_host: G from pinned host memory, the step, W back",
-                "matrices": e2e_n if e2e_n < len(Gs) else "all"},
+                "matrices": e2e_n if e2e_n < n_e2e_all else "all"},
         "gpu_launches": launches,
         "roofline": roofline,
     }
+    if extra:
+        line["workloads"] = extra
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         idx = oracle_sample(wl)
         host = host_sample(wl, idx)
@@ -440,7 +502,6 @@ def run_ours(args, wl, world, rank, local, pg):
             "sample": (f"{len(idx)} of {wl.n_matrices} matrices "
                        f"({u / full_useful:.3%} of the step's useful FLOPs), "
                        f"one float64 oracle step, {dt:.1f} s")}
-    opt.close()
     return line
 
 
@@ -453,6 +514,9 @@ def main():
     ap.add_argument("--workload", default="square_4096_bf16")
     ap.add_argument("--max-workspace", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra-workloads", default="qwen3_30b_a3b_block",
+                    help="comma-separated workloads also timed in the same run "
+                         "and reported under 'workloads' ('none': skip)")
     ap.add_argument("--max-matrices", type=int, default=None,
                     help="profiling aid: keep only the first N matrices")
     args = ap.parse_args()

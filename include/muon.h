@@ -204,6 +204,18 @@ MUON_API int muon_debug_set_exports(muon_handle h, int n, float* const* w_f32,
  * CUDA context stays usable.  Makes no other change. */
 MUON_API int muon_debug_wait_timeout(muon_handle h, int* err_word, int limit_ms);
 
+/* Validation of the chained launch (see muon_get_plan_info: groups of few
+ * large matrices run every product of a step in one launch whose tiles wait
+ * on per-tile counters).  skew_rounds > 0 makes the second products of later
+ * chained launches wait for that many counter rounds more than will ever be
+ * completed, so their bounded waits run out and muon_sync reports
+ * MUON_ERR_TIMEOUT (a timeout test without a fault; 0 = off).  counter_limit
+ * is the counter target from which a group's tile counters are zeroed before
+ * a step (1 .. 2^30; 0 = the default 2^30): a small limit exercises the
+ * restart.  Applies to later steps of this handle; MUON_ERR_INVALID_ARG for
+ * values out of range. */
+MUON_API int muon_debug_set_chain_test(muon_handle h, int skew_rounds, int64_t counter_limit);
+
 /* Host-only check of the chained launch's schedule for `mode`/`nb`: for every
  * group of the registered matrices (ignoring the size bounds that decide
  * whether a group chains), builds the per-pair tile lists and checks that
@@ -253,8 +265,11 @@ MUON_API int muon_get_plan_info(muon_handle h, int mode, int nb, muon_plan_info*
  *     4096 matrix fits, a 2048 x 2048 does not).  Larger matrices are
  *     rejected with MUON_ERR_UNSUPPORTED and a message before any GPU work.
  *   - The array exists once per device that loads this code and is held
- *     until the process exits.  The first call on a device resolves its
- *     address (cudaGetSymbolAddress) with that device current.
+ *     until the process exits.  The first call on a device is its set-up:
+ *     it resolves the array's address (cudaGetSymbolAddress) with that
+ *     device current, so make that first call before any stream capture.
+ *     The address is resolved again only if the device's context has been
+ *     replaced since (for example after cudaDeviceReset).
  *   - Every call reuses the same array and overwrites what the previous
  *     call left there; calls whose GPU work overlaps (different streams or
  *     threads) race and give wrong results.  Queue them on one stream.

@@ -36,7 +36,7 @@ EXPORTS = ("muon_create", "muon_set_stream", "muon_register_params",
            "muon_set_profiling", "muon_stage_times", "muon_last_launch_count",
            "muon_debug_set_exports", "muon_get_plan_info",
            "muon_step_noalloc", "muon_debug_wait_timeout", "muon_step_host",
-           "muon_debug_check_chain_schedule")
+           "muon_debug_check_chain_schedule", "muon_debug_set_chain_test")
 
 
 class MuonParam(ctypes.Structure):
@@ -103,6 +103,7 @@ def lib() -> ctypes.CDLL:
                               f32, f32, f32, vp, ctypes.c_char_p, sz],
         "muon_debug_wait_timeout": [H, vp, i32],
         "muon_debug_check_chain_schedule": [H, i32, i32],
+        "muon_debug_set_chain_test": [H, i32, ctypes.c_int64],
         "muon_step_host": [H, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), f32,
                            f32, i32, i32, f32, f32, f32, i32, i32],
     }

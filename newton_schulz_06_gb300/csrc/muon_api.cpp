@@ -129,8 +129,8 @@ struct muon_ctx {
     int chain_max_tiles = 8;   // X-update tiles per CTA pair up to which groups chain
     int chain_min_tiles = -1;  // X-update tiles from which groups chain (-1: one per pair)
     bool chain_last = true;    // a chain also runs the last X update (weight update folded in)
-    // failure test only: rounds added to what a chained launch's second
-    // products wait for, so their waits run out (MUON_DEBUG_CHAIN_SKEW)
+    // failure test only (muon_debug_set_chain_test): rounds added to what a
+    // chained launch's second products wait for, so their waits run out
     int debug_chain_skew = 0;
     int max_pairs = 0;
 };
@@ -842,15 +842,10 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     if (const char* pd = std::getenv("MUON_PDL")) set_programmatic_launch(std::string(pd) != "0");
     if (const char* fs = std::getenv("MUON_FUSE_STAGES")) h->fuse_stages = std::string(fs) != "0";
     if (const char* cl = std::getenv("MUON_CHAIN_LAST")) h->chain_last = std::string(cl) != "0";
-    if (const char* sk = std::getenv("MUON_DEBUG_CHAIN_SKEW")) h->debug_chain_skew = std::atoi(sk);
     if (const char* cn = std::getenv("MUON_CHAIN_MIN_TILES")) h->chain_min_tiles = std::atoi(cn);
     if (const char* cm = std::getenv("MUON_CHAIN_MAX_TILES")) {
         const int v = std::atoi(cm);
         if (v >= 0) h->chain_max_tiles = v;
-    }
-    if (const char* rl = std::getenv("MUON_FUSE_COUNTER_LIMIT")) {
-        const long long v = std::atoll(rl);
-        if (v > 0 && v <= (1ll << 30)) h->rc_limit = v;
     }
     if (const char* st = std::getenv("MUON_STAGES")) {
         const int v = std::atoi(st);
@@ -1234,6 +1229,17 @@ int muon_debug_set_exports(muon_handle h, int n, float* const* w_f32, void* cons
         if (o_bf16) h->exp_o[i] = o_bf16[i];
     }
     h->plan.valid = false;
+    return MUON_OK;
+}
+
+int muon_debug_set_chain_test(muon_handle h, int skew_rounds, int64_t counter_limit) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (skew_rounds < 0 || skew_rounds > (1 << 20))
+        return fail(h, MUON_ERR_INVALID_ARG, "skew_rounds must be in 0..2^20");
+    if (counter_limit < 0 || counter_limit > (int64_t(1) << 30))
+        return fail(h, MUON_ERR_INVALID_ARG, "counter_limit must be in 0..2^30");
+    h->debug_chain_skew = skew_rounds;
+    h->rc_limit = counter_limit ? counter_limit : (int64_t(1) << 30);
     return MUON_OK;
 }
 

@@ -179,19 +179,36 @@ void set_programmatic_launch(bool on);
 bool programmatic_launch();
 
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                 cudaStream_t s, Args&&... args) {
+inline cudaError_t launch_kernel_attr(void (*kern)(KArgs...), dim3 grid, dim3 block,
+                                      size_t smem, cudaStream_t s, bool cooperative,
+                                      Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (programmatic_launch()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cooperative) {
+        // every block of the grid resident at once, or the launch is refused
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = programmatic_launch() ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, Args&&... args) {
+    return launch_kernel_attr(kern, grid, block, smem, s, false, std::forward<Args>(args)...);
 }
 
 #ifdef __CUDACC__

@@ -13,14 +13,20 @@
 // The array is NOALLOC_SCRATCH_BYTES (32 MiB).  It exists once per device
 // that loads this code and stays until the process exits; with CUDA's lazy
 // module loading that happens at the first call of this entry point on the
-// device.  Every call shares it, so two calls whose GPU work overlaps (on two
-// streams, or from two threads) race and corrupt each other's results.  The
+// device.  Its device address is resolved at that first call (set-up, with
+// the device current) and cached; it is resolved again only if the device's
+// context was replaced since (after cudaDeviceReset the module is loaded
+// anew, possibly elsewhere).  Every call shares the array, so two calls
+// whose GPU work overlaps (on two streams, or from two threads) race and
+// corrupt each other's results.  The
 // planner, kernels and launch sequence are the ones muon_step uses (the
 // tables are rebuilt and uploaded on every call), so a matrix gets the same
 // bits from either entry point.
 #include <cstdio>
 #include <mutex>
 #include <string>
+
+#include <cudaTypedefs.h>
 
 #include "../../include/muon.h"
 #include "muon_internal.h"
@@ -42,23 +48,54 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH
 
 struct NoallocDevice {
     bool ready = false;
-    void* scratch = nullptr;   // device address of g_noalloc_scratch
+    void* scratch = nullptr;        // device address of g_noalloc_scratch
+    unsigned long long ctx_id = 0;  // the context it was resolved in
 };
 
 NoallocDevice g_dev[NA_MAX_DEVICES];
 std::mutex g_dev_mutex;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
 
 int na_fail(char* err, size_t len, int code, const std::string& msg) {
     if (err && len) std::snprintf(err, len, "%s", msg.c_str());
     return code;
 }
 
-// Once per device, with that device current: resolve the array's device
-// address (in host code its name is only a stand-in, not a device address).
+// The unique id of the calling thread's current context (0 if none is
+// current yet).  Driver functions are resolved once through the runtime.
+bool current_ctx_id(unsigned long long* id) {
+    *id = 0;
+    if (!g_ctx_current || !g_ctx_id) {
+        void* f0 = nullptr;
+        void* f1 = nullptr;
+        cudaDriverEntryPointQueryResult q0, q1;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f0, 4000, cudaEnableDefault,
+                                             &q0) != cudaSuccess ||
+            q0 != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f1, 12000, cudaEnableDefault,
+                                             &q1) != cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess || !f0 || !f1)
+            return false;
+        g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f0);
+        g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f1);
+    }
+    CUcontext c = nullptr;
+    if (g_ctx_current(&c) != CUDA_SUCCESS) return false;
+    if (!c) return true;
+    return g_ctx_id(c, id) == CUDA_SUCCESS;
+}
+
+// Set-up, once per device with that device current: resolve the array's
+// device address (in host code its name is only a stand-in, not a device
+// address).  Resolved again only if the device's context was replaced.
 int na_setup(int dev, void** out, char* err, size_t len) {
     std::lock_guard<std::mutex> lock(g_dev_mutex);
     NoallocDevice& d = g_dev[dev];
-    if (!d.ready) {
+    unsigned long long id = 0;
+    if (!current_ctx_id(&id))
+        return na_fail(err, len, MUON_ERR_CUDA, "cannot query the current CUDA context");
+    if (!d.ready || id == 0 || id != d.ctx_id) {
         void* p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p)
@@ -67,7 +104,11 @@ int na_setup(int dev, void** out, char* err, size_t len) {
                                cudaGetErrorString(e));
         const uintptr_t base = (reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023);
         d.scratch = reinterpret_cast<void*>(base);
-        d.ready = true;
+        // the lookup made the device's primary context current if it was not
+        if (!current_ctx_id(&id))
+            return na_fail(err, len, MUON_ERR_CUDA, "cannot query the current CUDA context");
+        d.ctx_id = id;
+        d.ready = id != 0;
     }
     *out = d.scratch;
     return MUON_OK;

@@ -1311,8 +1311,11 @@ cudaError_t launch_pair_st(const NsLaunch& p, int pairs, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_done[dev] = 1;
     }
-    return launch_kernel(ns2_kernel<OP, ST, FW, SL>, dim3(2 * pairs), dim3(p_threads<OP>()),
-                         p_smem<ST, FW>(), s, p);
+    // A chained launch's tiles wait on tiles of other pairs, so all of its
+    // pairs must be resident together: it is launched cooperatively, and a
+    // grid that cannot be co-resident is refused instead of left to stall.
+    return launch_kernel_attr(ns2_kernel<OP, ST, FW, SL>, dim3(2 * pairs),
+                              dim3(p_threads<OP>()), p_smem<ST, FW>(), s, OP == OP_CHAIN, p);
 }
 
 template <int OP>

@@ -8,12 +8,14 @@ compare with the tolerances of the step:
     update computes before it is stored (bf16 rounding of a N(0, 0.02)
     weight alone is ~1.7e-3), plus a bit-exact check that the stored bf16
     weight is the round-to-nearest-even of that fp32 value; fp32 weights are
-    compared directly.  The weight error is the O error scaled by
-    r = lr*scale*||O|| / ||W||, so the 1e-3 gate holds where r <= 1/30 (every
-    model-sized matrix); for small test matrices with a larger r the gate is
-    3e-2 * r.  Independently of size, the fp32 weight must equal
-    W - lr*scale*O_gpu within fp32 rounding (the update applied exactly the
-    exported O);
+    compared directly.  This fixed 1e-3 gate is the default and applies to
+    the single fp32 256 x 512 matrix and to every workload-sized matrix.
+    The weight error is the O error scaled by r = lr*scale*||O|| / ||W||,
+    which for W ~ N(0, 0.02) is about 1/sqrt(cols); small test shapes made
+    only to reach ragged tiles (cols of a few hundred or less, r up to 0.25)
+    opt in to a gate of max(1e-3, 3e-2 * r) with w_gate="scaled".
+    Independently of size, the fp32 weight must equal W - lr*scale*O_gpu
+    within fp32 rounding (the update applied exactly the exported O);
   * momentum: fp32 M = fma(beta, M, G) against the float64 value, within
     one fp32 rounding.
 """
@@ -47,11 +49,14 @@ def to_np(t):
 
 def gpu_step(triples, *, lr=0.02, beta=0.95, nesterov=True, ns_steps=5,
              coeffs=COEFFS, mode="full", nb=1, exports=True,
-             max_workspace=None, steps=1):
+             max_workspace=None, steps=1, chain_test=None):
     """Runs `steps` Muon steps on device tensors in place; returns
-    (host copies of the inputs, fp32 W exports, bf16 O exports, opt)."""
+    (host copies of the inputs, fp32 W exports, bf16 O exports, opt).
+    chain_test: (skew_rounds, counter_limit) for muon_debug_set_chain_test."""
     inputs = [(to_np(W), to_np(G), to_np(M)) for W, G, M in triples]
     opt = Muon(triples)
+    if chain_test is not None:
+        opt.set_chain_test(*chain_test)
     md = mode_code(mode)
     opt.ensure_workspace(md, nb, max_workspace)
     wexp = oexp = None
@@ -78,8 +83,12 @@ def oracle_step(inp, *, lr=0.02, beta=0.95, nesterov=True, ns_steps=5,
                             c=c, mode=mode, nb=nb)
 
 
-def check_against_oracle(triple, inp, wexp, oexp, ref, *, mode="full", nb=1):
-    """Asserts the three tolerances for one parameter; returns the errors."""
+def check_against_oracle(triple, inp, wexp, oexp, ref, *, mode="full", nb=1,
+                         w_gate="fixed"):
+    """Asserts the three tolerances for one parameter; returns the errors.
+    w_gate: "fixed" (relF(W) <= 1e-3) or "scaled" (small test shapes:
+    max(1e-3, 3e-2 * r))."""
+    assert w_gate in ("fixed", "scaled")
     W, G, M = triple
     rows, cols = W.shape
     errs = {}
@@ -97,7 +106,7 @@ def check_against_oracle(triple, inp, wexp, oexp, ref, *, mode="full", nb=1):
     W_in = inp[0]
     step = np.linalg.norm(ref["W"] - W_in)
     ratio = step / max(np.linalg.norm(ref["W"]), 1e-300)
-    w_tol = max(W_TOL, O_TOL * ratio)
+    w_tol = W_TOL if w_gate == "fixed" else max(W_TOL, O_TOL * ratio)
     errs["W_tol"] = w_tol
     assert errs["W"] <= w_tol, errs
     # the update applied the exported O exactly (fp32 fma, one rounding)

@@ -155,6 +155,12 @@ def test_register_rejects_bad_params(L):
     assert reg() == 0
     assert lib.muon_step(h, 0.02, 0.95, 1, 5, 3.4445, -4.775, 2.0315, 0,
                          1) == L.MUON_ERR_STATE
+    # the chained launch's validation switches are an explicit call (no
+    # environment variable can turn them on); out-of-range values rejected
+    assert lib.muon_debug_set_chain_test(h, 0, 0) == 0
+    assert lib.muon_debug_set_chain_test(h, 3, 1) == 0
+    assert lib.muon_debug_set_chain_test(h, -1, 0) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_debug_set_chain_test(h, 0, (1 << 30) + 1) == L.MUON_ERR_INVALID_ARG
     assert lib.muon_destroy(h) == 0
 
 

@@ -25,19 +25,21 @@ def test_bounded_wait_runs_out_and_context_survives():
     # the context still runs the real kernels correctly
     trip = list(random_case(192, 320, 4, device=DEV))
     inp, wexp, oexp, _ = gpu_step([trip])
-    check_against_oracle(trip, inp[0], wexp[0], oexp[0], oracle_step(inp[0]))
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], oracle_step(inp[0]),
+                         w_gate="scaled")
 
 
 def test_chained_launch_wait_runs_out_and_context_survives(monkeypatch):
     """A chained launch whose second products wait for counter rounds that
-    never come (a debug skew): the watcher's and the other bounded waits run
-    out after the limit, the step reports MUON_ERR_TIMEOUT at sync, and a new
-    handle steps correctly on the same context."""
+    never come (the skew of muon_debug_set_chain_test): the watcher's and the
+    other bounded waits run out after the limit, the step reports
+    MUON_ERR_TIMEOUT at sync, and a new handle steps correctly on the same
+    context."""
     monkeypatch.setenv("MUON_CHAIN_MIN_TILES", "0")
     monkeypatch.setenv("MUON_WAIT_LIMIT_MS", "300")
-    monkeypatch.setenv("MUON_DEBUG_CHAIN_SKEW", "1000")
     W, G, M = random_case(512, 1024, 5, device=DEV)
     opt = Muon([(W, G, M)])
+    opt.set_chain_test(skew_rounds=1000)
     opt.ensure_workspace(_lib.MUON_FULL, 1)
     assert opt.plan_info()["chained_groups"] == 1
     opt.step()
@@ -45,7 +47,6 @@ def test_chained_launch_wait_runs_out_and_context_survives(monkeypatch):
         opt.sync()
     assert ei.value.code == _lib.MUON_ERR_TIMEOUT
     opt.close()
-    monkeypatch.delenv("MUON_DEBUG_CHAIN_SKEW")
     trip = list(random_case(512, 1024, 6, device=DEV))
     inp, wexp, oexp, opt2 = gpu_step([trip])
     assert opt2.plan_info()["chained_groups"] == 1

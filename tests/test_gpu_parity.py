@@ -2,6 +2,9 @@
 
 Sizes here are ones the oracle finishes in seconds while spanning several
 128 x 256 tensor-core tiles, 64 x 64 element-wise tiles and ragged tails.
+The single fp32 256 x 512 matrix and the chained default-size cases are
+gated at relF(W) <= 1e-3; the small shapes made to reach ragged tiles use
+the size-scaled weight gate (w_gate="scaled", see gpu_helpers).
 """
 import numpy as np
 import pytest
@@ -41,7 +44,7 @@ def test_ragged_shapes_bf16(rows, cols):
     trip = case(rows, cols, 1)
     inp, wexp, oexp, _ = gpu_step([trip])
     ref = oracle_step(inp[0])
-    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref)
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref, w_gate="scaled")
 
 
 @pytest.mark.parametrize("nesterov", [False, True])
@@ -49,7 +52,7 @@ def test_f32_grad_bf16_weight_nesterov_flag(nesterov):
     trip = case(192, 320, 2, g_dtype=torch.float32)
     inp, wexp, oexp, _ = gpu_step([trip], nesterov=nesterov)
     ref = oracle_step(inp[0], nesterov=nesterov)
-    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref)
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref, w_gate="scaled")
 
 
 def test_grouped_matches_oracle_and_standalone_bitexact():
@@ -59,7 +62,7 @@ def test_grouped_matches_oracle_and_standalone_bitexact():
     inp, wexp, oexp, _ = gpu_step(trips)
     for i, tr in enumerate(trips):
         ref = oracle_step(inp[i])
-        check_against_oracle(tr, inp[i], wexp[i], oexp[i], ref)
+        check_against_oracle(tr, inp[i], wexp[i], oexp[i], ref, w_gate="scaled")
     # each matrix stepped alone gives the same bits
     for i, tr in enumerate(clones):
         _, w1, o1, _ = gpu_step([tr])
@@ -86,7 +89,7 @@ def test_blockwise_matches_oracle(rows, cols, nb):
     inp, wexp, oexp, _ = gpu_step([trip], mode="blockwise", nb=nb)
     ref = oracle_step(inp[0], mode="blockwise", nb=nb)
     check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref,
-                         mode="blockwise", nb=nb)
+                         mode="blockwise", nb=nb, w_gate="scaled")
 
 
 def test_blockwise_nb1_is_full_bitexact():
@@ -137,7 +140,7 @@ def test_ns_steps_and_coefficients_are_honoured():
     coeffs = (2.0, -1.5, 0.5)
     inp, wexp, oexp, _ = gpu_step([trip], ns_steps=3, coeffs=coeffs)
     ref = oracle_step(inp[0], ns_steps=3, coeffs=coeffs)
-    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref)
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref, w_gate="scaled")
 
 
 def test_output_singular_values_in_band():
@@ -164,7 +167,7 @@ def test_alternative_pipelines_match_oracle(fuse_env, monkeypatch):
     inp, wexp, oexp, _ = gpu_step(trips)
     for i, tr in enumerate(trips):
         ref = oracle_step(inp[i])
-        check_against_oracle(tr, inp[i], wexp[i], oexp[i], ref)
+        check_against_oracle(tr, inp[i], wexp[i], oexp[i], ref, w_gate="scaled")
 
 
 def test_update_folded_into_gemm_matches_separate_pass_bitexact(monkeypatch):
@@ -190,7 +193,7 @@ def test_distributed_mode_matches_oracle(rows, cols, P):
     trip = case(rows, cols, 600 + P)
     inp, wexp, oexp, _ = gpu_step([trip], mode="distributed", nb=P)
     ref = oracle_step(inp[0], mode="distributed", nb=P)
-    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref)
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref, w_gate="scaled")
 
 
 def test_distributed_one_slice_is_full_mode_bitexact():
@@ -295,7 +298,7 @@ def test_chained_launch_small_matrix_matches_oracle(rows, cols, ns_steps, monkey
     inp, wexp, oexp, opt = gpu_step([trip], ns_steps=ns_steps)
     assert opt.plan_info()["chained_groups"] == 1
     ref = oracle_step(inp[0], ns_steps=ns_steps)
-    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref)
+    check_against_oracle(trip, inp[0], wexp[0], oexp[0], ref, w_gate="scaled")
     monkeypatch.setenv("MUON_FUSE_STAGES", "0")
     _, _, o2, _ = gpu_step([clone], ns_steps=ns_steps)
     assert torch.equal(oexp[0], o2[0])
@@ -427,8 +430,7 @@ def test_chain_counters_zeroed_and_restarted_bitexact(monkeypatch):
     trips = [case(r, c, 950 + i) for i, (r, c) in enumerate(shapes)]
     clones = [[t.clone() for t in tr] for tr in trips]
     _, _, o1, _ = gpu_step(trips, steps=3)
-    monkeypatch.setenv("MUON_FUSE_COUNTER_LIMIT", "1")
-    _, _, o2, _ = gpu_step(clones, steps=3)
+    _, _, o2, _ = gpu_step(clones, steps=3, chain_test=(0, 1))
     for i in range(len(shapes)):
         assert torch.equal(o1[i], o2[i]), shapes[i]
         assert torch.equal(trips[i][0], clones[i][0]), shapes[i]

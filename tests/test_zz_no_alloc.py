@@ -53,9 +53,9 @@ def test_noalloc_matches_workspace_step_two_calls(rows, cols):
         torch.cuda.synchronize()
         assert relF(W, W2) <= 1e-3, (call, relF(W, W2))
         assert relF(M, M2) <= 1e-6, (call, relF(M, M2))
-        # same kernels, same tile order: expected to agree bit for bit
-        print(rows, cols, call, "bit-exact:", torch.equal(W, W2) and
-              torch.equal(M, M2))
+        # same planner, kernels and tile order as muon_step: the same bits
+        assert torch.equal(W, W2), (rows, cols, call)
+        assert torch.equal(M, M2), (rows, cols, call)
         # the next call gets a fresh gradient on both sides
         G.copy_(G.flip(0))
         G2.copy_(G)
