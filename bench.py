@@ -116,8 +116,8 @@ def traffic_for(kernel: str, workload: str):
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    ent = json.load(open(p)).get(kernel)
-    if not ent or ent.get("workload") != workload:
+    ent = json.load(open(p)).get(f"{kernel}@{workload}")
+    if not ent:
         return None
     if ent.get("source_sha") != source_sha(ent.get("source_files", [])):
         return None

@@ -13,6 +13,7 @@
 // formulas): M <- beta*M + G; U = G + beta*M (Nesterov) else U = M;
 // X0 = U / (||U||_F + eps); W <- W - lr*scale*O.
 #include "muon_internal.h"
+#include "tc_ptx.cuh"
 #include "../../include/muon.h"
 
 namespace muon {
@@ -274,6 +275,172 @@ ew_momentum_kernel(const EwLaunch p) {
     }
 }
 
+// The same pass with M and G streamed into shared memory by TMA: one
+// thread loads tile j + S - 1 of the CTA's walk while all threads process
+// tile j from an S-stage ring, so each CTA keeps S - 1 tiles of loads in
+// flight with few registers (two CTAs per SM).  The thread-to-element map,
+// the arithmetic, the masked stores and the order of the sum of squares are
+// those of ew_momentum_kernel, so both passes give identical bits.  Tiles
+// past the matrix edge read zeros (TMA fill), which add nothing to the sum.
+// GB: bytes of the largest gradient element (stage size); NS stages; CPS:
+// CTAs per SM the launch is sized for.  The transposed units' transpose
+// goes through the stage's momentum block once its values are in registers,
+// with column c of row r at (c + r) mod 64 (two-way bank conflicts at most).
+template <int GB, int NS>
+struct EwtCfg {
+    static constexpr int M_BYTES = EW_TILE * EW_TILE * 4;
+    static constexpr int G_BYTES = EW_TILE * EW_TILE * GB;
+    static constexpr int STAGE = M_BYTES + G_BYTES;
+    static constexpr int S = NS;
+    static constexpr int SMEM = S * STAGE + 2 * (EW_THREADS / 32) * 4 + S * 8 + 128;
+};
+
+template <int GB, int NS, int CPS>
+__global__ void __launch_bounds__(EW_THREADS, CPS)
+ew_momentum_tma_kernel(const EwLaunch p) {
+    using C = EwtCfg<GB, NS>;
+    extern __shared__ uint8_t ewt_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(ewt_raw) + 127) & ~uintptr_t(127));
+    float* red = reinterpret_cast<float*>(smem + C::S * C::STAGE);
+    uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * (EW_THREADS / 32));
+    __shared__ int abort_flag;
+    const int i = threadIdx.x >> 4;          // 0..15
+    const int j4 = (threadIdx.x & 15) * 4;   // 0..60
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < C::S; ++k) ptx::mbar_init(ptx::smem_u32(&full[k]), 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    grid_dependency_wait();
+    allow_dependent_launch();
+    const int64_t nj = p.num_tiles > blockIdx.x
+                           ? (p.num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    // thread 0: loads of the CTA's j-th tile into stage j % S
+    int pu = 0;                              // producer's unit cursor
+    auto issue = [&](int64_t j) {
+        const int64_t t = blockIdx.x + j * gridDim.x;
+        while (t >= __ldg(p.tile_base + pu + 1)) ++pu;
+        const EwUnit& U = p.units[pu];
+        const int64_t local = t - U.tile_base;
+        const int tr = static_cast<int>(local / U.tiles_n);
+        const int tc = static_cast<int>(local - static_cast<int64_t>(tr) * U.tiles_n);
+        const int wr0 = U.transposed ? tc * EW_TILE : tr * EW_TILE;
+        const int wc0 = U.transposed ? tr * EW_TILE : tc * EW_TILE;
+        const int st = static_cast<int>(j % C::S);
+        uint8_t* dst = smem + st * C::STAGE;
+        const uint32_t bar = ptx::smem_u32(&full[st]);
+        ptx::fence_proxy_async_smem();       // earlier reads of the stage first
+        ptx::mbar_expect_tx(bar, C::M_BYTES + EW_TILE * EW_TILE *
+                                     (U.g_dtype == MUON_F32 ? 4 : 2));
+        ptx::tma_load_2d(ptx::smem_u32(dst), &p.maps[pu].m, bar, wc0, wr0);
+        ptx::tma_load_2d(ptx::smem_u32(dst + C::M_BYTES), &p.maps[pu].g, bar, wc0, wr0);
+    };
+    if (threadIdx.x == 0)
+        for (int64_t j = 0; j < C::S - 1 && j < nj; ++j) issue(j);
+    int u = nj ? find_unit(p.tile_base, p.num_units, blockIdx.x) : 0;
+    EwU U = load_ewu(p.units + u);
+    int parity = 0;
+    int64_t j = 0;
+    for (; j < nj; ++j, parity ^= 1) {
+        const int64_t t = blockIdx.x + j * gridDim.x;
+        if (threadIdx.x == 0 && j + C::S - 1 < nj) issue(j + C::S - 1);
+        while (t >= U.tile_end) U = load_ewu(p.units + (++u));
+        const TileGeom g = geom_of(U, t);
+        const int st = static_cast<int>(j % C::S);
+        const uint32_t ph = static_cast<uint32_t>((j / C::S) & 1);
+        if (!ptx::wait_bounded(ptx::smem_u32(&full[st]), ph, &abort_flag, p.err,
+                               p.wait_limit_ns))
+            break;
+        const float* sm = reinterpret_cast<const float*>(smem + st * C::STAGE);
+        const uint8_t* sg = smem + st * C::STAGE + C::M_BYTES;
+        const bool interior =
+            U.vec && g.wr0 + EW_TILE <= U.rows && g.wc0 + EW_TILE <= U.cols;  // block-uniform
+        float uv[4][4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = i + 16 * k;
+            const float4 mq = *reinterpret_cast<const float4*>(sm + r * EW_TILE + j4);
+            float gv[4];
+            if (U.g_dtype == MUON_BF16) {
+                const uint2 q = *reinterpret_cast<const uint2*>(
+                    reinterpret_cast<const __nv_bfloat16*>(sg) + r * EW_TILE + j4);
+                const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.x));
+                const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.y));
+                gv[0] = lo.x; gv[1] = lo.y; gv[2] = hi.x; gv[3] = hi.y;
+            } else {
+                const float4 q = *reinterpret_cast<const float4*>(
+                    reinterpret_cast<const float*>(sg) + r * EW_TILE + j4);
+                gv[0] = q.x; gv[1] = q.y; gv[2] = q.z; gv[3] = q.w;
+            }
+            float mv[4] = {mq.x, mq.y, mq.z, mq.w};
+            const int wr = g.wr0 + r, wc = g.wc0 + j4;
+            const int nval = interior ? 4 : max((wr < U.rows) ? min(4, U.cols - wc) : 0, 0);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                mv[e] = fmaf(p.beta, mv[e], gv[e]);
+                uv[k][e] = e < nval ? (p.nesterov ? fmaf(p.beta, mv[e], gv[e]) : mv[e]) : 0.f;
+            }
+            if (interior)
+                __stcs(reinterpret_cast<float4*>(U.mom + static_cast<int64_t>(wr) * U.ld_m + wc),
+                       make_float4(mv[0], mv[1], mv[2], mv[3]));
+            else
+                st4(U.mom, MUON_F32, static_cast<int64_t>(wr) * U.ld_m + wc, nval, U.vec, mv);
+        }
+        if (U.transposed) {            // block-uniform
+            float* sT = const_cast<float*>(sm);
+            __syncthreads();           // every thread's M values are in registers
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = i + 16 * k, c = j4 + e;
+                    sT[r * EW_TILE + ((c + r) & (EW_TILE - 1))] = uv[k][e];
+                }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = j4 + e, c = i + 16 * k;
+                    uv[k][e] = sT[r * EW_TILE + ((c + r) & (EW_TILE - 1))];
+                }
+        }
+        // uv now holds X(i + 16k, j4 + e) of this tile
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc = fmaf(uv[k][e], uv[k][e], acc);
+            if (p.write_x) {
+                const int gr = g.xr0 + i + 16 * k, gc = g.xc0 + j4;
+                int nx = (gr < U.m) ? min(4, U.n - gc) : 0;
+                nx = max(nx, 0);
+                st4(U.x[0], MUON_BF16, static_cast<int64_t>(gr) * U.ld_x + gc, nx, true,
+                    uv[k]);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) red[parity * (EW_THREADS / 32) + warp] = acc;
+        __syncthreads();               // also: every read of this stage is done
+        if (threadIdx.x == 0) {
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < EW_THREADS / 32; ++w) sum += red[parity * (EW_THREADS / 32) + w];
+            p.partial[t] = sum;
+        }
+    }
+    if (j < nj && threadIdx.x == 0) {
+        // a wait ran out: let the loads still in flight land before leaving
+        for (int64_t q = j; q < nj && q < j + C::S - 1; ++q)
+            ptx::wait_quiet(ptx::smem_u32(&full[q % C::S]),
+                            static_cast<uint32_t>((q / C::S) & 1), p.wait_limit_ns);
+    }
+}
+
 // Per unit: ||U||_F from its tile sums in a fixed order (fp64), then
 // inv_norm = 1 / (||U|| + eps).  One block per unit: thread k sums tiles
 // k, k + 256, ... in order, then a fixed tree combines the 256 sums.
@@ -410,6 +577,29 @@ bool programmatic_launch() { return g_programmatic; }
 
 cudaError_t launch_ew_momentum(const EwLaunch& p, int grid, cudaStream_t s) {
     return launch_kernel(ew_momentum_kernel, dim3(grid), dim3(EW_THREADS), 0, s, p);
+}
+
+template <int GB, int NS, int CPS>
+cudaError_t launch_ewt(const EwLaunch& p, int grid, cudaStream_t s) {
+    static int attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    auto kern = ew_momentum_tma_kernel<GB, NS, CPS>;
+    const int smem = EwtCfg<GB, NS>::SMEM;
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = 1;
+    }
+    return launch_kernel(kern, dim3(grid), dim3(EW_THREADS), smem, s, p);
+}
+
+// Three CTAs per SM, three stages (two for fp32 gradients).  Measured on
+// GB300 against two CTAs with four stages: the same or slightly faster.
+cudaError_t launch_ew_momentum_tma(const EwLaunch& p, int grid, bool g_f32, cudaStream_t s) {
+    return g_f32 ? launch_ewt<4, 2, EWT_CTAS_PER_SM>(p, grid, s)
+                 : launch_ewt<2, 3, EWT_CTAS_PER_SM>(p, grid, s);
 }
 
 cudaError_t launch_ew_norm(const EwLaunch& p, cudaStream_t s) {

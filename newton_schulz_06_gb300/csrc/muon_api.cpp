@@ -59,6 +59,9 @@ struct GroupDesc {
     int u0 = 0, u1 = 0;                      // unit range [u0, u1)
     size_t ew_off = 0, ns_off = 0;           // metadata offsets in ws
     size_t tb_off = 0;                       // int64 tile_base[units + 1]
+    size_t em_off = 0;                       // EwMaps[units] (TMA-fed momentum)
+    bool ew_tma = false;                     // every unit's M and G suit TMA
+    bool g_f32 = false;                      // some unit's gradient is fp32
     bool w_tma = true;                       // every unit's W fits te_w
     size_t t_sx_off = 0, t_sa_off = 0, t_g_off = 0;
     int n_sx = 0, n_sa = 0, n_g = 0;
@@ -133,6 +136,10 @@ struct muon_ctx {
     // chained launch's second products wait for, so their waits run out
     int debug_chain_skew = 0;
     int max_pairs = 0;
+    // momentum pass fed by TMA: 1 = where the group's maps allow it and its
+    // units are small (EWT_MAX_TILES_PER_UNIT), 2 = wherever the maps allow
+    // it, 0 = never
+    int ew_tma = 1;
 };
 
 namespace {
@@ -267,13 +274,16 @@ size_t meta_bound(const std::vector<UnitDesc>& units) {
         g = std::max(g, g2);
         // tile lists (room for twice the tiles, as if every tile were split in
         // halves) and pair offsets
-        b += sizeof(EwUnit) + sizeof(NsUnit) + 8 * 256 + u.cnt_bytes +
+        b += sizeof(EwUnit) + sizeof(NsUnit) + sizeof(EwMaps) + 8 * 256 + u.cnt_bytes +
              2 * size_t(2 * s + g) * sizeof(TileItem) + 3 * 4 * 1024;
     }
     return align_up(b, 1024);
 }
 
 constexpr size_t GROUP_SLACK = 4096;
+// groups whose units average fewer 64 x 64 tiles than this use the TMA-fed
+// momentum pass
+constexpr int64_t EWT_MAX_TILES_PER_UNIT = 1024;
 
 void sizes_for(const std::vector<UnitDesc>& units, size_t* min_b, size_t* full_b) {
     const size_t fixed = align_up(HEADER_BYTES + meta_bound(units), 1024) + GROUP_SLACK;
@@ -328,6 +338,26 @@ int encode_map(muon_ctx* h, CUtensorMap* tm, void* base, int64_t inner,
         return fail(h, MUON_ERR_CUDA,
                     "cuTensorMapEncodeTiled failed with code " + std::to_string(int(r)));
     return MUON_OK;
+}
+
+// A {64, 64}-box, unswizzled map of a rows x cols matrix in the weight's
+// orientation (fp32 momentum or a gradient) for the TMA-fed momentum pass;
+// false if its base or row pitch does not suit TMA (16-byte multiples).
+bool encode_ew_map(muon_ctx* h, CUtensorMap* tm, const void* base, int dtype, int64_t rows,
+                   int64_t cols, int64_t ld) {
+    const size_t es = elem_size(dtype);
+    if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || (size_t(ld) * es) % 16 != 0)
+        return false;
+    cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(ld) * es};
+    cuuint32_t boxd[2] = {EW_TILE, EW_TILE};
+    cuuint32_t el[2] = {1, 1};
+    const CUresult r = h->encode(
+        tm, dtype == MUON_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+        2, const_cast<void*>(base), dims, strides, boxd, el, CU_TENSOR_MAP_INTERLEAVE_NONE,
+        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 void sort_tiles(std::vector<TileItem>* v) {
@@ -595,6 +625,17 @@ int build_plan(muon_ctx* h, int mode, int nb) {
         g.ew_off = off;
         off += sizeof(EwUnit) * nu;
         off = align_up(off, 256);
+        g.em_off = off;
+        off += sizeof(EwMaps) * nu;
+        // the TMA-fed momentum pass hides the per-tile unit lookups that the
+        // plain pass stalls on when units are small (measured on GB300: the
+        // Qwen3-30B-A3B block, 392 tiles per unit, 1.35 -> 1.23 ms); units
+        // of thousands of tiles stream as fast or faster with plain loads
+        // (the Kimi-K2 layer, 3600 per unit: 4.30 against 4.64 ms)
+        g.ew_tma = h->ew_tma == 2 ||
+                   (h->ew_tma == 1 && tiles < EWT_MAX_TILES_PER_UNIT * int64_t(nu));
+        g.g_f32 = false;
+        off = align_up(off, 256);
         g.ns_off = off;
         off += sizeof(NsUnit) * nu;
         g.shards = P.units[g.u0].shards;
@@ -657,6 +698,15 @@ int build_plan(muon_ctx* h, int mode, int nb) {
             e.shape_scale = u.scale;
             tile_base += u.ew_tiles;
             std::memcpy(meta.data() + g.ew_off + sizeof(EwUnit) * (i - g.u0), &e, sizeof(e));
+            if (g.ew_tma) {
+                EwMaps em;
+                std::memset(&em, 0, sizeof(em));
+                g.ew_tma = encode_ew_map(h, &em.m, e.mom, MUON_F32, u.rows, u.cols, pr.ld_m) &&
+                           encode_ew_map(h, &em.g, e.g, pr.g_dtype, u.rows, u.cols, pr.ld_g);
+                g.g_f32 = g.g_f32 || pr.g_dtype == MUON_F32;
+                std::memcpy(meta.data() + g.em_off + sizeof(EwMaps) * (i - g.u0), &em,
+                            sizeof(em));
+            }
 
             NsUnit ns;
             std::memset(&ns, 0, sizeof(ns));
@@ -847,6 +897,10 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
         const int v = std::atoi(cm);
         if (v >= 0) h->chain_max_tiles = v;
     }
+    if (const char* et = std::getenv("MUON_EW_TMA")) {
+        const int v = std::atoi(et);
+        if (v >= 0 && v <= 2) h->ew_tma = v;
+    }
     if (const char* st = std::getenv("MUON_STAGES")) {
         const int v = std::atoi(st);
         if (v >= 4 && v <= 5) h->stages = v;
@@ -982,6 +1036,9 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         ew.lr = lr;
         ew.src = 0;
         ew.eps = NORM_EPS;
+        ew.maps = g.ew_tma ? reinterpret_cast<const EwMaps*>(ws + g.em_off) : nullptr;
+        ew.err = err_word;
+        ew.wait_limit_ns = h->wait_limit_ns;
         // grid-stride over the tiles with the same number of tiles per block
         // (no part-empty last round)
         const int64_t ew_per_block =
@@ -998,7 +1055,14 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         ew.write_x = fused ? 1 : 0;
         cudaError_t e;
         if (!begin(ST_MOMENTUM)) return fail(h, MUON_ERR_CUDA, "event create");
-        e = launch_ew_momentum(ew, ew_grid, h->stream);
+        if (ew.maps)   // persistent CTAs, TMA-fed ring
+            e = launch_ew_momentum_tma(
+                ew,
+                static_cast<int>(std::min<int64_t>(g.ew_tiles,
+                                                   int64_t(EWT_CTAS_PER_SM) * h->num_sms)),
+                g.g_f32, h->stream);
+        else
+            e = launch_ew_momentum(ew, ew_grid, h->stream);
         end();
         if (e != cudaSuccess) return cuda_fail(h, e, "momentum launch");
         if (!begin(ST_NORM)) return fail(h, MUON_ERR_CUDA, "event create");

@@ -157,8 +157,20 @@ struct NsLaunch {
     int32_t shards;
 };
 
+// Tensor maps of one unit's momentum (fp32) and gradient, in the weight's
+// orientation with {64, 64} boxes and no swizzle, for the TMA-fed momentum
+// pass (groups whose every unit allows them).
+struct alignas(128) EwMaps {
+    CUtensorMap m;
+    CUtensorMap g;
+};
+
 struct EwLaunch {
     const EwUnit* units;
+    // per-unit momentum and gradient maps (nullptr: the plain-load pass)
+    const EwMaps* maps;
+    int* err;                // device error word (bounded waits)
+    unsigned long long wait_limit_ns;
     const int64_t* tile_base;   // units' first tiles, num_units + 1 entries
     int32_t write_x;         // momentum pass also stores bf16(U) into x[0]
     int32_t num_units;
@@ -225,6 +237,11 @@ __device__ __forceinline__ void allow_dependent_launch() {
 
 // Launch wrappers (defined in the .cu files).  Return cudaGetLastError().
 cudaError_t launch_ew_momentum(const EwLaunch& p, int grid, cudaStream_t s);
+// The TMA-fed momentum pass (p.maps set): persistent grid of `grid` CTAs,
+// EWT_CTAS_PER_SM per SM; g_f32: some unit's gradient is fp32 (larger ring
+// stages).
+constexpr int EWT_CTAS_PER_SM = 3;
+cudaError_t launch_ew_momentum_tma(const EwLaunch& p, int grid, bool g_f32, cudaStream_t s);
 cudaError_t launch_ew_norm(const EwLaunch& p, cudaStream_t s);
 cudaError_t launch_ew_normalise(const EwLaunch& p, int grid, cudaStream_t s);
 cudaError_t launch_ew_update(const EwLaunch& p, int grid, cudaStream_t s);

@@ -77,7 +77,7 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Bounded wait for the phase of parity `parity` to complete.  Returns false
 // if the CTA aborted, or if this wait ran out (it then records
 // DEV_ERR_TIMEOUT and raises the CTA's abort flag).
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                           volatile int* abort_flag, int* err,
                                           uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -99,7 +99,7 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
 // reaches `target`, with acquire semantics (the caller's later accesses see
 // what the raisers wrote before their release).  Same failure behaviour as
 // wait_bounded.
-__device__ __noinline__ bool wait_count(const int32_t* cnt, int32_t target,
+static __device__ __noinline__ bool wait_count(const int32_t* cnt, int32_t target,
                                         volatile int* abort_flag, int* err,
                                         uint64_t limit_ns) {
     const uint64_t t0 = global_ns();

@@ -92,6 +92,11 @@ def workload(name: str) -> Workload:
         return Workload(name, kimi_k2_layer_shapes(), torch.bfloat16,
                         torch.bfloat16, grad="normal", grad_std=1e-2,
                         mode="blockwise", nb=4)
+    if name == "square_4096_f32":
+        # fp32 weights and gradients at the square size: the update runs as
+        # its own pass (measurement of that pass's HBM rate)
+        return Workload(name, [(4096, 4096)], torch.float32, torch.float32,
+                        grad="log_scale_step", steps=20)
     if name == "square_4096_bf16_distributed4":
         return Workload(name, [(4096, 4096)], torch.bfloat16, torch.bfloat16,
                         grad="log_scale_step", mode="distributed", nb=4)
@@ -105,7 +110,7 @@ def workload(name: str) -> Workload:
 WORKLOADS = ["single_256x512_f32", "square_4096_bf16", "qwen3_30b_a3b_block",
              "qwen3_30b_a3b_48_layers", "kimi_k2_layer_full",
              "kimi_k2_layer_blockwise4", "square_4096_bf16_distributed4",
-             "qwen3_30b_a3b_block_distributed4"]
+             "qwen3_30b_a3b_block_distributed4", "square_4096_f32"]
 
 
 def seed_for(*parts) -> int:

@@ -434,3 +434,24 @@ def test_chain_counters_zeroed_and_restarted_bitexact(monkeypatch):
     for i in range(len(shapes)):
         assert torch.equal(o1[i], o2[i]), shapes[i]
         assert torch.equal(trips[i][0], clones[i][0]), shapes[i]
+
+
+@pytest.mark.parametrize("mode,nb", [("full", 1), ("blockwise", 4)])
+def test_momentum_pass_tma_and_plain_loads_bitexact(mode, nb, monkeypatch):
+    """The momentum pass fed by TMA (groups whose momenta and gradients suit
+    it) and the pass with plain loads give identical bits: the same element
+    map, arithmetic and summation order.  Plain and transposed units, ragged
+    edges, fp32 gradients, two steps (momentum carried)."""
+    shapes = [(256, 1024), (1024, 256), (320, 640), (64, 2048)]
+    a = [case(r, c, 1100 + i, g_dtype=torch.float32 if i == 2 else torch.bfloat16)
+         for i, (r, c) in enumerate(shapes)]
+    if mode == "full":
+        a.append(case(300, 300, 1105))
+    b = [[t.clone() for t in tr] for tr in a]
+    monkeypatch.setenv("MUON_EW_TMA", "2")
+    _, w1, o1, opt = gpu_step(a, steps=2, mode=mode, nb=nb)
+    monkeypatch.setenv("MUON_EW_TMA", "0")
+    _, w2, o2, _ = gpu_step(b, steps=2, mode=mode, nb=nb)
+    for i in range(len(a)):
+        assert torch.equal(o1[i], o2[i]), i
+        assert torch.equal(a[i][0], b[i][0]) and torch.equal(a[i][2], b[i][2]), i
