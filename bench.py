@@ -412,6 +412,12 @@ def run_ours(args, wl, world, rank, local, pg):
                 for W in Ws[:e2e_n]]
     h2d = sum(x.numel() * x.element_size() for x in pinned_g)
     d2h = sum(x.numel() * x.element_size() for x in pinned_w)
+    # two untimed calls first: the first copy into freshly pinned pages is
+    # several times slower than later ones, and the first call builds the
+    # pipelined plan (groups cut so that copies overlap compute)
+    for k in range(2):
+        e2e_opt.step_host(pinned_g, pinned_w, **kw)
+        e2e_opt.sync()
     e2e_ms = []
     for k in range(max(3, min(args.steps, 10))):
         flush.zero_()
@@ -484,7 +490,9 @@ def run_ours(args, wl, world, rank, local, pg):
         "e2e": {"value": world * e2e_useful / (e2e / 1e3) / 1e12,
                 "unit": "TFLOP/s", "ms_per_step": e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "path": "muon_step_host: G from pinned host memory, the step, W back",
+                "path": ("muon_step_host: G from pinned host memory, the step, W back; "
+                         "groups of about 1/8 of the set, copies on two streams overlapping "
+                         "other groups' compute"),
                 "matrices": e2e_n if e2e_n < n_e2e_all else "all"},
         "gpu_launches": launches,
         "roofline": roofline,

@@ -155,7 +155,14 @@ MUON_API int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns
  * the handle's stream and the call returns once it is queued: host buffers
  * must stay valid, and unchanged, until muon_sync returns, and should be
  * pinned (page-locked) for the copies to run asynchronously.  The caller
- * owns them.  Errors as muon_step; a failed copy is MUON_ERR_CUDA. */
+ * owns them.  Errors as muon_step; a failed copy is MUON_ERR_CUDA.
+ * The copies overlap the compute: the step runs in groups of whole matrices
+ * (about 1/8 of the registered elements each, at least 32 M elements), a
+ * group's gradients are copied in on a second stream while earlier groups
+ * compute, and its weights go out on a third stream once its update is
+ * done; the handle's stream waits for all of them.  The first call builds
+ * that grouping (later muon_step calls reuse it; results are the same bits
+ * with any grouping). */
 MUON_API int muon_step_host(muon_handle h, int n, const void* const* g_host,
                             void* const* w_host, float lr, float beta, int nesterov,
                             int ns_steps, float a, float b, float c, int mode, int nb);

@@ -87,6 +87,10 @@ struct GroupDesc {
 struct Plan {
     bool valid = false;
     int mode = -1, nb = 0;
+    // groups also cut (at matrix boundaries) every ~chunk_elems elements, so
+    // that muon_step_host can overlap one group's copies with another's
+    // compute (0: groups only where the workspace requires them)
+    int64_t chunk_elems = 0;
     void* ws = nullptr;
     size_t ws_bytes = 0;
     std::vector<UnitDesc> units;
@@ -136,6 +140,11 @@ struct muon_ctx {
     // chained launch's second products wait for, so their waits run out
     int debug_chain_skew = 0;
     int max_pairs = 0;
+    // muon_step_host: copy streams (gradients in, weights out) and events,
+    // created on first use
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    std::vector<cudaEvent_t> host_events;
+    int host_chunks = 8;       // groups muon_step_host aims for (at matrix boundaries)
     // momentum pass fed by TMA: 1 = where the group's maps allow it and its
     // units are small (EWT_MAX_TILES_PER_UNIT), 2 = wherever the maps allow
     // it, 0 = never
@@ -298,22 +307,28 @@ void sizes_for(const std::vector<UnitDesc>& units, size_t* min_b, size_t* full_b
 
 // Greedy grouping in registration order within the scratch budget.
 bool make_groups(const std::vector<UnitDesc>& units, size_t scratch,
-                 std::vector<GroupDesc>* groups) {
+                 std::vector<GroupDesc>* groups, int64_t chunk_elems = 0) {
     groups->clear();
     size_t acc = 0;
+    int64_t elems = 0;
     GroupDesc g;
     g.u0 = 0;
     for (size_t i = 0; i < units.size(); ++i) {
         const size_t need = units[i].need;
         if (need + GROUP_SLACK > scratch) return false;
-        if (acc + need + GROUP_SLACK > scratch && i > static_cast<size_t>(g.u0)) {
+        const bool full = acc + need + GROUP_SLACK > scratch;
+        // chunk cuts only where a matrix starts (its blocks stay together)
+        const bool chunk = chunk_elems > 0 && elems >= chunk_elems && units[i].block == 0;
+        if ((full || chunk) && i > static_cast<size_t>(g.u0)) {
             g.u1 = static_cast<int>(i);
             groups->push_back(g);
             g = GroupDesc();
             g.u0 = static_cast<int>(i);
             acc = 0;
+            elems = 0;
         }
         acc += need;
+        elems += units[i].rows * units[i].cols;
     }
     g.u1 = static_cast<int>(units.size());
     if (g.u1 > g.u0) groups->push_back(g);
@@ -586,9 +601,10 @@ void append_unit_tiles(const UnitDesc& u, int li, bool pair, std::vector<TileIte
     }
 }
 
-int build_plan(muon_ctx* h, int mode, int nb) {
+int build_plan(muon_ctx* h, int mode, int nb, int64_t chunk_elems = 0) {
     Plan& P = h->plan;
     P = Plan();
+    P.chunk_elems = chunk_elems;
     int rc = build_units(h, mode, nb, &P.units);
     if (rc) return rc;
     if (!h->ws) return fail(h, MUON_ERR_NO_WORKSPACE, "no workspace set (muon_set_workspace)");
@@ -601,7 +617,7 @@ int build_plan(muon_ctx* h, int mode, int nb) {
     const size_t meta_b = meta_bound(P.units);
     P.scratch_off = align_up(HEADER_BYTES + meta_b, 1024);
     const size_t scratch = h->ws_bytes - P.scratch_off;
-    if (!make_groups(P.units, scratch, &P.groups))
+    if (!make_groups(P.units, scratch, &P.groups, chunk_elems))
         return fail(h, MUON_ERR_NO_WORKSPACE, "a unit does not fit the workspace");
 
     // host image of header + metadata
@@ -974,8 +990,37 @@ int muon_set_workspace(muon_handle h, void* dptr, size_t bytes) {
     return MUON_OK;
 }
 
-int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
-              float a, float b, float c, int mode, int nb) {
+}  // extern "C"
+
+namespace {
+
+// muon_step_host's buffers: gradients in and weights out, per parameter.
+struct HostIO {
+    const void* const* g_host;
+    void* const* w_host;
+};
+
+// Elements per group muon_step_host plans for: about 1/host_chunks of the
+// registered set, at least 32 M elements (so that a chunk's copies stay long
+// against the per-group launch overhead); 0 when no cut would result.
+int64_t host_chunk_elems(const muon_ctx* h) {
+    int64_t total = 0;
+    for (const muon_param& p : h->params) total += p.rows * p.cols;
+    const int64_t c = std::max<int64_t>(int64_t(32) << 20, total / std::max(1, h->host_chunks));
+    return (h->params.size() > 1 && c < total) ? c : 0;
+}
+
+cudaEvent_t host_event(muon_ctx* h, size_t idx) {
+    while (h->host_events.size() <= idx) {
+        cudaEvent_t ev;
+        if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+        h->host_events.push_back(ev);
+    }
+    return h->host_events[idx];
+}
+
+int step_impl(muon_ctx* h, float lr, float beta, int nesterov, int ns_steps, float a, float b,
+              float c, int mode, int nb, const HostIO* io) {
     if (!h) return MUON_ERR_INVALID_ARG;
     if (h->device == MUON_HOST_ONLY) return fail(h, MUON_ERR_STATE, "host-only handle");
     if (h->params.empty()) return fail(h, MUON_ERR_STATE, "no parameters registered");
@@ -991,9 +1036,12 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
     DeviceGuard guard(h->device);
     const int want_nb = (mode == MUON_FULL) ? 1 : nb;
     Plan& P = h->plan;
+    // muon_step runs any valid plan; muon_step_host wants one cut into
+    // chunks (the same bits either way: groups do not change results)
+    const int64_t want_chunk = io ? host_chunk_elems(h) : P.chunk_elems;
     if (!P.valid || P.mode != mode || P.nb != want_nb || P.ws != h->ws ||
-        P.ws_bytes != h->ws_bytes) {
-        const int rc = build_plan(h, mode, nb);
+        P.ws_bytes != h->ws_bytes || (io && P.chunk_elems != want_chunk)) {
+        const int rc = build_plan(h, mode, nb, P.valid || io ? want_chunk : 0);
         if (rc) {
             P.valid = false;
             return rc;
@@ -1001,6 +1049,48 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
     }
     char* ws = static_cast<char*>(h->ws);
     int* err_word = reinterpret_cast<int*>(ws);
+    // muon_step_host: parameter i's gradient goes in before the first group
+    // holding one of its units, its weight comes out after the last
+    const int ngroups = static_cast<int>(P.groups.size());
+    std::vector<int> first_g, last_g;
+    cudaEvent_t ev_start = nullptr, ev_end = nullptr;
+    if (io) {
+        if (!h->s_in &&
+            cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking) != cudaSuccess)
+            return fail(h, MUON_ERR_CUDA, "copy stream create");
+        if (!h->s_out &&
+            cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) != cudaSuccess)
+            return fail(h, MUON_ERR_CUDA, "copy stream create");
+        ev_start = host_event(h, 0);
+        ev_end = host_event(h, 1);
+        if (!ev_start || !ev_end || !host_event(h, 1 + 2 * size_t(ngroups)))
+            return fail(h, MUON_ERR_CUDA, "event create");
+        first_g.assign(h->params.size(), -1);
+        last_g.assign(h->params.size(), -1);
+        for (int gi = 0; gi < ngroups; ++gi)
+            for (int i = P.groups[gi].u0; i < P.groups[gi].u1; ++i) {
+                const int prm = P.units[i].param;
+                if (first_g[prm] < 0) first_g[prm] = gi;
+                last_g[prm] = gi;
+            }
+        // gradients in, group by group, after everything queued so far
+        cudaError_t e = cudaEventRecord(ev_start, h->stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->s_in, ev_start, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->s_out, ev_start, 0);
+        for (int gi = 0; gi < ngroups && e == cudaSuccess; ++gi) {
+            for (size_t i = 0; i < h->params.size() && e == cudaSuccess; ++i) {
+                if (first_g[i] != gi) continue;
+                const muon_param& pr = h->params[i];
+                const size_t es = elem_size(pr.g_dtype);
+                e = cudaMemcpy2DAsync(const_cast<void*>(pr.g), size_t(pr.ld_g) * es,
+                                      io->g_host[i], size_t(pr.cols) * es,
+                                      size_t(pr.cols) * es, size_t(pr.rows),
+                                      cudaMemcpyHostToDevice, h->s_in);
+            }
+            if (e == cudaSuccess) e = cudaEventRecord(h->host_events[2 + 2 * gi], h->s_in);
+        }
+        if (e != cudaSuccess) return cuda_fail(h, e, "gradient copy to the device");
+    }
     h->launches.clear();
     size_t ev_idx = 0;
     int count = 0;
@@ -1020,7 +1110,12 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
         if (h->profiling) cudaEventRecord(h->launches.back().stop, h->stream);
     };
     const int ew_grid_cap = h->num_sms * 8;
-    for (GroupDesc& g : P.groups) {
+    for (int gi = 0; gi < ngroups; ++gi) {
+        GroupDesc& g = P.groups[gi];
+        if (io) {
+            const cudaError_t we = cudaStreamWaitEvent(h->stream, h->host_events[2 + 2 * gi], 0);
+            if (we != cudaSuccess) return cuda_fail(h, we, "wait for the gradient copies");
+        }
         const int nu = g.u1 - g.u0;
         const size_t inv_off = P.scratch_off;
         const size_t part_off = align_up(inv_off + size_t(nu) * 4, 256);
@@ -1172,9 +1267,39 @@ int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
             end();
             if (e != cudaSuccess) return cuda_fail(h, e, "update launch");
         }
+        if (io) {
+            // this group's weights out, once its update is done
+            cudaEvent_t done = h->host_events[3 + 2 * gi];
+            e = cudaEventRecord(done, h->stream);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(h->s_out, done, 0);
+            for (size_t i = 0; i < h->params.size() && e == cudaSuccess; ++i) {
+                if (last_g[i] != gi || !io->w_host[i]) continue;
+                const muon_param& pr = h->params[i];
+                const size_t es = elem_size(pr.w_dtype);
+                e = cudaMemcpy2DAsync(io->w_host[i], size_t(pr.cols) * es, pr.w,
+                                      size_t(pr.ld_w) * es, size_t(pr.cols) * es,
+                                      size_t(pr.rows), cudaMemcpyDeviceToHost, h->s_out);
+            }
+            if (e != cudaSuccess) return cuda_fail(h, e, "weight copy to the host");
+        }
+    }
+    if (io) {
+        // the handle's stream (and so muon_sync) covers the copies
+        cudaError_t e = cudaEventRecord(ev_end, h->s_out);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->stream, ev_end, 0);
+        if (e != cudaSuccess) return cuda_fail(h, e, "join of the copy streams");
     }
     h->last_launch_count = count;
     return MUON_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
+              float a, float b, float c, int mode, int nb) {
+    return step_impl(h, lr, beta, nesterov, ns_steps, a, b, c, mode, nb, nullptr);
 }
 
 int muon_step_host(muon_handle h, int n, const void* const* g_host, void* const* w_host,
@@ -1190,28 +1315,8 @@ int muon_step_host(muon_handle h, int n, const void* const* g_host, void* const*
     for (int i = 0; i < n; ++i)
         if (!g_host[i])
             return fail(h, MUON_ERR_INVALID_ARG, "g_host[" + std::to_string(i) + "] is NULL");
-    DeviceGuard guard(h->device);
-    for (int i = 0; i < n; ++i) {
-        const muon_param& p = h->params[i];
-        const size_t es = elem_size(p.g_dtype);
-        const cudaError_t e = cudaMemcpy2DAsync(
-            const_cast<void*>(p.g), size_t(p.ld_g) * es, g_host[i], size_t(p.cols) * es,
-            size_t(p.cols) * es, size_t(p.rows), cudaMemcpyHostToDevice, h->stream);
-        if (e != cudaSuccess) return cuda_fail(h, e, "gradient copy to the device");
-    }
-    const int rc = muon_step(h, lr, beta, nesterov, ns_steps, a, b, c, mode, nb);
-    if (rc) return rc;
-    for (int i = 0; i < n; ++i) {
-        if (!w_host[i]) continue;
-        const muon_param& p = h->params[i];
-        const size_t es = elem_size(p.w_dtype);
-        const cudaError_t e = cudaMemcpy2DAsync(w_host[i], size_t(p.cols) * es, p.w,
-                                                size_t(p.ld_w) * es, size_t(p.cols) * es,
-                                                size_t(p.rows), cudaMemcpyDeviceToHost,
-                                                h->stream);
-        if (e != cudaSuccess) return cuda_fail(h, e, "weight copy to the host");
-    }
-    return MUON_OK;
+    const HostIO io{g_host, w_host};
+    return step_impl(h, lr, beta, nesterov, ns_steps, a, b, c, mode, nb, &io);
 }
 
 int muon_sync(muon_handle h) {
@@ -1241,6 +1346,9 @@ int muon_destroy(muon_handle h) {
     if (h->device != MUON_HOST_ONLY) {
         DeviceGuard guard(h->device);
         for (cudaEvent_t ev : h->event_pool) cudaEventDestroy(ev);
+        for (cudaEvent_t ev : h->host_events) cudaEventDestroy(ev);
+        if (h->s_in) cudaStreamDestroy(h->s_in);
+        if (h->s_out) cudaStreamDestroy(h->s_out);
     }
     delete h;
     return MUON_OK;

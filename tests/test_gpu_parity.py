@@ -455,3 +455,36 @@ def test_momentum_pass_tma_and_plain_loads_bitexact(mode, nb, monkeypatch):
     for i in range(len(a)):
         assert torch.equal(o1[i], o2[i]), i
         assert torch.equal(a[i][0], b[i][0]) and torch.equal(a[i][2], b[i][2]), i
+
+
+def test_pipelined_host_step_matches_device_step_bitexact():
+    """muon_step_host over a set large enough to be cut into several groups
+    (gradients of one group copied in while another computes, weights of a
+    finished group copied out while the next computes): two steps give the
+    same bits as copying G in and W out around muon_step."""
+    shapes = [(2048, 4096)] * 6 + [(4096, 2048)] * 3 + [(768, 2048)] * 4
+    trips = [case(r, c, 1200 + i) for i, (r, c) in enumerate(shapes)]
+    clones = [[t.clone() for t in tr] for tr in trips]
+    opt = Muon(trips)
+    ref = Muon(clones)
+    for step in range(2):
+        g_host = [torch.randn(r, c, generator=torch.Generator().manual_seed(1300 + 17 * step + i)
+                              ).to(torch.bfloat16).pin_memory()
+                  for i, (r, c) in enumerate(shapes)]
+        w_host = [torch.empty(r, c, dtype=torch.bfloat16).pin_memory() for r, c in shapes]
+        opt.step_host(g_host, w_host)
+        opt.sync()
+        for (W, G, M), g in zip(clones, g_host):
+            G.copy_(g)
+        ref.step()
+        ref.sync()
+        torch.cuda.synchronize()
+        # the pipelined plan (three groups here, each of which chains) is not
+        # the single group that muon_step plans for the same set
+        assert opt.last_launch_count() != ref.last_launch_count()
+        for i in range(len(shapes)):
+            assert torch.equal(w_host[i], clones[i][0].cpu()), (step, shapes[i])
+            assert torch.equal(trips[i][0], clones[i][0]), (step, shapes[i])
+            assert torch.equal(trips[i][2], clones[i][2]), (step, shapes[i])
+    opt.close()
+    ref.close()
