@@ -13,9 +13,11 @@ with compute, as future work).
 
 Here ownership is a longest-processing-time partition by the step's FLOPs
 (costliest matrix first, to the least-loaded rank), the same cost model the
-single-GPU planner uses for tiles.  The exchange is one variable-size
-all-gather: each rank packs its owned weights' bytes into one buffer, the
-buffers are padded to the largest and gathered, and every rank unpacks the
+single-GPU planner uses for tiles.  The exchange is a variable-size
+all-gather (the pages' all_gatherv of the updated parameters): each rank
+packs its owned weights' bytes into one buffer of exactly that size, every
+owner broadcasts its buffer to the group (one broadcast per rank that owns
+anything, each of its own size, none padded), and every rank unpacks the
 others' segments.  It can be left pending (``async_gather=True``) so the
 caller overlaps it with other work and waits before the weights are read.
 
@@ -58,14 +60,17 @@ def matrix_costs(shapes, mode: str = "full", nb: int = 1) -> List[int]:
 class _Pending:
     """A weight exchange in flight; wait() completes it and unpacks."""
 
-    def __init__(self, work, finish: Callable[[], None]):
-        self._work = work
+    def __init__(self, works, finish: Callable[[], None]):
+        self._works = list(works)
         self._finish = finish
+        self._done = False
 
     def wait(self) -> None:
-        if self._work is not None:
-            self._work.wait()
-            self._work = None
+        if not self._done:
+            for w in self._works:
+                w.wait()
+            self._works = []
+            self._done = True
             self._finish()
 
 
@@ -109,7 +114,9 @@ class LayerwiseMuon:
         self._per_rank = [[i for i, o in enumerate(self.owner) if o == r]
                           for r in range(self.world)]
         self._rank_bytes = [sum(self._nbytes[i] for i in ids) for ids in self._per_rank]
-        self._pad = max(self._rank_bytes) if self._rank_bytes else 0
+        # bytes one exchange moves into every rank: the sum of the owners'
+        # packed weights (an equal-size all-gather would move world x max)
+        self.exchange_bytes = sum(self._rank_bytes)
 
     def step(self, *, async_gather: bool = False, **kw):
         """The owned matrices' step, then the weight exchange.  Returns None
@@ -127,27 +134,32 @@ class LayerwiseMuon:
 
     def _exchange(self) -> _Pending:
         dev = self.weights[0].device
-        send = torch.empty(self._pad, dtype=torch.uint8, device=dev)
-        off = 0
-        for i in self._per_rank[self.rank]:
-            send[off:off + self._nbytes[i]].copy_(
-                self.weights[i].contiguous().view(-1).view(torch.uint8))
-            off += self._nbytes[i]
-        recv = [torch.empty(self._pad, dtype=torch.uint8, device=dev)
-                for _ in range(self.world)]
-        work = self._dist.all_gather(recv, send, group=self.group, async_op=True)
+        bufs, works = {}, []
+        for r in range(self.world):
+            if self._rank_bytes[r] == 0:
+                continue                       # owns nothing: nothing to send
+            buf = torch.empty(self._rank_bytes[r], dtype=torch.uint8, device=dev)
+            if r == self.rank:
+                off = 0
+                for i in self._per_rank[r]:
+                    buf[off:off + self._nbytes[i]].copy_(
+                        self.weights[i].contiguous().view(-1).view(torch.uint8))
+                    off += self._nbytes[i]
+            src = r if self.group is None else self._dist.get_global_rank(self.group, r)
+            works.append(self._dist.broadcast(buf, src=src, group=self.group, async_op=True))
+            bufs[r] = buf
 
         def finish():
-            for r in range(self.world):
+            for r, buf in bufs.items():
                 if r == self.rank:
                     continue
                 o = 0
                 for i in self._per_rank[r]:
                     w = self.weights[i]
-                    w.view(-1).view(torch.uint8).copy_(recv[r][o:o + self._nbytes[i]])
+                    w.view(-1).view(torch.uint8).copy_(buf[o:o + self._nbytes[i]])
                     o += self._nbytes[i]
 
-        return _Pending(work, finish)
+        return _Pending(works, finish)
 
     def sync(self) -> None:
         if self.engine is not None:

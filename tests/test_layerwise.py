@@ -59,7 +59,9 @@ def _worker(rank, world, port, q, async_gather):
     import torch.distributed as dist
     from newton_schulz_06_gb300.layerwise import LayerwiseMuon
     dist.init_process_group("gloo", rank=rank, world_size=world)
-    shapes = [(64, 32), (16, 48), (40, 40), (8, 8), (96, 16), (24, 72), (33, 5)]
+    # shapes of very different sizes, so the ranks own very different bytes
+    shapes = [(64, 32), (16, 48), (40, 40), (8, 8), (96, 16), (24, 72), (33, 5),
+              (256, 128), (4, 4)]
     g = torch.Generator().manual_seed(11)
     W0 = [torch.randn(s, generator=g).to(torch.bfloat16) for s in shapes]
     G = [torch.randn(s, generator=g).to(torch.bfloat16) for s in shapes]
@@ -70,26 +72,29 @@ def _worker(rank, world, port, q, async_gather):
         h.wait()
     want = [w0 - 0.125 * g0 for w0, g0 in zip(W0, G)]
     ok = all(torch.equal(w, x) for w, x in zip(W, want))
+    # the exchange moves the weights' bytes once, with no padding
+    ok = ok and opt.exchange_bytes == sum(w.numel() * w.element_size() for w in W)
     q.put((rank, opt.owned, sorted(opt.momentum), ok,
            [float(w.float().sum()) for w in W]))
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("async_gather", [False, True])
-def test_two_gloo_ranks_exchange_updated_weights(async_gather):
+@pytest.mark.parametrize("world,async_gather", [(2, False), (2, True), (3, False)])
+def test_gloo_ranks_exchange_updated_weights(world, async_gather):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, q, async_gather))
-             for r in range(2)]
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q, async_gather))
+             for r in range(world)]
     for p in procs:
         p.start()
     out = sorted(q.get(timeout=120) for _ in procs)
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    (r0, own0, m0, ok0, s0), (r1, own1, m1, ok1, s1) = out
-    assert ok0 and ok1                       # every matrix as its owner updated it
-    assert sorted(own0 + own1) == list(range(7)) and not set(own0) & set(own1)
-    assert m0 == own0 and m1 == own1         # momentum only for owned matrices
-    assert s0 == s1                          # both ranks hold the same weights
+    owned = [o[1] for o in out]
+    assert all(o[3] for o in out)            # every matrix as its owner updated it
+    assert sorted(sum(owned, [])) == list(range(9))
+    assert sum(len(o) for o in owned) == len(set(sum(owned, [])))   # disjoint
+    assert all(o[2] == o[1] for o in out)    # momentum only for owned matrices
+    assert all(o[4] == out[0][4] for o in out)   # every rank holds the same weights
