@@ -1,7 +1,10 @@
 // Tensor-core stages of one Newton-Schulz iteration on CTA pairs
-// (tcgen05 cta_group::2): the same three operations as the single-CTA
-// kernels (A = X X^T; B = b A + c A A^T; X' = a X + B X), computed on
-// 256 x 256 output tiles by two CTAs of a cluster sharing one MMA.
+// (tcgen05 cta_group::2): the three products of the single-CTA kernels
+// (A = X X^T; B = b A + c A A^T; X' = a X + B X), computed on 256 x 256
+// output tiles by two CTAs of a cluster sharing one MMA.  Here the second
+// product stores B + a I (a added on the diagonal in its epilogue), so the
+// third is the single product X' = (B + a I) X: the same iteration, with
+// an X update that reads no input block in its epilogue.
 //
 // Why pairs: at full tensor rate a single CTA with 128 x 256 tiles consumes
 // 48 KB of operands per 512 cycles, and four 48 KB stages do not cover the
@@ -65,14 +68,15 @@ template <int OP> __host__ __device__ constexpr int p_threads() {
     return P_THREADS + (OP == OP_CHAIN ? 32 : 0);
 }
 constexpr int P_BLK = 32 * 32 * 2;                 // one 32x32 bf16 block
-// Per epilogue warp: input slots (an X or A block, plus a W block when the
-// update is folded into the last GEMM) and two staging blocks, so a block is
-// staged while the previous one's TMA store still reads its own.  Inputs
-// arrive two blocks ahead; with the W blocks one ahead, which keeps five
-// pipeline stages in shared memory.
+// Per epilogue warp: two input slots (an A block for the second product, a
+// W block when the weight update is folded into the last X update; the X
+// update itself reads no input: a X + B X is computed as (B + a I) X, with
+// a I added to B by the second product) and two staging blocks, so a block
+// is staged while the previous one's TMA store still reads its own.  Inputs
+// arrive two blocks ahead.
 constexpr int P_IN_SLOTS_MAX = 2;
-template <int ST, int FW> __host__ __device__ constexpr int p_in_slots() { return FW ? 1 : 2; }
-template <int FW> __host__ __device__ constexpr int p_in_blk() { return FW ? 2 * P_BLK : P_BLK; }
+template <int ST, int FW> __host__ __device__ constexpr int p_in_slots() { return 2; }
+template <int FW> __host__ __device__ constexpr int p_in_blk() { return P_BLK; }
 template <int ST, int FW> __host__ __device__ constexpr int p_epi_warp_bytes() {
     return p_in_slots<ST, FW>() * p_in_blk<FW>() + 2 * P_BLK;
 }
@@ -203,16 +207,11 @@ __device__ __noinline__ int wait_published(const uint64_t* slot, uint32_t tno, u
 }
 
 // Epilogue input block of a chained tile: the counter of the tile it comes
-// from (X update: the X tile (ti, tj) of iteration s; second product: the A
-// tile (ti, tj)); false if it waits for nothing.
+// from (second product: the A tile (ti, tj)); false if it waits for nothing
+// (the X update reads no X block; a weight-update tile's W blocks are
+// written by nothing in the launch).
 __device__ __forceinline__ bool input_dep(const NsLaunch& p, const NsUnit& U, const TileItem& t,
                                           int op, int s, const int32_t** c, int32_t* target) {
-    if (op == OP_GEMM_BX) {
-        if (s == 1) return false;
-        *c = x_cnt(U, t.ti, t.tj);
-        *target = PAIR_EPI_WARPS * (p.ep_x + s - 1);
-        return true;
-    }
     if (op == OP_SYRK_A) {
         *c = ab_cnt(U, 0, t.ti, t.tj);
         *target = PAIR_EPI_WARPS * (p.ep_a + s);
@@ -235,7 +234,7 @@ __device__ __forceinline__ void release_tile(const NsUnit& U, const TileItem& t,
 // tables, so fields read from the tables would be reloaded after every
 // store).
 struct EpiUnit {
-    const CUtensorMap* te_in;    // epilogue input blocks (GEMM: X, SYRK-2: A)
+    const CUtensorMap* te_in;    // epilogue input blocks of SYRK-2 (A)
     const CUtensorMap* te_out;   // output blocks (A, B or X')
     const CUtensorMap* te_w;     // weight blocks (update folded into the last GEMM)
     int m, n;
@@ -496,13 +495,11 @@ __device__ __forceinline__ uint8_t* next_stage(uint8_t* st0, uint32_t& st_seq, i
 // input blocks come from.  Built for the next tile while the current one is
 // drained, so its first inputs can be requested early.
 struct InPlan {
-    const CUtensorMap* te_in;    // GEMM: X, SYRK-2: A
-    const CUtensorMap* te_w;     // folded update: W
-    int transposed;              // folded update: W is the iterate's transpose
+    const CUtensorMap* te_in;    // the input blocks: A (second product) or W
+    int transposed;              // W blocks: the weight is the iterate's transpose
     int r0w, col0;               // first row, first column of the warp's part
     int n;                       // needed blocks
-    int uses_in;                 // the tile reads input blocks
-    int wb;                      // chained weight-update tile: a W item after each X item
+    int uses_in;                 // the tile reads one input block per needed block
     // chained launches: may its input blocks be loaded (1), not known yet
     // (0: the rows they come from are tested once, then waited for), or
     // tested and not complete (-1: the blocks wait until the tile starts)
@@ -513,19 +510,20 @@ struct InPlan {
     }
 };
 
-template <int OP>
+template <int OP, int FW>
 __device__ __forceinline__ InPlan plan_blocks(const NsLaunch& p, const TileItem& t, int s,
                                               uint32_t rank, int lg, int half) {
     const NsUnit* U = p.units + t.unit;
     const int op = tile_op<OP>(t);
     InPlan q;
-    q.te_in = (op == OP_GEMM_BX) ? &U->te_x[tile_src<OP>(p, s)] : &U->te_a;
-    q.te_w = &U->te_w;
-    q.transposed = (OP != OP_CHAIN && op == OP_GEMM_BX && p.last) ? p.ew[t.unit].transposed : 0;
-    q.uses_in = op != OP_SYRK_X;
-    q.ready = (OP == OP_CHAIN && q.uses_in) ? 0 : 1;
-    q.wb = chain_update_tile<OP>(p, op, s) ? 1 : 0;
-    if (q.wb) q.transposed = p.ew[t.unit].transposed;
+    // the X update reads W blocks where the weight update is folded in
+    // through TMA (FW; a chained launch's last X updates), nothing otherwise
+    const bool w_in = op == OP_GEMM_BX &&
+                      ((OP != OP_CHAIN && FW && p.last) || chain_update_tile<OP>(p, op, s));
+    q.te_in = w_in ? &U->te_w : &U->te_a;
+    q.transposed = w_in ? p.ew[t.unit].transposed : 0;
+    q.uses_in = op == OP_SYRK_A || w_in;
+    q.ready = (OP == OP_CHAIN && op == OP_SYRK_A) ? 0 : 1;
     q.r0w = t.ti * 256 + static_cast<int>(rank) * P_HALF + lg * 32;
     q.col0 = t.tj * 256 + half * 128;
     const int m = U->m;
@@ -543,29 +541,20 @@ __device__ __forceinline__ InPlan plan_blocks(const NsLaunch& p, const TileItem&
     return q;
 }
 
-// Input items of plan q: one per needed block, two (X, then W) for a
-// chained weight-update tile.
-__device__ __forceinline__ int in_items(const InPlan& q) { return q.n << q.wb; }
+// Input items of plan q: one per needed block.
+__device__ __forceinline__ int in_items(const InPlan& q) { return q.n; }
 
-// Lane 0: TMA load of input item j of plan q into input slot `slot`, on the
-// slot's barrier.  An item is the input block of needed block k (X or A)
-// and, when the update is folded in (FW), the matching W block beside it;
-// with q.wb, items alternate between the X block and the W block.  W blocks
-// sit at (x, y) in the weight's orientation, or (y, x) for a transposed unit.
-template <int FW>
+// Lane 0: TMA load of input item j of plan q (the input block of needed
+// block j: an A block, or a W block) into input slot `slot`, on the slot's
+// barrier.  W blocks sit at (x, y) in the weight's orientation, or (y, x)
+// for a transposed unit.
 __device__ __forceinline__ void issue_inputs(const InPlan& q, int j, uint8_t* slot,
                                              uint32_t bar) {
-    const int k = j >> q.wb;
-    const bool w_item = q.wb && (j & 1);
-    const int x = q.col0 + 32 * q.block(k), y = q.r0w;
+    const int x = q.col0 + 32 * q.block(j), y = q.r0w;
     fence_proxy_async_smem();
-    mbar_expect_tx(bar, p_in_blk<FW>());
-    if (!w_item) tma_load_2d(smem_u32(slot), q.te_in, bar, x, y);
-    if (FW || w_item) {
-        uint8_t* wdst = FW ? slot + P_BLK : slot;
-        if (q.transposed) tma_load_2d(smem_u32(wdst), q.te_w, bar, y, x);
-        else tma_load_2d(smem_u32(wdst), q.te_w, bar, x, y);
-    }
+    mbar_expect_tx(bar, P_BLK);
+    if (q.transposed) tma_load_2d(smem_u32(slot), q.te_in, bar, y, x);
+    else tma_load_2d(smem_u32(slot), q.te_in, bar, x, y);
 }
 
 // The update folded into the last GEMM, one 32 x 32 block: O = bf16(v) (the
@@ -1048,12 +1037,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
         // (warp - 2) / 4 (chunks 4h .. 4h + 3 of the 256 columns).  Blocks of
         // 32 x 32 go out through two alternating swizzled shared-memory
         // stages and TMA stores (which also clip at the matrix edge); the
-        // epilogue's input blocks (X for the GEMM, A for SYRK-2) come in by
-        // TMA two blocks ahead, the first two of a tile while its main loop
-        // still runs.  With the update folded in, the W block of each output
-        // block comes too: beside the X block in one slot (FW), or as the
-        // next item in the ring (a chained launch's last X update), so one
-        // block ahead.
+        // epilogue's input blocks (A for SYRK-2; W where the weight update is
+        // folded into the last X update) come in by TMA two blocks ahead,
+        // the first two of a tile while its main loop still runs.  The X
+        // update reads no input otherwise.
         const int ew = warp - 2;
         const int lg = warp & 3;
         const int half = ew >> 2;
@@ -1076,12 +1063,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
         // input blocks stream through the slots in tile order, across tile
         // boundaries: cur is this tile's plan, nxt the next tile's
         InPlan cur{}, nxt{};
-        if (tc.valid()) cur = plan_blocks<OP>(p, t_next, s_next, rank, lg, half);
+        if (tc.valid()) cur = plan_blocks<OP, FW>(p, t_next, s_next, rank, lg, half);
         int cur_issued = 0, nxt_issued = 0;
         auto issue_from = [&](const InPlan& q, int k) {
             const uint32_t sl = in_seq % NS;
             if (lane == 0)
-                issue_inputs<FW>(q, k, s_in + sl * p_in_blk<FW>(), smem_u32(&in_bar[NS * ew + sl]));
+                issue_inputs(q, k, s_in + sl * p_in_blk<FW>(), smem_u32(&in_bar[NS * ew + sl]));
             ++in_seq;
         };
         // chained launches: the tile a tile's input blocks come from is
@@ -1120,7 +1107,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                     issue_from(cur, cur_issued++);
             nxt.n = 0;
             nxt_issued = 0;
-            if (has_next) nxt = plan_blocks<OP>(p, t_next, s_next, rank, lg, half);
+            if (has_next) nxt = plan_blocks<OP, FW>(p, t_next, s_next, rank, lg, half);
             const int op = tile_op<OP>(t);
             const bool uses_in = cur.uses_in;
             // a chained weight-update tile: W read and written, no X' stored
@@ -1186,31 +1173,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                 if (uses_in) {
                     const uint32_t sl = in_use % NS;
                     const uint8_t* slot = s_in + sl * p_in_blk<FW>();
-                    bool got = wait_bounded(smem_u32(&in_bar[NS * ew + sl]),
-                                            (in_use / NS) & 1u, abort_flag, p.err, limit);
+                    const bool got = wait_bounded(smem_u32(&in_bar[NS * ew + sl]),
+                                                  (in_use / NS) & 1u, abort_flag, p.err, limit);
                     if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                     ++in_use;
-                    const uint8_t* s_w = slot + P_BLK;       // FW: W beside X
-                    if (OP == OP_CHAIN && upd) {
-                        // the W block is the next item
-                        const uint32_t sw = in_use % NS;
-                        s_w = s_in + sw * p_in_blk<FW>();
-                        got = wait_bounded(smem_u32(&in_bar[NS * ew + sw]), (in_use / NS) & 1u,
-                                           abort_flag, p.err, limit);
-                        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-                        ++in_use;
-                    }
-                    float x[32];
-                    ld_row_bf16(slot, lane, x);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        v[e] = (op == OP_SYRK_A) ? fmaf(p.b, x[e], p.c * v[e])
-                                                 : scale * fmaf(p.a, x[e], v[e]);
-                    const bool fold = FW || (OP == OP_CHAIN && upd);
+                    // an X update's input is its W block: the weight update
+                    // is folded in (no X' output)
+                    const bool fold = op == OP_GEMM_BX;
                     if (fold) {
-                        // W <- W - lr*scale*O, O = bf16(v); no X' output
-                        fused_update_block<FW == 2>(u, r0w, gc0, lane, v, s_w,
-                                           next_stage(s_st, st_seq, lane));
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] *= scale;
+                        fused_update_block<FW == 2>(u, r0w, gc0, lane, v, slot,
+                                                    next_stage(s_st, st_seq, lane));
+                    } else {
+                        // second product: b A + c A A, plus a on the
+                        // diagonal, so that the X update's single product
+                        // (B + a I) X is a X + B X
+                        float x[32];
+                        ld_row_bf16(slot, lane, x);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = fmaf(p.b, x[e], p.c * v[e]);
+                        if (gc0 == r0w) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (e == lane) v[e] += p.a;
+                        }
                     }
                     __syncwarp();      // every lane's reads of the slots are done
                     // refill the free slots: this tile's next items, else the
