@@ -130,7 +130,9 @@ struct muon_ctx {
     // GEMM through registers, 2 = folded in through TMA-loaded W blocks
     // (groups whose weights are all bf16 and 16-byte aligned; else pass 0)
     int fuse_update = 2;
-    int stages = 5;            // pair mode: TMA pipeline depth (4 or 5)
+    // pair mode: TMA pipeline depth (4, 5, or 6: six where the kernel's
+    // epilogue has no input slots, five for the second product)
+    int stages = 6;
     bool fuse_stages = true;   // pair mode: iterations chained in one launch where it pays
     int64_t rc_limit = int64_t(1) << 30;   // row-counter target at which they are zeroed
     int chain_max_tiles = 8;   // X-update tiles per CTA pair up to which groups chain
@@ -919,7 +921,7 @@ int muon_create(muon_handle* out, int device, void* cuda_stream) {
     }
     if (const char* st = std::getenv("MUON_STAGES")) {
         const int v = std::atoi(st);
-        if (v >= 4 && v <= 5) h->stages = v;
+        if (v >= 4 && v <= 6) h->stages = v;
     }
     if (pair) {
         h->max_pairs = ns_pair_max_clusters();

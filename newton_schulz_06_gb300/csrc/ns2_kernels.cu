@@ -52,7 +52,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int P_STAGES_MAX = 5;
+constexpr int P_STAGES_MAX = 6;
 constexpr int P_HALF = 128;                        // rows per CTA
 constexpr int P_A_BYTES = P_HALF * BK * 2;         // 16 KB
 constexpr int P_B_BYTES = P_HALF * BK * 2;         // 16 KB
@@ -74,19 +74,24 @@ constexpr int P_BLK = 32 * 32 * 2;                 // one 32x32 bf16 block
 // a I added to B by the second product) and two staging blocks, so a block
 // is staged while the previous one's TMA store still reads its own.  Inputs
 // arrive two blocks ahead.
+// Kernels whose epilogue reads nothing (the first product; the X update
+// without the folded weight update) have no input slots, which leaves room
+// for a sixth pipeline stage.
 constexpr int P_IN_SLOTS_MAX = 2;
-template <int ST, int FW> __host__ __device__ constexpr int p_in_slots() { return 2; }
-template <int FW> __host__ __device__ constexpr int p_in_blk() { return P_BLK; }
-template <int ST, int FW> __host__ __device__ constexpr int p_epi_warp_bytes() {
-    return p_in_slots<ST, FW>() * p_in_blk<FW>() + 2 * P_BLK;
+template <int OP, int FW> __host__ __device__ constexpr int p_in_slots() {
+    return (OP == OP_SYRK_X || (OP == OP_GEMM_BX && FW == 0)) ? 0 : 2;
 }
-template <int ST, int FW> __host__ __device__ constexpr int p_epi_bytes() {
-    return P_EPI_WARPS * p_epi_warp_bytes<ST, FW>();
+template <int FW> __host__ __device__ constexpr int p_in_blk() { return P_BLK; }
+template <int OP, int FW> __host__ __device__ constexpr int p_epi_warp_bytes() {
+    return p_in_slots<OP, FW>() * p_in_blk<FW>() + 2 * P_BLK;
+}
+template <int OP, int FW> __host__ __device__ constexpr int p_epi_bytes() {
+    return P_EPI_WARPS * p_epi_warp_bytes<OP, FW>();
 }
 // Shared memory of a kernel with ST pipeline stages.
 template <int ST> __host__ __device__ constexpr int p_epi_off() { return ST * (P_A_BYTES + P_B_BYTES) + 1024; }
-template <int ST, int FW> __host__ __device__ constexpr int p_smem() {
-    return p_epi_off<ST>() + p_epi_bytes<ST, FW>() + 1024;
+template <int OP, int ST, int FW> __host__ __device__ constexpr int p_smem() {
+    return p_epi_off<ST>() + p_epi_bytes<OP, FW>() + 1024;
 }
 
 __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -718,10 +723,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
     uint64_t* tfull_bar = bars + 2 * P_STAGES;
     uint64_t* tempty_bar = bars + 2 * P_STAGES + 2;
     uint64_t* drain_bar = bars + 2 * P_STAGES + 4;
-    constexpr int NS = p_in_slots<P_STAGES, FW>();
+    constexpr int NS_SLOTS = p_in_slots<OP, FW>();
+    constexpr int NS = NS_SLOTS > 0 ? NS_SLOTS : 1;   // ring arithmetic (unused if 0)
     uint64_t* in_bar = bars + 2 * P_STAGES + 5;    // NS per epilogue warp
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_bar + P_IN_SLOTS_MAX * P_EPI_WARPS);
-    static_assert(p_smem<P_STAGES, FW>() <= 232448, "shared memory per CTA");
+    static_assert(p_smem<OP, P_STAGES, FW>() <= 232448, "shared memory per CTA");
     static_assert((2 * P_STAGES + 5 + P_IN_SLOTS_MAX * P_EPI_WARPS) * 8 + 8 + 24 <= 1024,
                   "barrier area");
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -1044,9 +1050,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
         const int ew = warp - 2;
         const int lg = warp & 3;
         const int half = ew >> 2;
-        uint8_t* epi = smem + P_EPI_OFF + ew * p_epi_warp_bytes<P_STAGES, FW>();
+        uint8_t* epi = smem + P_EPI_OFF + ew * p_epi_warp_bytes<OP, FW>();
         uint8_t* s_in = epi;                                   // NS slots
-        uint8_t* s_st = epi + NS * p_in_blk<FW>();             // two staging blocks
+        uint8_t* s_st = epi + NS_SLOTS * p_in_blk<FW>();       // two staging blocks
         uint32_t in_seq = 0;     // input loads issued by this warp
         uint32_t in_use = 0;     // input loads consumed
         uint32_t st_seq = 0;     // staging blocks used
@@ -1294,7 +1300,7 @@ cudaError_t launch_pair_st(const NsLaunch& p, int pairs, cudaStream_t s) {
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
         cudaError_t e = cudaFuncSetAttribute(ns2_kernel<OP, ST, FW, SL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             p_smem<ST, FW>());
+                                             p_smem<OP, ST, FW>());
         if (e != cudaSuccess) return e;
         attr_done[dev] = 1;
     }
@@ -1302,7 +1308,7 @@ cudaError_t launch_pair_st(const NsLaunch& p, int pairs, cudaStream_t s) {
     // pairs must be resident together: it is launched cooperatively, and a
     // grid that cannot be co-resident is refused instead of left to stall.
     return launch_kernel_attr(ns2_kernel<OP, ST, FW, SL>, dim3(2 * pairs),
-                              dim3(p_threads<OP>()), p_smem<ST, FW>(), s, OP == OP_CHAIN, p);
+                              dim3(p_threads<OP>()), p_smem<OP, ST, FW>(), s, OP == OP_CHAIN, p);
 }
 
 template <int OP>
@@ -1310,7 +1316,11 @@ cudaError_t launch_pair_op(const NsLaunch& p, int pairs, int stages, cudaStream_
     if (OP == OP_SYRK_X && p.shards > 1) return launch_pair_st<OP_SYRK_X, 5, 0, 1>(p, pairs, s);
     switch (stages) {
         case 4: return launch_pair_st<OP, 4, 0>(p, pairs, s);
-        default: return launch_pair_st<OP, 5, 0>(p, pairs, s);
+        case 5: return launch_pair_st<OP, 5, 0>(p, pairs, s);
+        default:
+            // six stages where the epilogue has no input slots
+            if constexpr (OP == OP_SYRK_A) return launch_pair_st<OP, 5, 0>(p, pairs, s);
+            else return launch_pair_st<OP, 6, 0>(p, pairs, s);
     }
 }
 
@@ -1323,14 +1333,14 @@ int ns_pair_max_clusters() {
     if (cached[dev]) return cached[dev];
     cudaError_t e = cudaFuncSetAttribute(ns2_kernel<OP_GEMM_BX, P_STAGES_MAX, 0, 0>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         p_smem<P_STAGES_MAX, 0>());
+                                         p_smem<OP_GEMM_BX, P_STAGES_MAX, 0>());
     if (e != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
     cfg.blockDim = dim3(P_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = p_smem<P_STAGES_MAX, 0>();
+    cfg.dynamicSmemBytes = p_smem<OP_GEMM_BX, P_STAGES_MAX, 0>();
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, ns2_kernel<OP_GEMM_BX, P_STAGES_MAX, 0, 0>, &cfg);
     if (e != cudaSuccess || n <= 0) {
