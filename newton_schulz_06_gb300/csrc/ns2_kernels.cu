@@ -832,7 +832,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                     ok = false;
                     break;
                 }
-                for (int kb = 0; kb < kblocks; ++kb) {
+                // A and B (the symmetric products' outputs) hold only tiles
+                // on or above the diagonal: the k-blocks left of an
+                // operand's row block come from the stored transpose, as an
+                // MN-major operand (two {64, 64} boxes).  They come first
+                // in a loop of their own; the loop over the rest is the
+                // plain one.
+                const void* tmT = (op == OP_SYRK_A) ? &U->tm_a : &U->tm_b;
+                const int kb_at = (op == OP_SYRK_X) ? 0 : 4 * t.ti;
+                const int kb_bt = (op == OP_SYRK_A) ? 4 * t.tj : 0;
+                const int kb_t = kb_at > kb_bt ? kb_at : kb_bt;
+                int kb = 0;
+                for (; kb < kb_t; ++kb) {
+                    if (OP == OP_CHAIN && (kb >> 2) >= ready_c) {
+                        // the watcher warp publishes how many leading chunks
+                        // of this tile may be loaded
+                        const uint64_t v = ld_acquire_cta_u64(&dep_slot[tno & 1]);
+                        if (static_cast<uint32_t>(v >> 32) == tno &&
+                            static_cast<int>(static_cast<uint32_t>(v)) > (kb >> 2))
+                            ready_c = static_cast<int>(static_cast<uint32_t>(v));
+                        else
+                            ready_c = wait_published(&dep_slot[tno & 1], tno, kb >> 2,
+                                                     abort_flag, p.err, limit);
+                        if (ready_c < 0) {
+                            ok = false;
+                            break;
+                        }
+                        fence_proxy_async_global();    // TMA reads after the acquire
+                    }
+                    if (!mbar_try_wait(smem_u32(&empty_bar[stage]), phase ^ 1) &&
+                        !wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1, abort_flag,
+                                      p.err, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb_local = smem_u32(&full_bar[stage]);
+                    if (rank == 0) mbar_expect_tx(fb_local, tx_bytes);
+                    const uint32_t fb = map_to_rank(fb_local, 0);
+                    const uint32_t a_dst = smem_u32(sA + stage * P_A_BYTES);
+                    const uint32_t b_dst = smem_u32(sB + stage * P_B_BYTES);
+                    const int k0 = kb * BK;
+                    if (kb < kb_at) {
+                        tma_load_2d_pair(a_dst, tmT, fb, r0, k0);
+                        tma_load_2d_pair(a_dst + P_BOX, tmT, fb, r0 + 64, k0);
+                    } else {
+                        tma_load_2d_pair(a_dst, tmA, fb, k0, r0);
+                    }
+                    if (op == OP_GEMM_BX) {
+                        tma_load_2d_pair(b_dst, tmB, fb, b0, k0);
+                        if (hb > 64) tma_load_2d_pair(b_dst + P_BOX, tmB, fb, b0 + 64, k0);
+                    } else if (kb < kb_bt) {
+                        tma_load_2d_pair(b_dst, tmT, fb, b0, k0);
+                        tma_load_2d_pair(b_dst + P_BOX, tmT, fb, b0 + 64, k0);
+                    } else {
+                        tma_load_2d_pair(b_dst, tmB, fb, k0, b0);
+                    }
+                    issued[stage] = static_cast<int>(phase) + 1;
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                for (; kb < kblocks; ++kb) {
                     if (OP == OP_CHAIN && (kb >> 2) >= ready_c) {
                         // the watcher warp publishes how many leading chunks
                         // of this tile may be loaded
@@ -897,6 +956,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
             constexpr bool sliced = SL != 0;
             uint32_t u0 = 0, u1 = 0;
             const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024);
+            // an operand read from a symmetric input's stored transpose is
+            // MN-major: two 64-wide halves P_BOX apart, K rows of 128 bytes,
+            // 16 K rows (2048 bytes) per MMA step
+            const uint64_t a_desc_mn = smem_desc(smem_u32(sA), P_BOX, 1024);
             // B operand: MN-major for the GEMM (X), K-major otherwise
             const uint64_t b_desc_mn = smem_desc(smem_u32(sB), P_BOX, 1024);
             const uint64_t b_desc_k = smem_desc(smem_u32(sB), 16, 1024);
@@ -922,7 +985,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                 tc_fence_after();
                 uint32_t d_tmem = tmem_base + acc * 256 + t.n_off;
                 int kin = 0;                              // step within the slice
-                for (int kb = 0; kb < kblocks; ++kb) {
+                // k-blocks read from a symmetric input's stored transpose
+                // (MN-major operands) first, in a loop of their own
+                const int kb_at = (op == OP_SYRK_X) ? 0 : 4 * t.ti;
+                const int kb_bt = (op == OP_SYRK_A) ? 4 * t.tj : 0;
+                const int kb_t = sliced ? 0 : (kb_at > kb_bt ? kb_at : kb_bt);
+                int kb = 0;
+                for (; kb < kb_t; ++kb) {
+                    if (!mbar_try_wait(smem_u32(&full_bar[stage]), phase) &&
+                        !wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag, p.err,
+                                      limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const bool at = kb < kb_at, bt = kb < kb_bt;
+                    const uint64_t ad0 = (at ? a_desc_mn : a_desc0) +
+                                         static_cast<uint64_t>(stage) * (P_A_BYTES >> 4);
+                    const uint64_t bd0 = (bt ? b_desc_mn : b_desc0) +
+                                         static_cast<uint64_t>(stage) * (P_B_BYTES >> 4);
+                    const uint32_t a_step = at ? (2048 >> 4) : (32 >> 4);
+                    const uint32_t b_step = bt ? (2048 >> 4) : b_kstep;
+                    const uint32_t id = idesc | (at ? (1u << 15) : 0u) | (bt ? (1u << 16) : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_pair(d_tmem, ad0 + static_cast<uint64_t>(kk * a_step),
+                                 bd0 + static_cast<uint64_t>(kk * b_step), id,
+                                 (kb > 0 || kk > 0) ? 1u : 0u);
+                    any = true;
+                    commit_pair_multicast(smem_u32(&empty_bar[stage]));
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                for (; kb < kblocks; ++kb) {
                     if (sliced && kin == 0 && kb > 0) {
                         // a new slice into accumulator 1, once the epilogue
                         // has taken the previous one out
@@ -1252,9 +1347,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                     uint8_t* st = next_stage(s_st, st_seq, lane);
                     st_row_bf16(st, lane, v);
                     store_block(u.te_out, st, gc0, r0w, lane);
-                    st = next_stage(s_st, st_seq, lane);
-                    st_col_bf16(st, lane, v);
-                    store_block(u.te_out, st, r0w, gc0, lane);   // mirror
+                    if (t.ti == t.tj) {
+                        // a diagonal tile is stored whole: its lower part
+                        // too (consumers read whole rows of it); other
+                        // tiles are read through their stored transpose
+                        st = next_stage(s_st, st_seq, lane);
+                        st_col_bf16(st, lane, v);
+                        store_block(u.te_out, st, r0w, gc0, lane);   // mirror
+                    }
                 }
             }
             if (!__all_sync(0xffffffffu, ok)) break;
