@@ -141,7 +141,12 @@ MUON_API int muon_set_workspace(muon_handle h, void* dptr, size_t bytes);
  *                        MUON_DISTRIBUTED with nb tensor-parallel slices
  * The first step after registering params, changing the workspace, the mode
  * or nb builds the plan and uploads its tables (host work plus one copy);
- * later steps only queue kernels.  Returns once the work is queued. */
+ * later steps only queue kernels.  Returns once the work is queued.
+ * A step carries no device state from earlier steps beyond W and M, so a
+ * step queued while the handle's stream is being captured into a CUDA graph
+ * replays correctly; the plan must exist before the capture (run one step
+ * outside it first: MUON_ERR_STATE otherwise), and stage profiling must be
+ * off during the capture. */
 MUON_API int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns_steps,
               float a, float b, float c, int mode, int nb);
 
@@ -213,15 +218,13 @@ MUON_API int muon_debug_wait_timeout(muon_handle h, int* err_word, int limit_ms)
 
 /* Validation of the chained launch (see muon_get_plan_info: groups of few
  * large matrices run every product of a step in one launch whose tiles wait
- * on per-tile counters).  skew_rounds > 0 makes the second products of later
- * chained launches wait for that many counter rounds more than will ever be
- * completed, so their bounded waits run out and muon_sync reports
- * MUON_ERR_TIMEOUT (a timeout test without a fault; 0 = off).  counter_limit
- * is the counter target from which a group's tile counters are zeroed before
- * a step (1 .. 2^30; 0 = the default 2^30): a small limit exercises the
- * restart.  Applies to later steps of this handle; MUON_ERR_INVALID_ARG for
- * values out of range. */
-MUON_API int muon_debug_set_chain_test(muon_handle h, int skew_rounds, int64_t counter_limit);
+ * on per-tile counters, zeroed by each step's momentum pass).  skew_rounds
+ * > 0 makes the second products of later chained launches wait for that
+ * many counter rounds more than will ever be completed, so their bounded
+ * waits run out and muon_sync reports MUON_ERR_TIMEOUT (a timeout test
+ * without a fault; 0 = off).  Applies to later steps of this handle;
+ * MUON_ERR_INVALID_ARG for values out of range. */
+MUON_API int muon_debug_set_chain_test(muon_handle h, int skew_rounds);
 
 /* Host-only check of the chained launch's schedule for `mode`/`nb`: for every
  * group of the registered matrices (ignoring the size bounds that decide

@@ -103,7 +103,7 @@ def lib() -> ctypes.CDLL:
                               f32, f32, f32, vp, ctypes.c_char_p, sz],
         "muon_debug_wait_timeout": [H, vp, i32],
         "muon_debug_check_chain_schedule": [H, i32, i32],
-        "muon_debug_set_chain_test": [H, i32, ctypes.c_int64],
+        "muon_debug_set_chain_test": [H, i32],
         "muon_step_host": [H, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), f32,
                            f32, i32, i32, f32, f32, f32, i32, i32],
     }

@@ -74,12 +74,11 @@ struct GroupDesc {
     size_t t_c_off = 0, o_c_off = 0, e_c_off = 0;
     int n_c = 0, p_c = 0;
     bool chain_ok = false;
-    // completed rounds of the X, A and B tile counters since they were last
-    // zeroed; the counters sit in the metadata region (never aliased by a
-    // group's scratch) and only grow
-    int64_t ep_x = 0, ep_a = 0, ep_b = 0;
-    size_t rc_off = 0, rc_bytes = 0;         // this group's counter block
-    int64_t rc_step = 0;                     // a counter's increment per round
+    // this group's tile counters (chained launches): in the metadata region
+    // (never aliased by a group's scratch), zeroed by every step's momentum
+    // pass, so a step's launches carry no state from earlier steps (a step
+    // captured in a CUDA graph replays correctly)
+    size_t rc_off = 0, rc_bytes = 0;
     int64_t ew_tiles = 0;
     int shards = 1;                          // distributed mode: P
 };
@@ -134,7 +133,6 @@ struct muon_ctx {
     // epilogue has no input slots, five for the second product)
     int stages = 6;
     bool fuse_stages = true;   // pair mode: iterations chained in one launch where it pays
-    int64_t rc_limit = int64_t(1) << 30;   // row-counter target at which they are zeroed
     int chain_max_tiles = 8;   // X-update tiles per CTA pair up to which groups chain
     int chain_min_tiles = -1;  // X-update tiles from which groups chain (-1: one per pair)
     bool chain_last = true;    // a chain also runs the last X update (weight update folded in)
@@ -660,7 +658,6 @@ int build_plan(muon_ctx* h, int mode, int nb, int64_t chunk_elems = 0) {
         // tile counters of chained launches, zero in the uploaded image
         off = align_up(off, 256);
         g.rc_off = off;
-        g.rc_step = PAIR_EPI_WARPS;             // every tile counter, per round
         for (int i = g.u0; i < g.u1; ++i) off += P.units[i].cnt_bytes;
         g.rc_bytes = off - g.rc_off;
         size_t rc_next = g.rc_off;
@@ -797,7 +794,6 @@ int build_plan(muon_ctx* h, int mode, int nb, int64_t chunk_elems = 0) {
         put(tsx, &g.t_sx_off, &g.n_sx, &g.o_sx_off, &g.p_sx);
         put(tsa, &g.t_sa_off, &g.n_sa, &g.o_sa_off, &g.p_sa);
         put(tg, &g.t_g_off, &g.n_g, &g.o_g_off, &g.p_g);
-        g.ep_x = g.ep_a = g.ep_b = 0;
         g.chain_ok = chain_eligible(h, g.shards, static_cast<int64_t>(tg0.size()));
         if (g.chain_ok) {
             const int pairs = std::max(
@@ -1041,8 +1037,20 @@ int step_impl(muon_ctx* h, float lr, float beta, int nesterov, int ns_steps, flo
     // muon_step runs any valid plan; muon_step_host wants one cut into
     // chunks (the same bits either way: groups do not change results)
     const int64_t want_chunk = io ? host_chunk_elems(h) : P.chunk_elems;
+    // while the stream is captured into a CUDA graph: no plan build (its
+    // table upload reads host memory that the graph would read again on
+    // every replay) and no stage-timing events
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (h->stream && cudaStreamIsCapturing(h->stream, &cap) != cudaSuccess)
+        return fail(h, MUON_ERR_CUDA, "stream capture query");
+    const bool capturing = cap != cudaStreamCaptureStatusNone;
+    if (capturing && h->profiling)
+        return fail(h, MUON_ERR_STATE, "stage profiling is not allowed while capturing");
     if (!P.valid || P.mode != mode || P.nb != want_nb || P.ws != h->ws ||
         P.ws_bytes != h->ws_bytes || (io && P.chunk_elems != want_chunk)) {
+        if (capturing)
+            return fail(h, MUON_ERR_STATE,
+                        "the plan must be built before stream capture: run one step first");
         const int rc = build_plan(h, mode, nb, P.valid || io ? want_chunk : 0);
         if (rc) {
             P.valid = false;
@@ -1142,13 +1150,8 @@ int step_impl(muon_ctx* h, float lr, float beta, int nesterov, int ns_steps, flo
             std::max<int64_t>(1, ceil_div(g.ew_tiles, int64_t(ew_grid_cap)));
         const int ew_grid = static_cast<int>(ceil_div(g.ew_tiles, ew_per_block));
         const bool fused = h->pair && h->fuse;
-        if (g.chain_ok &&
-            g.rc_step * (std::max({g.ep_x, g.ep_a, g.ep_b}) + ns_steps) > h->rc_limit) {
-            // the targets would near int32 overflow: start the counters over
-            const cudaError_t ce = cudaMemsetAsync(ws + g.rc_off, 0, g.rc_bytes, h->stream);
-            if (ce != cudaSuccess) return cuda_fail(h, ce, "tile counter reset");
-            g.ep_x = g.ep_a = g.ep_b = 0;
-        }
+        ew.cnt_zero = g.chain_ok ? reinterpret_cast<int32_t*>(ws + g.rc_off) : nullptr;
+        ew.cnt_words = g.chain_ok ? static_cast<int64_t>(g.rc_bytes / 4) : 0;
         ew.write_x = fused ? 1 : 0;
         cudaError_t e;
         if (!begin(ST_MOMENTUM)) return fail(h, MUON_ERR_CUDA, "event create");
@@ -1203,9 +1206,9 @@ int step_impl(muon_ctx* h, float lr, float beta, int nesterov, int ns_steps, flo
             L.pair_off = reinterpret_cast<const int32_t*>(ws + g.o_c_off);
             L.pair_end_last = reinterpret_cast<const int32_t*>(ws + g.e_c_off);
             L.iters = ns_steps;
-            L.ep_x = static_cast<int32_t>(g.ep_x);
-            L.ep_a = static_cast<int32_t>(g.ep_a + h->debug_chain_skew);
-            L.ep_b = static_cast<int32_t>(g.ep_b);
+            L.ep_x = 0;
+            L.ep_a = h->debug_chain_skew;
+            L.ep_b = 0;
             L.shards = 1;
             if (!begin(ST_CHAIN)) return fail(h, MUON_ERR_CUDA, "event create");
             e = launch_ns_pair(OP_CHAIN, L, g.p_c, h->stages, h->stream);
@@ -1214,9 +1217,6 @@ int step_impl(muon_ctx* h, float lr, float beta, int nesterov, int ns_steps, flo
                 P.valid = false;              // rebuilt (and re-uploaded) next step
                 return cuda_fail(h, e, "chained launch");
             }
-            g.ep_x += ns_steps - 1;
-            g.ep_a += ns_steps;
-            g.ep_b += ns_steps;
             cur = (ns_steps - 1) & 1;
             if (chain_last) cur ^= 1;
         }
@@ -1406,14 +1406,11 @@ int muon_debug_set_exports(muon_handle h, int n, float* const* w_f32, void* cons
     return MUON_OK;
 }
 
-int muon_debug_set_chain_test(muon_handle h, int skew_rounds, int64_t counter_limit) {
+int muon_debug_set_chain_test(muon_handle h, int skew_rounds) {
     if (!h) return MUON_ERR_INVALID_ARG;
     if (skew_rounds < 0 || skew_rounds > (1 << 20))
         return fail(h, MUON_ERR_INVALID_ARG, "skew_rounds must be in 0..2^20");
-    if (counter_limit < 0 || counter_limit > (int64_t(1) << 30))
-        return fail(h, MUON_ERR_INVALID_ARG, "counter_limit must be in 0..2^30");
     h->debug_chain_skew = skew_rounds;
-    h->rc_limit = counter_limit ? counter_limit : (int64_t(1) << 30);
     return MUON_OK;
 }
 

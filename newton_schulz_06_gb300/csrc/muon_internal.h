@@ -139,10 +139,12 @@ struct NsLaunch {
     const int32_t* pair_off;
     // OP_CHAIN: iterations in the launch; pair_end_last[p]: end of pair p's
     // list without its X-update tiles (the last iteration's walk); ep_x,
-    // ep_a, ep_b: completed rounds of the X, A and B counters before the
-    // launch (an X tile read in iteration s is complete once its counter
-    // reaches PAIR_EPI_WARPS * (ep_x + s - 1), an A tile once
-    // PAIR_EPI_WARPS * (ep_a + s), a B tile once PAIR_EPI_WARPS * (ep_b + s)).
+    // ep_a, ep_b: rounds the X, A and B counters held when the launch began
+    // (0: the step's momentum pass zeroes them; the A rounds carry a test
+    // skew when muon_debug_set_chain_test asks for one).  An X tile read in
+    // iteration s is complete once its counter reaches PAIR_EPI_WARPS *
+    // (ep_x + s - 1), an A tile once PAIR_EPI_WARPS * (ep_a + s), a B tile
+    // once PAIR_EPI_WARPS * (ep_b + s).
     int32_t iters;
     const int32_t* pair_end_last;
     // OP_CHAIN: 1 = the last iteration's X-update tiles run too, with the
@@ -182,6 +184,11 @@ struct EwLaunch {
     float lr;
     int32_t src;             // X buffer holding the final iterate (update)
     float eps;
+    // momentum pass, block 0: zero the group's tile counters (chained
+    // launches) once the previous step's kernels are complete, so that
+    // every step's chained launch counts from zero (nullptr: none)
+    int32_t* cnt_zero;
+    int64_t cnt_words;
 };
 
 // Programmatic dependent launch: kernels are launched so that they may start

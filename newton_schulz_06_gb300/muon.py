@@ -170,11 +170,10 @@ class Muon:
               self._h)
         return {k: getattr(info, k) for k, _ in info._fields_}
 
-    def set_chain_test(self, skew_rounds: int = 0, counter_limit: int = 0):
-        """Validation of the chained launch: waits that run out (skew) and
-        early counter restarts (limit); 0, 0 = normal operation."""
-        check(lib().muon_debug_set_chain_test(self._h, int(skew_rounds),
-                                              int(counter_limit)), self._h)
+    def set_chain_test(self, skew_rounds: int = 0):
+        """Validation of the chained launch: waits that run out (skew rounds
+        that never come); 0 = normal operation."""
+        check(lib().muon_debug_set_chain_test(self._h, int(skew_rounds)), self._h)
 
     def close(self):
         if self._h:

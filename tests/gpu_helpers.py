@@ -52,11 +52,11 @@ def gpu_step(triples, *, lr=0.02, beta=0.95, nesterov=True, ns_steps=5,
              max_workspace=None, steps=1, chain_test=None):
     """Runs `steps` Muon steps on device tensors in place; returns
     (host copies of the inputs, fp32 W exports, bf16 O exports, opt).
-    chain_test: (skew_rounds, counter_limit) for muon_debug_set_chain_test."""
+    chain_test: skew_rounds for muon_debug_set_chain_test."""
     inputs = [(to_np(W), to_np(G), to_np(M)) for W, G, M in triples]
     opt = Muon(triples)
     if chain_test is not None:
-        opt.set_chain_test(*chain_test)
+        opt.set_chain_test(chain_test)
     md = mode_code(mode)
     opt.ensure_workspace(md, nb, max_workspace)
     wexp = oexp = None

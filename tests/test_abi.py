@@ -157,10 +157,10 @@ def test_register_rejects_bad_params(L):
                          1) == L.MUON_ERR_STATE
     # the chained launch's validation switches are an explicit call (no
     # environment variable can turn them on); out-of-range values rejected
-    assert lib.muon_debug_set_chain_test(h, 0, 0) == 0
-    assert lib.muon_debug_set_chain_test(h, 3, 1) == 0
-    assert lib.muon_debug_set_chain_test(h, -1, 0) == L.MUON_ERR_INVALID_ARG
-    assert lib.muon_debug_set_chain_test(h, 0, (1 << 30) + 1) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_debug_set_chain_test(h, 0) == 0
+    assert lib.muon_debug_set_chain_test(h, 3) == 0
+    assert lib.muon_debug_set_chain_test(h, -1) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_debug_set_chain_test(h, (1 << 20) + 1) == L.MUON_ERR_INVALID_ARG
     assert lib.muon_destroy(h) == 0
 
 
