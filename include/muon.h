@@ -218,11 +218,11 @@ MUON_API int muon_debug_wait_timeout(muon_handle h, int* err_word, int limit_ms)
 
 /* Validation of the chained launch (see muon_get_plan_info: groups of few
  * large matrices run every product of a step in one launch whose tiles wait
- * on per-tile counters, zeroed by each step's momentum pass).  skew_rounds
- * > 0 makes the second products of later chained launches wait for that
- * many counter rounds more than will ever be completed, so their bounded
- * waits run out and muon_sync reports MUON_ERR_TIMEOUT (a timeout test
- * without a fault; 0 = off).  Applies to later steps of this handle;
+ * on per-tile counters; the launch's last CTA zeroes them as it leaves).
+ * skew_rounds > 0 makes the second products of later chained launches wait
+ * for that many counter rounds more than will ever be completed, so their
+ * bounded waits run out and muon_sync reports MUON_ERR_TIMEOUT (a timeout
+ * test without a fault; 0 = off).  Applies to later steps of this handle;
  * MUON_ERR_INVALID_ARG for values out of range. */
 MUON_API int muon_debug_set_chain_test(muon_handle h, int skew_rounds);
 

@@ -145,16 +145,6 @@ __device__ __forceinline__ TileGeom geom_of(const EwU& U, int64_t t) {
     return g;
 }
 
-// Block 0 of the momentum pass: zero the group's chained-launch tile
-// counters.  It runs after the grid dependency wait, so the previous step's
-// chained launch (the last reader and writer of the counters) is complete,
-// and the step's own chained launch starts after this pass (and the norm
-// pass) has completed.
-__device__ __forceinline__ void zero_tile_counters(const EwLaunch& p) {
-    if (blockIdx.x != 0 || !p.cnt_zero) return;
-    for (int64_t i = threadIdx.x; i < p.cnt_words; i += blockDim.x) p.cnt_zero[i] = 0;
-}
-
 // Pass 1: M <- beta*M + G; U as above; per tile and warp one fp32 sum of U^2
 // taken in the X orientation (short side first) in a fixed order, so that a
 // matrix and its transpose give the same sums.  With write_x the
@@ -165,7 +155,6 @@ __global__ void __launch_bounds__(EW_THREADS, 4)
 ew_momentum_kernel(const EwLaunch p) {
     grid_dependency_wait();
     allow_dependent_launch();
-    zero_tile_counters(p);
     __shared__ float sU[EW_TILE][EW_TILE + 1];
     __shared__ float red[2][EW_THREADS / 32];
     const int i = threadIdx.x >> 4;          // 0..15
@@ -327,7 +316,6 @@ ew_momentum_tma_kernel(const EwLaunch p) {
     __syncthreads();
     grid_dependency_wait();
     allow_dependent_launch();
-    zero_tile_counters(p);
     const int64_t nj = p.num_tiles > blockIdx.x
                            ? (p.num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     // thread 0: loads of the CTA's j-th tile into stage j % S

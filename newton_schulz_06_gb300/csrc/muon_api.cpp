@@ -283,7 +283,9 @@ size_t meta_bound(const std::vector<UnitDesc>& units) {
         g = std::max(g, g2);
         // tile lists (room for twice the tiles, as if every tile were split in
         // halves) and pair offsets
-        b += sizeof(EwUnit) + sizeof(NsUnit) + sizeof(EwMaps) + 8 * 256 + u.cnt_bytes +
+        // (per unit: 256-byte alignment of 8 tables, and room for a group's
+        // counter header, as if every unit were a group)
+        b += sizeof(EwUnit) + sizeof(NsUnit) + sizeof(EwMaps) + 9 * 256 + u.cnt_bytes +
              2 * size_t(2 * s + g) * sizeof(TileItem) + 3 * 4 * 1024;
     }
     return align_up(b, 1024);
@@ -655,12 +657,14 @@ int build_plan(muon_ctx* h, int mode, int nb, int64_t chunk_elems = 0) {
         g.ns_off = off;
         off += sizeof(NsUnit) * nu;
         g.shards = P.units[g.u0].shards;
-        // tile counters of chained launches, zero in the uploaded image
+        // tile counters of chained launches (a header, then every unit's),
+        // zero in the uploaded image
         off = align_up(off, 256);
         g.rc_off = off;
+        off += CNT_HEADER_WORDS * 4;
         for (int i = g.u0; i < g.u1; ++i) off += P.units[i].cnt_bytes;
         g.rc_bytes = off - g.rc_off;
-        size_t rc_next = g.rc_off;
+        size_t rc_next = g.rc_off + CNT_HEADER_WORDS * 4;
         std::vector<TileItem> tsx, tsa, tg;
         int64_t tile_base = 0;
         for (int i = g.u0; i < g.u1; ++i) {
@@ -1150,8 +1154,6 @@ int step_impl(muon_ctx* h, float lr, float beta, int nesterov, int ns_steps, flo
             std::max<int64_t>(1, ceil_div(g.ew_tiles, int64_t(ew_grid_cap)));
         const int ew_grid = static_cast<int>(ceil_div(g.ew_tiles, ew_per_block));
         const bool fused = h->pair && h->fuse;
-        ew.cnt_zero = g.chain_ok ? reinterpret_cast<int32_t*>(ws + g.rc_off) : nullptr;
-        ew.cnt_words = g.chain_ok ? static_cast<int64_t>(g.rc_bytes / 4) : 0;
         ew.write_x = fused ? 1 : 0;
         cudaError_t e;
         if (!begin(ST_MOMENTUM)) return fail(h, MUON_ERR_CUDA, "event create");
@@ -1210,6 +1212,8 @@ int step_impl(muon_ctx* h, float lr, float beta, int nesterov, int ns_steps, flo
             L.ep_a = h->debug_chain_skew;
             L.ep_b = 0;
             L.shards = 1;
+            L.cnt_block = reinterpret_cast<int32_t*>(ws + g.rc_off);
+            L.cnt_words = static_cast<int32_t>(g.rc_bytes / 4);
             if (!begin(ST_CHAIN)) return fail(h, MUON_ERR_CUDA, "event create");
             e = launch_ns_pair(OP_CHAIN, L, g.p_c, h->stages, h->stream);
             end();

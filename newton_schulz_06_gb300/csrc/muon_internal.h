@@ -78,7 +78,7 @@ struct alignas(128) NsUnit {
     // X tiles (ti, cj) at tile_cnt[ti * RT + cj], then A tiles (i <= j) at
     // tile_cnt[T * RT + i * T + j] and B tiles at tile_cnt[T * RT + T * T +
     // i * T + j]; T = 256-row blocks of m, RT = 256-column blocks of n.
-    // They only grow.
+    // Zero at the start of every launch (see NsLaunch::cnt_block).
     int32_t* tile_cnt;
     int32_t m, n, ld_x, ld_mm;
 };
@@ -99,6 +99,8 @@ struct TileItem {
 constexpr int TILE_OP_MASK = 3;
 // epilogue warps of a CTA pair (each counts once per finished tile and row)
 constexpr int PAIR_EPI_WARPS = 16;
+// header words of a group's counter block (NsLaunch::cnt_block)
+constexpr int CNT_HEADER_WORDS = 64;
 
 // OP_CHAIN: iterations 1 .. iters of Newton-Schulz in one launch, every
 // product but the last X update.  Each pair walks its one-iteration list
@@ -140,7 +142,7 @@ struct NsLaunch {
     // OP_CHAIN: iterations in the launch; pair_end_last[p]: end of pair p's
     // list without its X-update tiles (the last iteration's walk); ep_x,
     // ep_a, ep_b: rounds the X, A and B counters held when the launch began
-    // (0: the step's momentum pass zeroes them; the A rounds carry a test
+    // (the counters are zero at launch, so 0; the A rounds carry a test
     // skew when muon_debug_set_chain_test asks for one).  An X tile read in
     // iteration s is complete once its counter reaches PAIR_EPI_WARPS *
     // (ep_x + s - 1), an A tile once PAIR_EPI_WARPS * (ep_a + s), a B tile
@@ -151,6 +153,12 @@ struct NsLaunch {
     // weight update folded in (W read and written by TMA; no X' stored)
     int32_t chain_last;
     int32_t ep_x, ep_a, ep_b;
+    // OP_CHAIN: the group's counter block (cnt_words words: a header of 64
+    // words, word 0 counting the CTAs that have left the launch, then every
+    // unit's tile_cnt block).  The last CTA to leave zeroes the block, so
+    // the next launch finds it zero (the uploaded plan starts it at zero).
+    int32_t* cnt_block;
+    int32_t cnt_words;
     // Distributed mode, first product (CTA-pair kernels): the K range of
     // every tile is `shards` equal slices.  The pair runs them in turn, slice
     // 0 into accumulator 0 and each later slice into accumulator 1, which
@@ -184,11 +192,6 @@ struct EwLaunch {
     float lr;
     int32_t src;             // X buffer holding the final iterate (update)
     float eps;
-    // momentum pass, block 0: zero the group's tile counters (chained
-    // launches) once the previous step's kernels are complete, so that
-    // every step's chained launch counts from zero (nullptr: none)
-    int32_t* cnt_zero;
-    int64_t cnt_words;
 };
 
 // Programmatic dependent launch: kernels are launched so that they may start

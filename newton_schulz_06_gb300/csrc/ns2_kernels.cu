@@ -32,7 +32,9 @@
 // finished tiles on per-tile counters (after their TMA stores complete),
 // and an eleventh warp per CTA polls the counters of the producer's coming
 // chunks and publishes how many are ready through shared memory, so the
-// producer's loop never waits on global memory.
+// producer's loop never waits on global memory.  The last CTA to leave
+// zeroes the counters, so every launch (a replay of a captured graph too)
+// starts from zero.
 //
 // Distributed mode's first product (SL = 1) runs each tile's K slices in
 // turn on the same pair and sums them in tensor memory (accumulator 0 holds
@@ -40,8 +42,10 @@
 //
 // Symmetric stages compute tiles (ti, tj) with ti <= tj on the 256 grid
 // ("Advancing Emerging Optimizers for Accelerated LLM Training", section
-// "SYRK and fused all-reduce": upper-triangle tiles, diagonal tiles in full,
-// the full matrix written) and mirror every element above the diagonal.
+// "SYRK and fused all-reduce": upper-triangle tiles, diagonal tiles in
+// full) and store them as computed; nothing below the diagonal tiles is
+// written.  Consumers read the k-blocks left of an operand's diagonal tile
+// from the stored transpose.
 //
 // Every wait is bounded as in the single-CTA kernels.
 #include "../../include/muon.h"
@@ -539,8 +543,9 @@ __device__ __forceinline__ InPlan plan_blocks(const NsLaunch& p, const TileItem&
     for (int c = 0; c < 4; ++c) {
         const int gc0 = q.col0 + 32 * c;
         const int rel = half * 128 + 32 * c;          // column within the tile
-        bool nd = q.r0w < m && gc0 < lim_c && rel >= t.n_off && rel < t.n_off + t.n_len;
-        if (op != OP_GEMM_BX) nd = nd && gc0 >= q.r0w;    // upper blocks only
+        // every block of the tile (a symmetric product's diagonal tile is
+        // stored whole, each warp storing what its TMEM lanes computed)
+        const bool nd = q.r0w < m && gc0 < lim_c && rel >= t.n_off && rel < t.n_off + t.n_len;
         if (nd) q.order |= static_cast<uint32_t>(c) << (2 * q.n++);
     }
     return q;
@@ -728,7 +733,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
     uint64_t* in_bar = bars + 2 * P_STAGES + 5;    // NS per epilogue warp
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_bar + P_IN_SLOTS_MAX * P_EPI_WARPS);
     static_assert(p_smem<OP, P_STAGES, FW>() <= 232448, "shared memory per CTA");
-    static_assert((2 * P_STAGES + 5 + P_IN_SLOTS_MAX * P_EPI_WARPS) * 8 + 8 + 24 <= 1024,
+    static_assert((2 * P_STAGES + 5 + P_IN_SLOTS_MAX * P_EPI_WARPS) * 8 + 8 + 24 + 8 <= 1024,
                   "barrier area");
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // chained launches: the watcher warp's ready chunks of tile number tno
@@ -736,6 +741,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
     // in prod_seq
     uint64_t* dep_slot = reinterpret_cast<uint64_t*>(tmem_slot + 2);
     uint64_t* prod_seq = dep_slot + 2;
+    // chained launches: is this CTA the last to leave?
+    volatile int* leave_last = reinterpret_cast<volatile int*>(prod_seq + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1320,41 +1327,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] *= scale;
                 }
-                if (op == OP_GEMM_BX) {
-                    if (OP != OP_CHAIN && p.last) {     // a chain never holds the last
-                        stage_free(lane);
-                        gemm_update_block(u, r0w, gc0, lane, v, s_st + (st_seq & 1u) * P_BLK);
-                    } else {
-                        uint8_t* st = next_stage(s_st, st_seq, lane);
-                        st_row_bf16(st, lane, v);
-                        store_block(u.te_out, st, gc0, r0w, lane);
-                    }
-                } else if (gc0 == r0w) {
-                    // diagonal block: upper part as computed, lower part
-                    // mirrored from the upper, so the block is symmetric
-                    uint8_t* st = next_stage(s_st, st_seq, lane);
-                    st_col_bf16(st, lane, v);
-                    __syncwarp();
-                    float mir[32];
-                    ld_row_bf16(st, lane, mir);
-                    __syncwarp();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (e < lane) v[e] = mir[e];
-                    st_row_bf16(st, lane, v);
-                    store_block(u.te_out, st, gc0, r0w, lane);
+                if (OP != OP_CHAIN && op == OP_GEMM_BX && p.last) {   // a chain never holds the last
+                    stage_free(lane);
+                    gemm_update_block(u, r0w, gc0, lane, v, s_st + (st_seq & 1u) * P_BLK);
                 } else {
+                    // every block as computed: X', and the symmetric
+                    // products' tiles on or above the diagonal, where a
+                    // diagonal tile comes out whole (its pair computes both
+                    // triangles; consumers read whole rows of it)
                     uint8_t* st = next_stage(s_st, st_seq, lane);
                     st_row_bf16(st, lane, v);
                     store_block(u.te_out, st, gc0, r0w, lane);
-                    if (t.ti == t.tj) {
-                        // a diagonal tile is stored whole: its lower part
-                        // too (consumers read whole rows of it); other
-                        // tiles are read through their stored transpose
-                        st = next_stage(s_st, st_seq, lane);
-                        st_col_bf16(st, lane, v);
-                        store_block(u.te_out, st, r0w, gc0, lane);   // mirror
-                    }
                 }
             }
             if (!__all_sync(0xffffffffu, ok)) break;
@@ -1389,6 +1372,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                      "r"(P_TMEM_COLS)
                      : "memory");
+    }
+    if (OP == OP_CHAIN) {
+        // the last CTA to leave (every counter read and raise of the launch
+        // done) zeroes the group's counters for the next launch
+        if (threadIdx.x == 0) {
+            fence_acq_rel_gpu();
+            *leave_last = count_fetch_add(p.cnt_block) == static_cast<int32_t>(gridDim.x) - 1;
+        }
+        __syncthreads();
+        if (*leave_last)
+            for (int i = threadIdx.x; i < p.cnt_words; i += blockDim.x) p.cnt_block[i] = 0;
     }
 }
 

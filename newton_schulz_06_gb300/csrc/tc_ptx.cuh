@@ -152,6 +152,16 @@ __device__ __forceinline__ void count_release(int32_t* cnt) {
     asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(cnt) : "memory");
 }
 
+// Adds n to a global counter (acquire and release) and returns its old value.
+__device__ __forceinline__ int32_t count_fetch_add(int32_t* cnt, int32_t n = 1) {
+    int32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(cnt), "r"(n)
+                 : "memory");
+    return old;
+}
+
 // Orders this thread's generic-proxy and async-proxy (TMA) accesses to
 // global memory with each other.
 __device__ __forceinline__ void fence_proxy_async_global() {

@@ -426,8 +426,8 @@ def test_chained_fp32_weights_match_oracle(monkeypatch):
 def test_step_captured_in_cuda_graph_replays_bitexact(shapes):
     """A step captured into a CUDA graph (after one plain step has built the
     plan) and replayed gives the same bits as plain steps: one group that
-    chains (its tile counters are zeroed by every step's momentum pass, so
-    replays carry no stale counts) and one that runs a launch per product.
+    chains (the last CTA of every chained launch zeroes its tile counters,
+    so replays carry no stale counts) and one that runs a launch per product.
     Plain steps after the replays stay in agreement too."""
     trips = [case(r, c, 960 + i) for i, (r, c) in enumerate(shapes)]
     clones = [[t.clone() for t in tr] for tr in trips]
