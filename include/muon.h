@@ -250,6 +250,68 @@ typedef struct {
 } muon_plan_info;
 MUON_API int muon_get_plan_info(muon_handle h, int mode, int nb, muon_plan_info* out);
 
+/* ---- distributed mode across ranks ------------------------------------- */
+
+/* "Advancing Emerging Optimizers for Accelerated LLM Training", section
+ * "Distributed mode": the iterate X (m x n, short side first) of one matrix
+ * is split along n over the P ranks of a tensor-parallel group, one GPU
+ * each.  A rank holds its slice of W, G and M and runs the step in phases;
+ * between the phases the caller sums across the group (an all-reduce, e.g.
+ * torch.distributed over NCCL).  Per iteration the only exchange is the sum
+ * of the partial products X_r X_r^T (the all-reduce after the first matrix
+ * product), plus one sum of squares for the norm before the first:
+ *
+ *   muon_dist_momentum(h, ...)        momentum on the slice; the slice's
+ *                                     sum of squares of U -> sumsq
+ *   [sum sumsq over the group]
+ *   for s = 0 .. ns_steps - 1:
+ *     muon_dist_gram(h, ...)          the partial X_r X_r^T -> A (fp32)
+ *     [sum A over the group]
+ *     muon_dist_update(h, ...)        B' = b A + c A A + a I from the sum,
+ *                                     X_r <- B' X_r; on the last iteration
+ *                                     W_r <- W_r - lr * scale * O_r
+ *
+ * The handle must hold exactly one registered parameter, the rank's slice,
+ * and must have been configured with muon_dist_configure first; the phases
+ * use its workspace (muon_workspace_size with MUON_FULL).  Phases are queued
+ * on the handle's stream in the order above; errors as for muon_step, and
+ * MUON_ERR_STATE for a phase out of order.  The weight update of the last
+ * iteration is folded into the X update as in muon_step. */
+
+/* The slice's place in the whole matrix: transposed = 1 if the whole weight
+ * is tall (rows > cols; its iterate is W^T, and the slice is a block of W's
+ * rows), 0 otherwise (the slice is a block of W's columns); shape_scale =
+ * the whole matrix's max(1, rows / cols) ** 0.5.  The slice's short side must
+ * then be the whole matrix's short side: its iterate is m x n_r with
+ * m = cols (transposed) or rows.  Invalidates the plan. */
+MUON_API int muon_dist_configure(muon_handle h, int transposed, float shape_scale);
+
+/* M <- beta M + G and U on the slice; the iterate slice X_r = bf16(U), not
+ * yet normalised.  *sumsq (device memory, one double) receives the slice's
+ * sum of U^2, taken per 64 x 64 tile and then over the tiles in a fixed
+ * order, so that the sum of all slices' values is ||U||_F^2. */
+MUON_API int muon_dist_momentum(muon_handle h, float beta, int nesterov, double* sumsq);
+
+/* Iteration s's partial product A_r = X_r X_r^T of the slice, unscaled fp32,
+ * into the m x m row-major device buffer a (leading dimension lda >= m),
+ * for the 256 x 256 tiles (ti, tj) with ti <= tj and band_begin <= ti <
+ * band_end (256-row blocks; band_end = -1: to the last).  Nothing else of a
+ * is written: the caller zeroes it once, so that the tiles below the
+ * diagonal stay zero, and may sum the bands as each is queued (the
+ * "SYRK and fused all-reduce" exchange of finished upper tiles). */
+MUON_API int muon_dist_gram(muon_handle h, float* a, int64_t lda, int band_begin,
+                            int band_end);
+
+/* The rest of iteration s from the group's sum of the partial products in
+ * a (fp32, upper tiles as written by muon_dist_gram): A = bf16(sum * scale)
+ * with scale = 1 / (||U||_F + eps)^2 when first (sumsq_total: device double,
+ * the group's sum of the momentum phase's values; ignored otherwise), then
+ * B' = b A + c A A + a I and X_r <- B' X_r (times 1 / (||U||_F + eps) when
+ * first).  When last, the update O_r = X_r (transposed back) is applied:
+ * W_r <- W_r - lr * shape_scale * O_r. */
+MUON_API int muon_dist_update(muon_handle h, const float* a, int64_t lda, int first, int last,
+                              const double* sumsq_total, float lr, float ca, float cb, float cc);
+
 /* ---- step without a workspace ------------------------------------------ */
 
 /* One Muon step (full mode) on ONE matrix without any workspace: the plan

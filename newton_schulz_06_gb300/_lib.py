@@ -36,7 +36,9 @@ EXPORTS = ("muon_create", "muon_set_stream", "muon_register_params",
            "muon_set_profiling", "muon_stage_times", "muon_last_launch_count",
            "muon_debug_set_exports", "muon_get_plan_info",
            "muon_step_noalloc", "muon_debug_wait_timeout", "muon_step_host",
-           "muon_debug_check_chain_schedule", "muon_debug_set_chain_test")
+           "muon_debug_check_chain_schedule", "muon_debug_set_chain_test",
+           "muon_dist_configure", "muon_dist_momentum", "muon_dist_gram",
+           "muon_dist_update")
 
 
 class MuonParam(ctypes.Structure):
@@ -106,6 +108,11 @@ def lib() -> ctypes.CDLL:
         "muon_debug_set_chain_test": [H, i32],
         "muon_step_host": [H, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), f32,
                            f32, i32, i32, f32, f32, f32, i32, i32],
+        "muon_dist_configure": [H, i32, f32],
+        "muon_dist_momentum": [H, f32, i32, vp],
+        "muon_dist_gram": [H, vp, ctypes.c_int64, i32, i32],
+        "muon_dist_update": [H, vp, ctypes.c_int64, i32, i32, vp, f32, f32, f32,
+                             f32],
     }
     for name, args in sig.items():
         fn = getattr(L, name)

@@ -444,11 +444,9 @@ ew_momentum_tma_kernel(const EwLaunch p) {
 // Per unit: ||U||_F from its tile sums in a fixed order (fp64), then
 // inv_norm = 1 / (||U|| + eps).  One block per unit: thread k sums tiles
 // k, k + 256, ... in order, then a fixed tree combines the 256 sums.
-__global__ void __launch_bounds__(256) ew_norm_kernel(const EwLaunch p) {
-    grid_dependency_wait();
-    allow_dependent_launch();
-    __shared__ double red[256];
-    const int u = blockIdx.x;
+// Unit u's sum of its tile sums in that order, by one block of 256 threads;
+// the result in thread 0 (red: 256 doubles of shared memory).
+__device__ __forceinline__ double unit_sum_squares(const EwLaunch& p, int u, double* red) {
     const EwUnit& U = p.units[u];
     const int64_t base = U.tile_base * EW_PARTIALS_PER_TILE;
     const int64_t count = U.tile_count * EW_PARTIALS_PER_TILE;
@@ -462,8 +460,57 @@ __global__ void __launch_bounds__(256) ew_norm_kernel(const EwLaunch p) {
         if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
         __syncthreads();
     }
+    return red[0];
+}
+
+__global__ void __launch_bounds__(256) ew_norm_kernel(const EwLaunch p) {
+    grid_dependency_wait();
+    allow_dependent_launch();
+    __shared__ double red[256];
+    const int u = blockIdx.x;
+    const double ss = unit_sum_squares(p, u, red);
     if (threadIdx.x == 0)
-        p.inv_norm[u] = static_cast<float>(1.0 / (sqrt(red[0]) + (double)p.eps));
+        p.inv_norm[u] = static_cast<float>(1.0 / (sqrt(ss) + (double)p.eps));
+}
+
+// Distributed mode across ranks: the slice's sum of squares itself, summed
+// over the group by the caller; the norm follows in dist_convert_kernel with
+// the same arithmetic as ew_norm_kernel.
+__global__ void __launch_bounds__(256) ew_sumsq_kernel(const EwLaunch p, double* out) {
+    grid_dependency_wait();
+    allow_dependent_launch();
+    __shared__ double red[256];
+    const double ss = unit_sum_squares(p, 0, red);
+    if (threadIdx.x == 0) *out = ss;
+}
+
+// Distributed mode across ranks: the group's summed fp32 partial products to
+// the bf16 A buffer the second product reads, on and above the 256-tile
+// diagonal (what the symmetric products' consumers read), times inv^2 in
+// iteration 1: A = bf16(sum * scale), the first product's epilogue rounding
+// of a one-GPU step.  One thread per 4 consecutive columns of a row.
+__global__ void __launch_bounds__(256) dist_convert_kernel(const DistLaunch p) {
+    grid_dependency_wait();
+    allow_dependent_launch();
+    float scale = 1.f;
+    if (p.first) {
+        const float inv = static_cast<float>(1.0 / (sqrt(*p.sumsq_total) + (double)p.eps));
+        scale = inv * inv;
+        if (blockIdx.x == 0 && threadIdx.x == 0) *p.inv_norm = inv;
+    }
+    const int64_t q4 = (p.m + 3) / 4;              // 4-column groups per row
+    const int64_t total = static_cast<int64_t>(p.m) * q4;
+    for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int i = static_cast<int>(g / q4);
+        const int j0 = static_cast<int>(g - static_cast<int64_t>(i) * q4) * 4;
+        if ((j0 >> 8) < (i >> 8)) continue;          // below the diagonal tiles
+        const float* src = p.a32 + static_cast<int64_t>(i) * p.lda32 + j0;
+        __nv_bfloat16* dst = p.a16 + static_cast<int64_t>(i) * p.ld_mm + j0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (j0 + e < p.m) dst[e] = __float2bfloat16_rn(src[e] * scale);
+    }
 }
 
 // Pass 2: X0 = bf16(U * inv_norm) in the X orientation.
@@ -604,6 +651,14 @@ cudaError_t launch_ew_momentum_tma(const EwLaunch& p, int grid, bool g_f32, cuda
 
 cudaError_t launch_ew_norm(const EwLaunch& p, cudaStream_t s) {
     return launch_kernel(ew_norm_kernel, dim3(p.num_units), dim3(256), 0, s, p);
+}
+
+cudaError_t launch_ew_sumsq(const EwLaunch& p, double* out, cudaStream_t s) {
+    return launch_kernel(ew_sumsq_kernel, dim3(1), dim3(256), 0, s, p, out);
+}
+
+cudaError_t launch_dist_convert(const DistLaunch& p, int grid, cudaStream_t s) {
+    return launch_kernel(dist_convert_kernel, dim3(grid), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_ew_normalise(const EwLaunch& p, int grid, cudaStream_t s) {

@@ -75,10 +75,15 @@ struct GroupDesc {
     int n_c = 0, p_c = 0;
     bool chain_ok = false;
     // this group's tile counters (chained launches): in the metadata region
-    // (never aliased by a group's scratch), zeroed by every step's momentum
-    // pass, so a step's launches carry no state from earlier steps (a step
-    // captured in a CUDA graph replays correctly)
+    // (never aliased by a group's scratch), zeroed by the chained launch's
+    // last CTA, so a step's launches carry no state from earlier steps (a
+    // step captured in a CUDA graph replays correctly)
     size_t rc_off = 0, rc_bytes = 0;
+    // distributed mode across ranks: the first product's tiles in row-block
+    // order (in the chained launch's space, unused then), and where each
+    // 256-row block's tiles start (T + 1 entries)
+    size_t t_d_off = 0;
+    std::vector<int> d_band;
     int64_t ew_tiles = 0;
     int shards = 1;                          // distributed mode: P
 };
@@ -95,6 +100,8 @@ struct Plan {
     std::vector<UnitDesc> units;
     std::vector<GroupDesc> groups;
     size_t scratch_off = 0;                  // start of the group scratch
+    // distributed mode across ranks (one unit): its bf16 A buffer
+    __nv_bfloat16* d_a16 = nullptr;
     int64_t syrk_tiles = 0, gemm_tiles = 0, ew_tiles = 0;
     int64_t useful_flops_iter = 0, executed_flops_iter = 0;
 };
@@ -149,6 +156,17 @@ struct muon_ctx {
     // units are small (EWT_MAX_TILES_PER_UNIT), 2 = wherever the maps allow
     // it, 0 = never
     int ew_tma = 1;
+    // distributed mode across ranks (muon_dist_configure): the one
+    // registered parameter is a rank's slice of a matrix whose orientation
+    // (dist_transposed) and shape scale (dist_scale) it takes
+    bool dist = false;
+    int dist_transposed = 0;
+    float dist_scale = 1.f;
+    // the phases' progress: momentum done, grams queued this iteration, the
+    // X buffer holding the iterate
+    bool dist_ready = false;
+    int dist_grams = 0;
+    int dist_cur = 0;
 };
 
 namespace {
@@ -226,6 +244,10 @@ int build_units(muon_ctx* h, int mode, int nb, std::vector<UnitDesc>* out) {
     if (nblk < 1 || shards < 1) return fail(h, MUON_ERR_INVALID_ARG, "nb must be >= 1");
     if (shards > 1 && !h->pair)
         return fail(h, MUON_ERR_UNSUPPORTED, "distributed mode needs the CTA-pair kernels");
+    if (h->dist && (mode != MUON_FULL || h->params.size() != 1 || !h->pair))
+        return fail(h, MUON_ERR_UNSUPPORTED,
+                    "a rank's slice (muon_dist_configure) runs alone, in full mode, on the "
+                    "CTA-pair kernels");
     for (size_t i = 0; i < h->params.size(); ++i) {
         const muon_param& p = h->params[i];
         if (p.cols % nblk != 0)
@@ -251,6 +273,17 @@ int build_units(muon_ctx* h, int mode, int nb, std::vector<UnitDesc>* out) {
             u.ld_mm = static_cast<int>(align_up(u.m, 64));
             u.scale = static_cast<float>(
                 std::sqrt(std::max(1.0, double(p.rows) / double(bc))));
+            if (h->dist) {
+                // a rank's slice: the whole matrix's orientation and scale
+                u.transposed = h->dist_transposed != 0;
+                u.m = static_cast<int>(u.transposed ? bc : p.rows);
+                u.n = static_cast<int>(u.transposed ? p.rows : bc);
+                u.scale = h->dist_scale;
+                if (u.m > MAX_SHORT)
+                    return fail(h, MUON_ERR_UNSUPPORTED, "short side above 32768");
+                u.ld_x = static_cast<int>(align_up(u.n, 64));
+                u.ld_mm = static_cast<int>(align_up(u.m, 64));
+            }
             u.x_bytes = align_up(size_t(u.m) * u.ld_x * 2, 1024);
             u.mm_bytes = align_up(size_t(u.m) * u.ld_mm * 2, 1024);
             u.shards = shards;
@@ -773,6 +806,7 @@ int build_plan(muon_ctx* h, int mode, int nb, int64_t chunk_elems = 0) {
             ns.x[0] = e.x[0];
             ns.x[1] = e.x[1];
             ns.a = reinterpret_cast<__nv_bfloat16*>(ab);
+            if (h->dist) P.d_a16 = reinterpret_cast<__nv_bfloat16*>(ab);
             ns.b = reinterpret_cast<__nv_bfloat16*>(bb);
             ns.tile_cnt = reinterpret_cast<int32_t*>(ws + rc_next);
             rc_next += u.cnt_bytes;
@@ -823,7 +857,23 @@ int build_plan(muon_ctx* h, int mode, int nb, int64_t chunk_elems = 0) {
         put(tsx, &g.t_sx_off, &g.n_sx, &g.o_sx_off, &g.p_sx);
         put(tsa, &g.t_sa_off, &g.n_sa, &g.o_sa_off, &g.p_sa);
         put(tg, &g.t_g_off, &g.n_g, &g.o_g_off, &g.p_g);
-        g.chain_ok = chain_eligible(h, g.shards, static_cast<int64_t>(tg0.size()));
+        g.chain_ok = !h->dist && chain_eligible(h, g.shards, static_cast<int64_t>(tg0.size()));
+        if (h->dist) {
+            // a rank's slice: the first product's tiles by row block, in the
+            // space a chained launch would use
+            std::vector<TileItem> vd = tsx0;
+            std::stable_sort(vd.begin(), vd.end(), [](const TileItem& x, const TileItem& y) {
+                return x.ti != y.ti ? x.ti < y.ti : x.tj < y.tj;
+            });
+            const int T = static_cast<int>(ceil_div(P.units[g.u0].m, 256));
+            g.d_band.assign(T + 1, static_cast<int>(vd.size()));
+            for (int k = static_cast<int>(vd.size()) - 1; k >= 0; --k) g.d_band[vd[k].ti] = k;
+            for (int b = T - 1; b >= 0; --b) g.d_band[b] = std::min(g.d_band[b], g.d_band[b + 1]);
+            off = align_up(off, 256);
+            g.t_d_off = off;
+            std::memcpy(meta.data() + off, vd.data(), vd.size() * sizeof(TileItem));
+            off += vd.size() * sizeof(TileItem);
+        }
         if (g.chain_ok) {
             const int pairs = std::max(
                 1, std::min(h->max_pairs,
@@ -1051,6 +1101,8 @@ int step_impl(muon_ctx* h, float lr, float beta, int nesterov, int ns_steps, flo
     if (!h) return MUON_ERR_INVALID_ARG;
     if (h->device == MUON_HOST_ONLY) return fail(h, MUON_ERR_STATE, "host-only handle");
     if (h->params.empty()) return fail(h, MUON_ERR_STATE, "no parameters registered");
+    if (h->dist)
+        return fail(h, MUON_ERR_STATE, "a rank's slice steps through the muon_dist_* phases");
     if (ns_steps < 1 || ns_steps > 64)
         return fail(h, MUON_ERR_INVALID_ARG, "ns_steps must be in 1..64");
     if (!std::isfinite(lr) || !std::isfinite(beta) || !std::isfinite(a) ||
@@ -1324,6 +1376,206 @@ int step_impl(muon_ctx* h, float lr, float beta, int nesterov, int ns_steps, flo
     return MUON_OK;
 }
 
+// Distributed mode across ranks: checks shared by the phases, and the plan
+// (full mode, the one slice) built on first use.
+int dist_prepare(muon_ctx* h) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (h->device == MUON_HOST_ONLY) return fail(h, MUON_ERR_STATE, "host-only handle");
+    if (!h->dist) return fail(h, MUON_ERR_STATE, "muon_dist_configure has not been called");
+    if (h->params.size() != 1)
+        return fail(h, MUON_ERR_STATE, "a rank's slice handle holds exactly one parameter");
+    Plan& P = h->plan;
+    if (!P.valid || P.mode != MUON_FULL || P.nb != 1 || P.ws != h->ws ||
+        P.ws_bytes != h->ws_bytes) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (h->stream && cudaStreamIsCapturing(h->stream, &cap) != cudaSuccess)
+            return fail(h, MUON_ERR_CUDA, "stream capture query");
+        if (cap != cudaStreamCaptureStatusNone)
+            return fail(h, MUON_ERR_STATE, "the plan must be built before stream capture");
+        const int rc = build_plan(h, MUON_FULL, 1, 0);
+        if (rc) {
+            P.valid = false;
+            return rc;
+        }
+        h->dist_ready = false;
+    }
+    if (P.groups.size() != 1)
+        return fail(h, MUON_ERR_STATE, "internal: a rank's slice plan has one group");
+    return MUON_OK;
+}
+
+// The NsLaunch fields every phase's tensor-core launch shares.
+NsLaunch dist_launch(muon_ctx* h, float ca, float cb, float cc, float lr) {
+    Plan& P = h->plan;
+    const GroupDesc& g = P.groups[0];
+    char* ws = static_cast<char*>(h->ws);
+    NsLaunch L{};
+    L.units = reinterpret_cast<const NsUnit*>(ws + g.ns_off);
+    L.a = ca;
+    L.b = cb;
+    L.c = cc;
+    L.wait_limit_ns = h->wait_limit_ns;
+    L.err = reinterpret_cast<int*>(ws);
+    L.inv_norm = reinterpret_cast<float*>(ws + P.scratch_off);
+    L.ew = reinterpret_cast<const EwUnit*>(ws + g.ew_off);
+    L.lr = lr;
+    L.iters = 1;
+    L.shards = 1;
+    return L;
+}
+
+// The element-wise launch fields of the slice's group.
+EwLaunch dist_ew(muon_ctx* h) {
+    Plan& P = h->plan;
+    const GroupDesc& g = P.groups[0];
+    char* ws = static_cast<char*>(h->ws);
+    EwLaunch ew{};
+    ew.units = reinterpret_cast<const EwUnit*>(ws + g.ew_off);
+    ew.tile_base = reinterpret_cast<const int64_t*>(ws + g.tb_off);
+    ew.num_units = 1;
+    ew.num_tiles = g.ew_tiles;
+    ew.partial = reinterpret_cast<float*>(ws + align_up(P.scratch_off + 4, 256));
+    ew.inv_norm = reinterpret_cast<float*>(ws + P.scratch_off);
+    ew.eps = NORM_EPS;
+    ew.err = reinterpret_cast<int*>(ws);
+    ew.wait_limit_ns = h->wait_limit_ns;
+    return ew;
+}
+
+int dist_ew_grid(muon_ctx* h) {
+    const int64_t tiles = h->plan.groups[0].ew_tiles;
+    const int64_t per_block = std::max<int64_t>(1, ceil_div(tiles, int64_t(h->num_sms) * 8));
+    return static_cast<int>(ceil_div(tiles, per_block));
+}
+
+int dist_momentum(muon_ctx* h, float beta, int nesterov, double* sumsq) {
+    if (int rc = dist_prepare(h)) return rc;
+    if (!sumsq) return fail(h, MUON_ERR_INVALID_ARG, "sumsq is null");
+    if (!std::isfinite(beta)) return fail(h, MUON_ERR_INVALID_ARG, "non-finite beta");
+    DeviceGuard guard(h->device);
+    const GroupDesc& g = h->plan.groups[0];
+    char* ws = static_cast<char*>(h->ws);
+    EwLaunch ew = dist_ew(h);
+    ew.beta = beta;
+    ew.nesterov = nesterov ? 1 : 0;
+    ew.src = 0;
+    ew.maps = g.ew_tma ? reinterpret_cast<const EwMaps*>(ws + g.em_off) : nullptr;
+    ew.write_x = 1;
+    cudaError_t e;
+    if (ew.maps)
+        e = launch_ew_momentum_tma(
+            ew, static_cast<int>(std::min<int64_t>(g.ew_tiles, int64_t(EWT_CTAS_PER_SM) *
+                                                                   h->num_sms)),
+            g.g_f32, h->stream);
+    else
+        e = launch_ew_momentum(ew, dist_ew_grid(h), h->stream);
+    if (e == cudaSuccess) e = launch_ew_sumsq(ew, sumsq, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "momentum phase launch");
+    h->dist_ready = true;
+    h->dist_grams = 0;
+    h->dist_cur = 0;
+    return MUON_OK;
+}
+
+int dist_gram(muon_ctx* h, float* a, int64_t lda, int band_begin, int band_end) {
+    if (int rc = dist_prepare(h)) return rc;
+    if (!h->dist_ready)
+        return fail(h, MUON_ERR_STATE, "muon_dist_gram before muon_dist_momentum");
+    const Plan& P = h->plan;
+    const GroupDesc& g = P.groups[0];
+    const int m = P.units[g.u0].m;
+    const int T = static_cast<int>(g.d_band.size()) - 1;
+    if (!a || lda < m) return fail(h, MUON_ERR_INVALID_ARG, "a is null or lda < m");
+    if (band_end < 0) band_end = T;
+    if (band_begin < 0 || band_begin > band_end || band_end > T)
+        return fail(h, MUON_ERR_INVALID_ARG, "band outside the 256-row blocks of A");
+    DeviceGuard guard(h->device);
+    const int t0 = g.d_band[band_begin], t1 = g.d_band[band_end];
+    h->dist_grams += 1;
+    if (t1 == t0) return MUON_OK;
+    NsLaunch L = dist_launch(h, 0.f, 0.f, 0.f, 0.f);
+    char* ws = static_cast<char*>(h->ws);
+    L.tiles = reinterpret_cast<const TileItem*>(ws + g.t_d_off) + t0;
+    L.num_tiles = t1 - t0;
+    L.pair_off = nullptr;
+    L.src = h->dist_cur;
+    L.first = 0;                 // scaled after the group's sum
+    L.last = 0;
+    L.a32 = a;
+    L.lda32 = lda;
+    const int pairs = std::max(1, std::min(h->max_pairs, t1 - t0));
+    const cudaError_t e = launch_ns_pair_gram32(L, pairs, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "first product launch");
+    return MUON_OK;
+}
+
+int dist_update(muon_ctx* h, const float* a, int64_t lda, int first, int last,
+                const double* sumsq_total, float lr, float ca, float cb, float cc) {
+    if (int rc = dist_prepare(h)) return rc;
+    if (!h->dist_ready || h->dist_grams == 0)
+        return fail(h, MUON_ERR_STATE, "muon_dist_update before this iteration's muon_dist_gram");
+    if (!std::isfinite(lr) || !std::isfinite(ca) || !std::isfinite(cb) || !std::isfinite(cc))
+        return fail(h, MUON_ERR_INVALID_ARG, "non-finite hyper-parameter");
+    Plan& P = h->plan;
+    const GroupDesc& g = P.groups[0];
+    const UnitDesc& u = P.units[g.u0];
+    if (!a || lda < u.m) return fail(h, MUON_ERR_INVALID_ARG, "a is null or lda < m");
+    if (first && !sumsq_total) return fail(h, MUON_ERR_INVALID_ARG, "sumsq_total is null");
+    DeviceGuard guard(h->device);
+    char* ws = static_cast<char*>(h->ws);
+    DistLaunch d{};
+    d.a32 = a;
+    d.lda32 = lda;
+    d.a16 = P.d_a16;
+    d.ld_mm = u.ld_mm;
+    d.m = u.m;
+    d.first = first ? 1 : 0;
+    d.sumsq_total = sumsq_total;
+    d.inv_norm = reinterpret_cast<float*>(ws + P.scratch_off);
+    d.eps = NORM_EPS;
+    cudaError_t e = launch_dist_convert(d, h->num_sms * 4, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "conversion launch");
+    NsLaunch L = dist_launch(h, ca, cb, cc, lr);
+    L.src = h->dist_cur;
+    L.first = 0;
+    L.last = 0;
+    // the second product: B' = b A + c A A + a I
+    L.tiles = reinterpret_cast<const TileItem*>(ws + g.t_sa_off);
+    L.num_tiles = g.n_sa;
+    L.pair_off = reinterpret_cast<const int32_t*>(ws + g.o_sa_off);
+    e = launch_ns_pair(OP_SYRK_A, L, g.p_sa, h->stages, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "second product launch");
+    // the X update, scaled by inv in iteration 1, with the weight update
+    // folded in on the last iteration where the weights allow it
+    const bool upd_regs = last && h->fuse_update == 1;
+    const bool upd_tma = last && h->fuse_update == 2 && g.w_tma;
+    L.first = first ? 1 : 0;
+    L.last = (upd_regs || upd_tma) ? 1 : 0;
+    L.tiles = reinterpret_cast<const TileItem*>(ws + g.t_g_off);
+    L.num_tiles = g.n_g;
+    L.pair_off = reinterpret_cast<const int32_t*>(ws + g.o_g_off);
+    const bool exports_on =
+        std::any_of(h->exp_w.begin(), h->exp_w.end(), [](float* q) { return q != nullptr; }) ||
+        std::any_of(h->exp_o.begin(), h->exp_o.end(), [](void* q) { return q != nullptr; });
+    if (upd_tma)
+        e = launch_ns_pair_update(L, g.p_g, exports_on, h->stream);
+    else
+        e = launch_ns_pair(OP_GEMM_BX, L, g.p_g, h->stages, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "X update launch");
+    h->dist_cur ^= 1;
+    h->dist_grams = 0;
+    if (last && !L.last) {
+        // the weight update as a pass of its own (fp32 or unaligned weights)
+        EwLaunch ew = dist_ew(h);
+        ew.lr = lr;
+        ew.src = h->dist_cur;
+        e = launch_ew_update(ew, dist_ew_grid(h), h->stream);
+        if (e != cudaSuccess) return cuda_fail(h, e, "update launch");
+    }
+    if (last) h->dist_ready = false;
+    return MUON_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1348,6 +1600,31 @@ int muon_step_host(muon_handle h, int n, const void* const* g_host, void* const*
             return fail(h, MUON_ERR_INVALID_ARG, "g_host[" + std::to_string(i) + "] is NULL");
     const HostIO io{g_host, w_host};
     return step_impl(h, lr, beta, nesterov, ns_steps, a, b, c, mode, nb, &io);
+}
+
+int muon_dist_configure(muon_handle h, int transposed, float shape_scale) {
+    if (!h) return MUON_ERR_INVALID_ARG;
+    if (!std::isfinite(shape_scale) || shape_scale < 1.f)
+        return fail(h, MUON_ERR_INVALID_ARG, "shape_scale must be finite and >= 1");
+    h->dist = true;
+    h->dist_transposed = transposed ? 1 : 0;
+    h->dist_scale = shape_scale;
+    h->dist_ready = false;
+    h->plan.valid = false;
+    return MUON_OK;
+}
+
+int muon_dist_momentum(muon_handle h, float beta, int nesterov, double* sumsq) {
+    return dist_momentum(h, beta, nesterov, sumsq);
+}
+
+int muon_dist_gram(muon_handle h, float* a, int64_t lda, int band_begin, int band_end) {
+    return dist_gram(h, a, lda, band_begin, band_end);
+}
+
+int muon_dist_update(muon_handle h, const float* a, int64_t lda, int first, int last,
+                     const double* sumsq_total, float lr, float ca, float cb, float cc) {
+    return dist_update(h, a, lda, first, last, sumsq_total, lr, ca, cb, cc);
 }
 
 int muon_sync(muon_handle h) {

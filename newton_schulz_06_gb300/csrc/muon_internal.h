@@ -153,6 +153,11 @@ struct NsLaunch {
     // weight update folded in (W read and written by TMA; no X' stored)
     int32_t chain_last;
     int32_t ep_x, ep_a, ep_b;
+    // Distributed mode across ranks, first product (FW == 3): the unscaled
+    // fp32 partial product goes to a32 (leading dimension lda32) instead of
+    // the bf16 A buffer.
+    float* a32;
+    int64_t lda32;
     // OP_CHAIN: the group's counter block (cnt_words words: a header of 64
     // words, word 0 counting the CTAs that have left the launch, then every
     // unit's tile_cnt block).  The last CTA to leave zeroes the block, so
@@ -191,6 +196,24 @@ struct EwLaunch {
     int32_t nesterov;
     float lr;
     int32_t src;             // X buffer holding the final iterate (update)
+    float eps;
+};
+
+// Distributed mode across ranks: the group's summed fp32 partial products
+// a32 (m x m, leading dimension lda32; tiles on or above the diagonal of the
+// 256 grid) into the bf16 A buffer a16 (leading dimension ld_mm) that the
+// second product reads, times scale = inv^2 in iteration 1, where inv =
+// 1 / (sqrt(*sumsq_total) + eps) is also stored to *inv_norm for the X
+// update.
+struct DistLaunch {
+    const float* a32;
+    int64_t lda32;
+    __nv_bfloat16* a16;
+    int64_t ld_mm;
+    int32_t m;
+    int32_t first;
+    const double* sumsq_total;
+    float* inv_norm;
     float eps;
 };
 
@@ -253,12 +276,18 @@ cudaError_t launch_ew_momentum(const EwLaunch& p, int grid, cudaStream_t s);
 constexpr int EWT_CTAS_PER_SM = 3;
 cudaError_t launch_ew_momentum_tma(const EwLaunch& p, int grid, bool g_f32, cudaStream_t s);
 cudaError_t launch_ew_norm(const EwLaunch& p, cudaStream_t s);
+// the group's single unit: its sum of squares (the norm pass's order) -> *out
+cudaError_t launch_ew_sumsq(const EwLaunch& p, double* out, cudaStream_t s);
+cudaError_t launch_dist_convert(const DistLaunch& p, int grid, cudaStream_t s);
 cudaError_t launch_ew_normalise(const EwLaunch& p, int grid, cudaStream_t s);
 cudaError_t launch_ew_update(const EwLaunch& p, int grid, cudaStream_t s);
 cudaError_t launch_ns(NsOp op, const NsLaunch& p, int grid, cudaStream_t s);
 size_t ns_smem_bytes();
 // CTA-pair (cta_group::2) kernels on 256 x 256 tiles; `pairs` clusters of 2.
 cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, int stages, cudaStream_t s);
+// First product of distributed mode across ranks: unscaled fp32 partial
+// product to p.a32 (tiles as in p.tiles, one stride over the pairs).
+cudaError_t launch_ns_pair_gram32(const NsLaunch& p, int pairs, cudaStream_t s);
 // Last GEMM with W <- W - lr*scale*O folded in (W blocks by TMA; bf16 W).
 cudaError_t launch_ns_pair_update(const NsLaunch& p, int pairs, bool exports, cudaStream_t s);
 int ns_pair_max_clusters();

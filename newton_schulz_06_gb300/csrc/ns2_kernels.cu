@@ -710,7 +710,8 @@ __device__ __forceinline__ TileCursor<OP> tile_cursor(const NsLaunch& p, int pai
 }
 
 // FW: the last X update with the weight update folded in through TMA-loaded
-// W blocks (1; 2 also writes the validation exports).
+// W blocks (1; 2 also writes the validation exports); for the first
+// product, 3 = distributed mode across ranks (fp32 partial product out).
 // SL: distributed mode's first product (K in p.shards slices, OP_SYRK_X).
 template <int OP, int P_STAGES, int FW, int SL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
@@ -1330,6 +1331,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                 if (OP != OP_CHAIN && op == OP_GEMM_BX && p.last) {   // a chain never holds the last
                     stage_free(lane);
                     gemm_update_block(u, r0w, gc0, lane, v, s_st + (st_seq & 1u) * P_BLK);
+                } else if (OP == OP_SYRK_X && FW == 3) {
+                    // distributed mode across ranks: this rank's fp32 partial
+                    // product, to be summed over the group before use
+                    const int row = r0w + lane;
+                    if (row < u.m) {
+                        float* dst = p.a32 + static_cast<int64_t>(row) * p.lda32 + gc0;
+                        const bool vec = gc0 + 32 <= u.m && (p.lda32 & 3) == 0 &&
+                                         (reinterpret_cast<uintptr_t>(p.a32) & 15) == 0;
+                        if (vec) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                *reinterpret_cast<float4*>(dst + 4 * q) =
+                                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (gc0 + e < u.m) dst[e] = v[e];
+                        }
+                    }
                 } else {
                     // every block as computed: X', and the symmetric
                     // products' tiles on or above the diagonal, where a
@@ -1458,6 +1478,10 @@ cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, int stages,
 
 // The last GEMM with the update folded in through TMA-loaded W blocks (one
 // input slot of X and W blocks, five pipeline stages).
+cudaError_t launch_ns_pair_gram32(const NsLaunch& p, int pairs, cudaStream_t s) {
+    return launch_pair_st<OP_SYRK_X, 6, 3>(p, pairs, s);
+}
+
 cudaError_t launch_ns_pair_update(const NsLaunch& p, int pairs, bool exports, cudaStream_t s) {
     return exports ? launch_pair_st<OP_GEMM_BX, 5, 2>(p, pairs, s)
                    : launch_pair_st<OP_GEMM_BX, 5, 1>(p, pairs, s);
