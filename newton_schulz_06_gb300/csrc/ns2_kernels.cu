@@ -807,6 +807,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                 if (cur.valid()) {
                     t_next = p.tiles[cur.it];
                     s_next = cur.s;
+                    // the next tile's operand maps, while this tile streams
+                    // (tiles of a grouped launch change matrix every time)
+                    if (t_next.unit != t.unit) {
+                        const NsUnit* Un = p.units + t_next.unit;
+                        const int opn = tile_op<OP>(t_next);
+                        const int srcn = tile_src<OP>(p, s_next);
+                        if (opn == OP_SYRK_X) {
+                            prefetch_tmap(&Un->tk_x[srcn]);
+                        } else if (opn == OP_SYRK_A) {
+                            prefetch_tmap(&Un->tk_a);
+                            prefetch_tmap(&Un->tm_a);
+                        } else {
+                            prefetch_tmap(&Un->tk_b);
+                            prefetch_tmap(&Un->tm_b);
+                            prefetch_tmap(&Un->tm_x[srcn]);
+                        }
+                    }
                 }
                 const NsUnit* U = p.units + t.unit;
                 const int op = tile_op<OP>(t);
@@ -1203,6 +1220,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
             if (has_next) {
                 t_next = p.tiles[tc.it];
                 s_next = tc.s;
+                // the next tile's output and input maps (one warp per CTA)
+                if (ew == 0 && lane == 0 && t_next.unit != t.unit) {
+                    const NsUnit* Un = p.units + t_next.unit;
+                    const int opn = tile_op<OP>(t_next);
+                    if (opn == OP_SYRK_X) {
+                        prefetch_tmap(&Un->te_a);
+                    } else if (opn == OP_SYRK_A) {
+                        prefetch_tmap(&Un->te_b);
+                        prefetch_tmap(&Un->te_a);
+                    } else {
+                        prefetch_tmap(&Un->te_x[tile_src<OP>(p, s_next) ^ 1]);
+                        if (FW || OP == OP_CHAIN) prefetch_tmap(&Un->te_w);
+                    }
+                }
             }
             if (OP == OP_CHAIN && cur.uses_in && cur.ready != 1) {
                 if (!input_ready(t, s_it, true)) {

@@ -162,6 +162,12 @@ __device__ __forceinline__ int32_t count_fetch_add(int32_t* cnt, int32_t n = 1) 
     return old;
 }
 
+// Brings a tensor map (in global memory) into the TMA unit's descriptor
+// cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 // Orders this thread's generic-proxy and async-proxy (TMA) accesses to
 // global memory with each other.
 __device__ __forceinline__ void fence_proxy_async_global() {
