@@ -1,6 +1,7 @@
 """The C ABI without a GPU: the library loads, exports every declared entry
 point, validates arguments, and its host planner counts tiles and FLOPs the
 way an independent enumeration does."""
+import ctypes
 import os
 import re
 
@@ -183,6 +184,44 @@ def test_distributed_mode_plan_and_validation(L):
     with pytest.raises(L.MuonError) as e:
         p.plan_info(L.MUON_DISTRIBUTED, 0)
     assert e.value.code == L.MUON_ERR_INVALID_ARG
+
+
+def test_distributed_ranks_slice_plan_and_validation(L):
+    """A rank's slice (muon_dist_configure) takes the whole matrix's
+    orientation: a 4096 x 2048 column slice of a 4096 x 8192 weight keeps
+    m = 4096 (its own shape would be transposed to m = 2048), so its plan
+    holds 4096^2 products.  Configuration and phases are checked before any
+    CUDA call; a host-only handle runs no phase, and a slice never runs
+    muon_step."""
+    lib = L.lib()
+    own = _planner([(4096, 2048)])
+    sl = _planner([(4096, 2048)])
+    assert lib.muon_dist_configure(sl._h, 0, 2.0) == 0
+    t_own = own.plan_info(L.MUON_FULL, 1)["syrk_tiles"]
+    t_sl = sl.plan_info(L.MUON_FULL, 1)["syrk_tiles"]
+    assert t_own == 8 * 9 // 2 and t_sl == 16 * 17 // 2, (t_own, t_sl)
+    assert sl.workspace_size()[1] > own.workspace_size()[1]
+    # the same slice as a block of a tall weight's rows: transposed, m = 2048
+    assert lib.muon_dist_configure(sl._h, 1, 2.0) == 0
+    assert sl.plan_info(L.MUON_FULL, 1)["syrk_tiles"] == t_own
+    assert lib.muon_dist_configure(sl._h, 0, 0.5) == L.MUON_ERR_INVALID_ARG
+    assert lib.muon_dist_configure(sl._h, 0, float("nan")) == L.MUON_ERR_INVALID_ARG
+    with pytest.raises(L.MuonError) as e:                  # slices run in full mode
+        sl.plan_info(L.MUON_BLOCKWISE, 2)
+    assert e.value.code == L.MUON_ERR_UNSUPPORTED
+    buf = ctypes.c_void_p(0x1000)
+    assert lib.muon_dist_momentum(sl._h, 0.95, 1, buf) == L.MUON_ERR_STATE
+    assert lib.muon_dist_gram(sl._h, buf, 4096, 0, -1) == L.MUON_ERR_STATE
+    assert lib.muon_dist_update(sl._h, buf, 4096, 1, 0, buf, 0.02, 1.0, 1.0, 1.0) == \
+        L.MUON_ERR_STATE
+    assert lib.muon_step(sl._h, 0.02, 0.95, 1, 5, 3.4, -4.7, 2.0, L.MUON_FULL, 1) == \
+        L.MUON_ERR_STATE
+    two = _planner([(256, 512), (256, 512)])
+    assert lib.muon_dist_configure(two._h, 0, 1.0) == 0
+    with pytest.raises(L.MuonError) as e:                  # one slice per handle
+        two.plan_info(L.MUON_FULL, 1)
+    assert e.value.code == L.MUON_ERR_UNSUPPORTED
+    assert lib.muon_dist_configure(None, 0, 1.0) == L.MUON_ERR_INVALID_ARG
 
 
 def test_chained_launch_only_for_few_large_matrices(L):

@@ -125,6 +125,16 @@ def test_virtual_ranks_are_the_one_gpu_distributed_mode_bitexact(shape, world, b
     assert relF(dW, want) <= 3e-2, relF(dW, want)
 
 
+def test_a_slice_handle_refuses_muon_step():
+    """A handle configured as a rank's slice steps only through the phases
+    (its norm and products need the group's sums)."""
+    W, G, M = case(256, 512, 5310)
+    eng = SliceEngine(W, G, M, transposed=False, shape_scale=1.0)
+    with pytest.raises(Exception):
+        eng._opt.step(**KW)
+    eng.close()
+
+
 def test_phases_out_of_order_are_refused():
     W, G, M = case(256, 512, 5300)
     eng = SliceEngine(W, G, M, transposed=False, shape_scale=1.0)
