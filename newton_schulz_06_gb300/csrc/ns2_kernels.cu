@@ -45,7 +45,8 @@
 // "SYRK and fused all-reduce": upper-triangle tiles, diagonal tiles in
 // full) and store them as computed; nothing below the diagonal tiles is
 // written.  Consumers read the k-blocks left of an operand's diagonal tile
-// from the stored transpose.
+// from the stored transpose.  On a diagonal tile both operands are the same
+// rows, so its K-major k-blocks are loaded once and read as A and as B.
 //
 // Every wait is bounded as in the single-CTA kernels.
 #include "../../include/muon.h"
@@ -61,6 +62,8 @@ constexpr int P_HALF = 128;                        // rows per CTA
 constexpr int P_A_BYTES = P_HALF * BK * 2;         // 16 KB
 constexpr int P_B_BYTES = P_HALF * BK * 2;         // 16 KB
 constexpr int P_BOX = 64 * 64 * 2;                 // one {64,64} box
+// a diagonal tile's B descriptor steps through A's stages with B's stride
+static_assert(P_A_BYTES == P_B_BYTES, "A and B stages of one size");
 // K-major operands (A of every product, B of the symmetric ones) come in as
 // one {64, 128} box per CTA and k-block rather than two {64, 64} boxes
 constexpr bool P_WIDE_BOX = true;
@@ -849,7 +852,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                 // N = n_len columns split evenly over the pair (64 or 128 each)
                 const int hb = t.n_len >> 1;
                 const int b0 = t.tj * 256 + t.n_off + static_cast<int>(rank) * hb;
-                const uint32_t tx_bytes = 2u * (P_A_BYTES + hb * BK * 2);
+                // a symmetric product's diagonal tile: each CTA's half of B
+                // is its own rows of A, so A's stage serves as both operands
+                // (K-major k-blocks only: with both operands MN-major from
+                // one buffer the second product ran 5% slower on GB300)
+                const bool same = op != OP_GEMM_BX && t.ti == t.tj && t.n_off == 0;
+                const uint32_t tx_mn = 2u * (P_A_BYTES + hb * BK * 2);
+                const uint32_t tx_bytes = same ? 2u * P_A_BYTES : tx_mn;
                 if (P_WIDE_BOX && op != OP_GEMM_BX && hb != 128) {
                     // a K-major B half is one 128-row box: full-width tiles only
                     atomicCAS(p.err, 0, DEV_ERR_BAD_TILE);
@@ -892,7 +901,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                         break;
                     }
                     const uint32_t fb_local = smem_u32(&full_bar[stage]);
-                    if (rank == 0) mbar_expect_tx(fb_local, tx_bytes);
+                    if (rank == 0) mbar_expect_tx(fb_local, tx_mn);
                     const uint32_t fb = map_to_rank(fb_local, 0);
                     const uint32_t a_dst = smem_u32(sA + stage * P_A_BYTES);
                     const uint32_t b_dst = smem_u32(sB + stage * P_B_BYTES);
@@ -950,7 +959,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                     if (op == OP_GEMM_BX) {
                         tma_load_2d_pair(b_dst, tmB, fb, b0, k0);
                         if (hb > 64) tma_load_2d_pair(b_dst + P_BOX, tmB, fb, b0 + 64, k0);
-                    } else {
+                    } else if (!same) {
                         tma_load_2d_pair(b_dst, tmB, fb, k0, b0);
                         if (!P_WIDE_BOX && hb > 64)
                             tma_load_2d_pair(b_dst + P_BOX, tmB, fb, k0, b0 + 64);
@@ -996,7 +1005,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(p_threads<OP>(), 1)
                 if (cur.valid()) t_next = p.tiles[cur.it];
                 const int op = tile_op<OP>(t);
                 const uint32_t idesc = instr_desc(256, t.n_len, op == OP_GEMM_BX ? 1 : 0);
-                const uint64_t b_desc0 = (op == OP_GEMM_BX) ? b_desc_mn : b_desc_k;
+                // a symmetric product's diagonal tile reads B from A's stage
+                // in its K-major k-blocks
+                const bool same = op != OP_GEMM_BX && t.ti == t.tj && t.n_off == 0;
+                const uint64_t b_desc0 = (op == OP_GEMM_BX) ? b_desc_mn : same ? a_desc0 : b_desc_k;
                 const uint32_t b_kstep = (op == OP_GEMM_BX) ? (2048 >> 4) : (32 >> 4);
                 const int kblocks = t.k_blocks;
                 const int kslice = sliced ? kblocks / p.shards : kblocks;
