@@ -292,9 +292,7 @@ struct EwtCfg {
     static constexpr int G_BYTES = EW_TILE * EW_TILE * GB;
     static constexpr int STAGE = M_BYTES + G_BYTES;
     static constexpr int S = NS;
-    static constexpr int UNIT = static_cast<int>(sizeof(EwUnit));
-    static constexpr int SMEM = S * STAGE + S * UNIT + 2 * (EW_THREADS / 32) * 4 + S * 8 + 128;
-    static_assert(UNIT % 16 == 0 && STAGE % 16 == 0, "bulk-copy alignment");
+    static constexpr int SMEM = S * STAGE + 2 * (EW_THREADS / 32) * 4 + S * 8 + 128;
 };
 
 template <int GB, int NS, int CPS>
@@ -304,11 +302,7 @@ ew_momentum_tma_kernel(const EwLaunch p) {
     extern __shared__ uint8_t ewt_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(ewt_raw) + 127) & ~uintptr_t(127));
-    // each stage's tile comes with its unit's record (one bulk copy on the
-    // stage's barrier), so the threads read the unit's fields from shared
-    // memory instead of waiting on a global load whenever the unit changes
-    uint8_t* uslot = smem + C::S * C::STAGE;
-    float* red = reinterpret_cast<float*>(uslot + C::S * C::UNIT);
+    float* red = reinterpret_cast<float*>(smem + C::S * C::STAGE);
     uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * (EW_THREADS / 32));
     __shared__ int abort_flag;
     const int i = threadIdx.x >> 4;          // 0..15
@@ -339,26 +333,27 @@ ew_momentum_tma_kernel(const EwLaunch p) {
         uint8_t* dst = smem + st * C::STAGE;
         const uint32_t bar = ptx::smem_u32(&full[st]);
         ptx::fence_proxy_async_smem();       // earlier reads of the stage first
-        ptx::mbar_expect_tx(bar, C::M_BYTES + C::UNIT + EW_TILE * EW_TILE *
+        ptx::mbar_expect_tx(bar, C::M_BYTES + EW_TILE * EW_TILE *
                                      (U.g_dtype == MUON_F32 ? 4 : 2));
         ptx::tma_load_2d(ptx::smem_u32(dst), &p.maps[pu].m, bar, wc0, wr0);
         ptx::tma_load_2d(ptx::smem_u32(dst + C::M_BYTES), &p.maps[pu].g, bar, wc0, wr0);
-        ptx::bulk_load(ptx::smem_u32(uslot + st * C::UNIT), p.units + pu, C::UNIT, bar);
     };
     if (threadIdx.x == 0)
         for (int64_t j = 0; j < C::S - 1 && j < nj; ++j) issue(j);
+    int u = nj ? find_unit(p.tile_base, p.num_units, blockIdx.x) : 0;
+    EwU U = load_ewu(p.units + u);
     int parity = 0;
     int64_t j = 0;
     for (; j < nj; ++j, parity ^= 1) {
         const int64_t t = blockIdx.x + j * gridDim.x;
         if (threadIdx.x == 0 && j + C::S - 1 < nj) issue(j + C::S - 1);
+        while (t >= U.tile_end) U = load_ewu(p.units + (++u));
+        const TileGeom g = geom_of(U, t);
         const int st = static_cast<int>(j % C::S);
         const uint32_t ph = static_cast<uint32_t>((j / C::S) & 1);
         if (!ptx::wait_bounded(ptx::smem_u32(&full[st]), ph, &abort_flag, p.err,
                                p.wait_limit_ns))
             break;
-        const EwU U = load_ewu(reinterpret_cast<const EwUnit*>(uslot + st * C::UNIT));
-        const TileGeom g = geom_of(U, t);
         const float* sm = reinterpret_cast<const float*>(smem + st * C::STAGE);
         const uint8_t* sg = smem + st * C::STAGE + C::M_BYTES;
         const bool interior =

@@ -31,9 +31,7 @@ constexpr int DEV_ERR_BAD_TILE = 2;
 // matrix (blockwise mode), seen by the element-wise stages.  All pointers are
 // already offset to the unit's first element.  X is the unit oriented short
 // side first: m x n with m = min(rows, cols); if `transposed`, X = W-block^T.
-// A multiple of 16 bytes, so that a bulk copy can bring one into shared
-// memory.
-struct alignas(16) EwUnit {
+struct EwUnit {
     void* w;
     const void* g;
     float* mom;

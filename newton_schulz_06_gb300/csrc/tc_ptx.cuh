@@ -191,16 +191,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
-// Untiled bulk copy of `bytes` from global to this CTA's shared memory,
-// counted on `bar` (both addresses 16-byte aligned, bytes a multiple of 16).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
 // TMA load into this CTA's shared memory whose completion is counted on a
 // barrier that may live in the peer CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
