@@ -436,7 +436,7 @@ def e2e_leg(wl, args, t, dev, pg, useful):
             "unit": "TFLOP/s", "ms_per_step": e2e,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "path": ("muon_step_host: G from pinned host memory, the step, W back; "
-                     "groups of about 1/8 of the set, copies on two streams overlapping "
+                     "groups of about 1/16 of the set, copies on two streams overlapping "
                      "other groups' compute"),
             "matrices": e2e_n if e2e_n < len(Gs) else "all"}
 

@@ -162,7 +162,7 @@ MUON_API int muon_step(muon_handle h, float lr, float beta, int nesterov, int ns
  * pinned (page-locked) for the copies to run asynchronously.  The caller
  * owns them.  Errors as muon_step; a failed copy is MUON_ERR_CUDA.
  * The copies overlap the compute: the step runs in groups of whole matrices
- * (about 1/8 of the registered elements each, at least 32 M elements), a
+ * (about 1/16 of the registered elements each, at least 32 M elements), a
  * group's gradients are copied in on a second stream while earlier groups
  * compute, and its weights go out on a third stream once its update is
  * done; the handle's stream waits for all of them.  The first call builds
