@@ -1,7 +1,7 @@
 """Benchmark of the Muon optimizer step (libmuon on one GB300 per rank).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-cpu-baseline]
+                    [--workload NAME] [--no-cpu-baseline] [--no-cublas-side]
 
 A step is one full Muon step (momentum, normalisation, five Newton-Schulz
 iterations, weight update) over every matrix of the workload, with a fresh
@@ -14,6 +14,8 @@ on their upper triangle); GEMM-equivalent TFLOP/s, % of the measured dense
 bf16 peak, ms/step and matrices/s are reported beside it.  L2 is flushed
 before every timed step (a 512 MiB write, then a 512 MiB read that carries
 the write's dirty lines out before the step begins).  Prints one JSON line on rank 0.
+"cublas_side" times the same step written with torch operations (cuBLAS
+batched matmuls) on the same workload, as a side comparison.
 
 With N > 1 (torchrun) every rank runs the whole workload on its own GPU as an
 independent replica (weak scaling); value = all ranks' FLOPs / the slowest
@@ -441,6 +443,75 @@ def e2e_leg(wl, args, t, dev, pg, useful):
             "matrices": e2e_n if e2e_n < len(Gs) else "all"}
 
 
+# the side comparison stacks each shape's W, G and M (about 30 B per element
+# with its temporaries): up to the Kimi-K2 layer, not the 48-layer set
+CUBLAS_SIDE_MAX_ELEMENTS = 4 << 30
+
+
+def cublas_side(wl, args, dev, useful, ours_ms):
+    """The same Muon step written with torch operations, timed like the
+    libmuon step (L2 flushed before each step, CUDA events on the stream): a
+    side comparison of what the fused kernels replace, not a path of the
+    library (none of its kernels run here).  Matrices of one shape are
+    stacked; every product is a cuBLAS bf16 batched matmul with fp32
+    accumulation, the symmetric ones computed in full, b*A + c*A*A and
+    a*X + B*X folded into the matmuls (baddbmm); momentum, norm and update
+    are separate element-wise kernels.  Full mode only, and only for
+    workloads whose stacked state fits beside the bench's own."""
+    import torch
+    from newton_schulz_06_gb300 import inputs as I
+    from newton_schulz_06_gb300.muon import DEFAULT_COEFFS
+    if args.no_cublas_side or wl.mode != "full" or wl.n_elements > CUBLAS_SIDE_MAX_ELEMENTS:
+        return None
+    Ws, Gs, Ms = I.make_state(wl, dev)
+    by_shape = {}
+    for i, shape in enumerate(wl.shapes):
+        by_shape.setdefault(tuple(shape), []).append(i)
+    sets = []
+    for (r, c), idx in by_shape.items():
+        sets.append((r, c, torch.stack([Ws[i] for i in idx]), torch.stack([Gs[i] for i in idx]),
+                     torch.stack([Ms[i] for i in idx])))
+    del Ws, Gs, Ms
+    a, b, c3 = DEFAULT_COEFFS
+    beta, lr, eps = 0.95, 0.02, 1e-7
+
+    def step():
+        for r, c, W, G, M in sets:
+            M.mul_(beta).add_(G)
+            U = torch.add(G, M, alpha=beta)                  # Nesterov
+            X = U.transpose(1, 2) if r > c else U
+            inv = 1.0 / (torch.linalg.vector_norm(X, dim=(1, 2), keepdim=True) + eps)
+            X = (X * inv).to(torch.bfloat16)
+            for _ in range(5):
+                A = torch.bmm(X, X.transpose(1, 2))
+                B = torch.baddbmm(A, A, A, beta=b, alpha=c3)
+                X = torch.baddbmm(X, B, X, beta=a, alpha=1.0)
+            O = X.transpose(1, 2) if r > c else X
+            W.add_(O, alpha=-lr * max(1.0, r / c) ** 0.5)
+
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(min(args.steps, 10))]
+    for e0, e1 in ev:
+        flush()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    del sets, flush
+    torch.cuda.empty_cache()
+    return {"ms_per_step": ms, "useful_tflops": useful / (ms / 1e3) / 1e12,
+            "libmuon_speedup": ms / ours_ms, "steps": len(ev),
+            "what": ("the same step in torch ops: cuBLAS bf16 batched matmuls (fp32 "
+                     "accumulation), symmetric products in full, matrices of one shape "
+                     "stacked; a side comparison, not a path of the library")}
+
+
 def run_ours(args, wl, world, rank, local, pg):
     import torch
     import __graft_entry__
@@ -470,6 +541,8 @@ def run_ours(args, wl, world, rank, local, pg):
     prof_ms, wall, launches = t["prof_ms"], t["wall"], t["launches"]
     opt.close()
     del opt, trips, t
+    torch.cuda.empty_cache()
+    side = cublas_side(wl, args, dev, useful, ms) if world == 1 else None
 
     # further workloads timed in the same run (the target configs besides
     # the headline one), each with its own state, freed before the next
@@ -500,6 +573,9 @@ def run_ours(args, wl, world, rank, local, pg):
         xt["opt"].close()
         del xt
         torch.cuda.empty_cache()
+        xs = cublas_side(xw, args, dev, xu, xms) if world == 1 else None
+        if xs:
+            extra[name]["cublas_side"] = xs
     clocks = sampler.stop()
 
     value = world * useful / (ms / 1e3) / 1e12
@@ -529,6 +605,8 @@ def run_ours(args, wl, world, rank, local, pg):
         "gpu_launches": launches,
         "roofline": roofline,
     }
+    if side:
+        line["cublas_side"] = side
     if extra:
         line["workloads"] = extra
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -554,6 +632,8 @@ def main():
     ap.add_argument("--workload", default="square_4096_bf16")
     ap.add_argument("--max-workspace", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cublas-side", action="store_true",
+                    help="skip the side comparison with the step in torch/cuBLAS ops")
     ap.add_argument("--extra-workloads", default="qwen3_30b_a3b_block",
                     help="comma-separated workloads also timed in the same run "
                          "and reported under 'workloads' ('none': skip)")
