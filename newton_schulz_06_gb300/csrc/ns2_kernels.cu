@@ -10,8 +10,9 @@
 // 48 KB of operands per 512 cycles, and four 48 KB stages do not cover the
 // TMA round trip under load.  In a pair each CTA stages only its 128 rows of
 // A and its half (128 rows or columns) of B, 32 KB per k-block, so five
-// stages fit in shared memory beside the epilogue's buffers and the L2-to-SM
-// traffic per FLOP drops by a third.  The even CTA of the pair (the leader) issues
+// stages fit in shared memory beside the epilogue's buffers (six where the
+// epilogue reads no input) and the L2-to-SM traffic per FLOP drops by a
+// third.  The even CTA of the pair (the leader) issues
 // tcgen05.mma.cta_group::2 with M = 256, N = 256: rows 0-127 of A and the
 // first half of B come from its shared memory, rows 128-255 and the second
 // half of B from the peer's, and each CTA's TMEM receives its own 128 rows of
@@ -1519,12 +1520,14 @@ cudaError_t launch_ns_pair(NsOp op, const NsLaunch& p, int pairs, int stages,
     return cudaErrorInvalidValue;
 }
 
-// The last GEMM with the update folded in through TMA-loaded W blocks (one
-// input slot of X and W blocks, five pipeline stages).
+// Distributed mode across ranks: the first product's unscaled fp32 partial
+// (its epilogue reads no input, so six pipeline stages).
 cudaError_t launch_ns_pair_gram32(const NsLaunch& p, int pairs, cudaStream_t s) {
     return launch_pair_st<OP_SYRK_X, 6, 3>(p, pairs, s);
 }
 
+// The last GEMM with the update folded in through TMA-loaded W blocks (W
+// blocks in the epilogue's input slots, five pipeline stages).
 cudaError_t launch_ns_pair_update(const NsLaunch& p, int pairs, bool exports, cudaStream_t s) {
     return exports ? launch_pair_st<OP_GEMM_BX, 5, 2>(p, pairs, s)
                    : launch_pair_st<OP_GEMM_BX, 5, 1>(p, pairs, s);
