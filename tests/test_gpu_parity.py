@@ -223,22 +223,27 @@ def test_distributed_mode_reproducible_and_standalone_bitexact():
     assert torch.equal(o1[1], o3[0]) and torch.equal(trips[1][0], alone[0])
 
 
-def test_step_with_host_buffers_matches_device_step_bitexact():
+@pytest.mark.parametrize("mode,nb,shapes", [
+    ("full", 1, [(256, 640), (640, 256), (300, 300)]),
+    ("blockwise", 4, [(256, 640), (640, 256), (300, 300)]),
+    ("distributed", 2, [(256, 640), (640, 256), (384, 512)])])
+def test_step_with_host_buffers_matches_device_step_bitexact(mode, nb, shapes):
     """muon_step_host: gradients in from pinned host memory, weights back out,
-    gives the same bits as copying G in and W out around muon_step."""
-    shapes = [(256, 640), (640, 256), (300, 300)]
+    gives the same bits as copying G in and W out around muon_step, in each
+    mode."""
     trips = [case(r, c, 700 + i) for i, (r, c) in enumerate(shapes)]
     clones = [[t.clone() for t in tr] for tr in trips]
     g_host = [torch.randn(r, c, generator=torch.Generator().manual_seed(710 + i)
                           ).to(torch.bfloat16).pin_memory() for i, (r, c) in enumerate(shapes)]
     w_host = [torch.empty(r, c, dtype=torch.bfloat16).pin_memory() for r, c in shapes]
+    md = mode_code(mode)
     opt = Muon(trips)
-    opt.step_host(g_host, w_host)
+    opt.step_host(g_host, w_host, mode=md, nb=nb)
     opt.sync()
     ref = Muon(clones)
     for (W, G, M), g in zip(clones, g_host):
         G.copy_(g)
-    ref.step()
+    ref.step(mode=md, nb=nb)
     ref.sync()
     torch.cuda.synchronize()
     for i in range(len(shapes)):
