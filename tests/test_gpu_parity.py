@@ -273,12 +273,13 @@ def test_layerwise_single_rank_is_the_grouped_step_bitexact():
         assert torch.equal(trips[i][2], lw.momentum[i]), shapes[i]
 
 
-@pytest.mark.parametrize("ns_steps", [1, 2, 5])
+@pytest.mark.parametrize("ns_steps", [1, 2, 5, 64])
 def test_chained_launch_bitexact(ns_steps, monkeypatch):
     """One launch holding every product of the step but the last X update
     (tiles waiting on row-block counters) computes every tile as the
     separate launches do: identical bits, over two steps (the counters carry
-    across launches and steps)."""
+    across launches and steps), up to the largest iteration count the ABI
+    accepts (64: counter targets of 16 x 64 rounds)."""
     monkeypatch.setenv("MUON_CHAIN_MIN_TILES", "0")     # small shapes chain too
     shapes = [(512, 768), (768, 2048), (300, 300), (2048, 640), (96, 1000)]
     trips = [case(r, c, 900 + i) for i, (r, c) in enumerate(shapes)]
