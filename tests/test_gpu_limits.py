@@ -123,3 +123,25 @@ def test_largest_short_side_block_diagonal():
         assert eo <= O_TOL and ew <= W_TOL, (k, eo, ew)
     print("32768^2 block-diagonal", errs)
     opt.close()
+
+
+def test_many_tiny_matrices_in_one_group():
+    """5000 matrices of 1 to 96 rows and columns, every one its own unit in
+    one grouped step (tables of thousands of units, tiles that are mostly
+    edge): a sample against the oracle, and a sample stepped alone gives the
+    same bits as inside the group."""
+    gen = np.random.default_rng(5000)
+    shapes = [tuple(int(x) for x in gen.integers(1, 97, size=2)) for _ in range(5000)]
+    trips = [list(I.random_case(r, c, 3000 + i, device=DEV)) for i, (r, c) in enumerate(shapes)]
+    sample = sorted(int(i) for i in gen.choice(len(shapes), 12, replace=False))
+    clones = {i: [t.clone() for t in trips[i]] for i in sample}
+    inp, wexp, oexp, opt = gpu_step(trips)
+    assert opt.plan_info()["units"] == len(shapes)
+    for i in sample:
+        ref = oracle_step(inp[i])
+        check_against_oracle(trips[i], inp[i], wexp[i], oexp[i], ref, w_gate="scaled")
+        _, _, o1, opt1 = gpu_step([clones[i]])
+        assert torch.equal(o1[0], oexp[i]), shapes[i]
+        assert torch.equal(clones[i][0], trips[i][0]), shapes[i]
+        opt1.close()
+    opt.close()
