@@ -597,6 +597,15 @@ def run_ours(args, wl, world, rank, local, pg):
         "matrices_per_s": world * wl.n_matrices / (ms / 1e3),
         "useful_tflop_per_step": useful / 1e12,
         "gemm_equiv_tflop_per_step": gemm_eq / 1e12,
+        # the plan's tiles per iteration (256 x 256 tiles on CTA pairs) and
+        # the FLOPs the tensor cores execute (diagonal tiles whole, edge
+        # tiles padded) over the useful ones
+        "plan": {"units": info["units"], "groups": info["groups"],
+                 "symmetric_product_tiles": info["syrk_tiles"],
+                 "x_update_tiles": info["gemm_tiles"],
+                 "elementwise_tiles": info["ew_tiles"],
+                 "chained_groups": info["chained_groups"],
+                 "executed_over_useful_flops": info["executed_flops"] / max(1, info["useful_flops"])},
         "stage_ms_per_step": {k: v[0] / args.steps for k, v in stage_tot.items()},
         "ms_per_step_with_stage_events": statistics.mean(prof_ms),
         "wall_s_timed_region": wall,
