@@ -273,7 +273,7 @@ cudaError_t launch_ew_momentum(const EwLaunch& p, int grid, cudaStream_t s);
 // The TMA-fed momentum pass (p.maps set): persistent grid of `grid` CTAs,
 // EWT_CTAS_PER_SM per SM; g_f32: some unit's gradient is fp32 (larger ring
 // stages).
-constexpr int EWT_CTAS_PER_SM = 3;
+constexpr int EWT_CTAS_PER_SM = 2;
 cudaError_t launch_ew_momentum_tma(const EwLaunch& p, int grid, bool g_f32, cudaStream_t s);
 cudaError_t launch_ew_norm(const EwLaunch& p, cudaStream_t s);
 // the group's single unit: its sum of squares (the norm pass's order) -> *out
