@@ -33,7 +33,14 @@ def test_traffic_record_goes_stale_when_a_source_changes(tmp_path, monkeypatch):
     for d in ("profiles", os.path.join("newton_schulz_06_gb300", "csrc")):
         shutil.copytree(os.path.join(ROOT, d), tmp_path / d)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.traffic_for("ns2_kernel<3>", "square_4096_bf16") is not None
+    # as if just captured on these sources
+    rec_path = tmp_path / "profiles" / "traffic.json"
+    recs = json.loads(rec_path.read_text())
+    ent = recs["ns2_kernel<3>@square_4096_bf16"]
+    ent["source_sha"] = bench.source_sha(ent["source_files"])
+    rec_path.write_text(json.dumps(recs))
+    assert bench.traffic_for("ns2_kernel<3>", "square_4096_bf16") == \
+        ent["bytes_per_launch_full_workload"]
     src = tmp_path / "newton_schulz_06_gb300" / "csrc" / "ns2_kernels.cu"
     src.write_text(src.read_text() + "\n// edited\n")
     assert bench.traffic_for("ns2_kernel<3>", "square_4096_bf16") is None
