@@ -532,3 +532,38 @@ def test_pipelined_host_step_matches_device_step_bitexact():
             assert torch.equal(trips[i][2], clones[i][2]), (step, shapes[i])
     opt.close()
     ref.close()
+
+
+@pytest.mark.parametrize("pad,offset", [(64, 0), (40, 3)])
+def test_padded_and_offset_layouts_bitexact(pad, offset):
+    """W, G and M as column views of wider buffers (leading dimension
+    cols + pad, first column `offset`): the same bits as contiguous tensors,
+    and nothing written outside the views (the padding keeps its sentinel).
+    offset 3 leaves every row start unaligned, which rules out the TMA and
+    16-byte paths; pad 64 keeps them."""
+    shapes = [(256, 640), (640, 256), (300, 300), (768, 2048)]
+    ref = [case(r, c, 1400 + i) for i, (r, c) in enumerate(shapes)]
+    bigs, views = [], []
+    for (W, G, M) in ref:
+        r, c = W.shape
+        trip_big, trip_view = [], []
+        for t in (W, G, M):
+            big = torch.full((r, c + pad), 7.0, dtype=t.dtype, device=DEV)
+            v = big[:, offset:offset + c]
+            v.copy_(t)
+            trip_big.append(big)
+            trip_view.append(v)
+        bigs.append(trip_big)
+        views.append(trip_view)
+    for _ in range(2):
+        gpu_step(ref, exports=False)
+        gpu_step(views, exports=False)
+    torch.cuda.synchronize()
+    for i in range(len(shapes)):
+        for k in (0, 2):                               # W and M
+            assert torch.equal(views[i][k], ref[i][k]), (shapes[i], k)
+        c = shapes[i][1]
+        for big in bigs[i]:
+            keep = torch.ones(big.shape[1], dtype=torch.bool, device=DEV)
+            keep[offset:offset + c] = False
+            assert bool((big[:, keep] == 7.0).all()), shapes[i]
