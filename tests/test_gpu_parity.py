@@ -534,14 +534,19 @@ def test_pipelined_host_step_matches_device_step_bitexact():
     ref.close()
 
 
-@pytest.mark.parametrize("pad,offset", [(64, 0), (40, 3)])
-def test_padded_and_offset_layouts_bitexact(pad, offset):
+@pytest.mark.parametrize("pad,offset,chained", [(64, 0, False), (40, 3, False),
+                                                (64, 0, True), (40, 3, True)])
+def test_padded_and_offset_layouts_bitexact(pad, offset, chained, monkeypatch):
     """W, G and M as column views of wider buffers (leading dimension
     cols + pad, first column `offset`): the same bits as contiguous tensors,
     and nothing written outside the views (the padding keeps its sentinel).
     offset 3 leaves every row start unaligned, which rules out the TMA and
-    16-byte paths; pad 64 keeps them."""
+    16-byte paths; pad 64 keeps them.  Separate launches over a mixed group,
+    and a chained launch over one matrix."""
     shapes = [(256, 640), (640, 256), (300, 300), (768, 2048)]
+    if chained:
+        monkeypatch.setenv("MUON_CHAIN_MIN_TILES", "0")
+        shapes = [(1024, 2048)]
     ref = [case(r, c, 1400 + i) for i, (r, c) in enumerate(shapes)]
     bigs, views = [], []
     for (W, G, M) in ref:
@@ -557,7 +562,8 @@ def test_padded_and_offset_layouts_bitexact(pad, offset):
         views.append(trip_view)
     for _ in range(2):
         gpu_step(ref, exports=False)
-        gpu_step(views, exports=False)
+        *_, opt = gpu_step(views, exports=False)
+        assert opt.plan_info()["chained_groups"] == (1 if chained else 0)
     torch.cuda.synchronize()
     for i in range(len(shapes)):
         for k in (0, 2):                               # W and M
