@@ -85,8 +85,11 @@ def test_groups_from_a_small_workspace_bitexact():
 
 
 @pytest.mark.parametrize("rows,cols,nb", [(256, 1024, 4), (1024, 512, 4),
-                                          (300, 600, 3), (128, 2048, 8)])
+                                          (300, 600, 3), (128, 2048, 8),
+                                          (256, 606, 3), (606, 300, 2)])
 def test_blockwise_matches_oracle(rows, cols, nb):
+    """Blockwise mode against the oracle's; 202- and 150-column blocks start
+    at unaligned addresses (no 16-byte or TMA access to W, G, M there)."""
     trip = case(rows, cols, 40)
     inp, wexp, oexp, _ = gpu_step([trip], mode="blockwise", nb=nb)
     ref = oracle_step(inp[0], mode="blockwise", nb=nb)
